@@ -1,0 +1,26 @@
+"""CLiS (Certified Loop-invariant Stabilization) attention forward for GB300.
+
+The compute lives in ``libclis.so`` (CUDA for sm_103a, C ABI declared in
+``include/clis.h``).  :mod:`certified_fixed_stabilizer_gb300.clis` is the thin
+ctypes binding with the same function names; it is imported on first use so
+that ``workloads`` can be used on machines without the built library.  Using
+any binding name without the built library raises an error: there is no CPU
+fallback.
+"""
+from __future__ import annotations
+
+import importlib
+
+_BINDING_NAMES = {
+    "clis_certify", "clis_certify_workspace_size", "clis_attn_fwd",
+    "clis_status_string", "clis_get_device_error", "clis_clear_device_error",
+    "ClisError", "attention", "certify", "Cert", "VARIANT", "FMT",
+    "library_path", "load_library",
+}
+
+
+def __getattr__(name):
+    if name in _BINDING_NAMES:
+        mod = importlib.import_module(".clis", __name__)
+        return getattr(mod, name)
+    raise AttributeError(name)
