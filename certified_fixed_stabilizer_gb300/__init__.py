@@ -14,8 +14,9 @@ import importlib
 _BINDING_NAMES = {
     "clis_certify", "clis_certify_workspace_size", "clis_attn_fwd",
     "clis_status_string", "clis_get_device_error", "clis_clear_device_error",
-    "ClisError", "attention", "certify", "Cert", "VARIANT", "FMT",
-    "library_path", "load_library",
+    "ClisError", "attention", "certify", "Cert", "VARIANT", "FMT", "STATUS",
+    "library_path", "load_library", "decode_certs", "make_shape", "scale_log2_for",
+    "Shape", "CERT_WORDS", "LOG2E",
 }
 
 

@@ -1,0 +1,220 @@
+"""ctypes binding of libclis.so -- argument marshalling only.
+
+Function names match the C ABI in ``include/clis.h``.  Tensors are torch
+tensors used purely as device (or pinned host) memory; every step of the
+computation runs in the library's CUDA kernels.  If the library is missing,
+importing this module raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from . import build as _build
+
+LOG2E = 1.4426950408889634
+
+FMT = {"fp16": 0, "bf16": 1, "fp32": 2}
+VARIANT = {"auto": 0, "online": 1, "certified": 2}
+STATUS = {0: "CLIS_OK", 1: "CLIS_ERR_INVALID_ARG", 2: "CLIS_ERR_UNSUPPORTED", 3: "CLIS_ERR_MISALIGNED",
+          4: "CLIS_ERR_WORKSPACE", 5: "CLIS_ERR_CUDA", 6: "CLIS_ERR_TIMEOUT"}
+
+
+class ClisError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)} ({clis_status_string(status)})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "B", "H", "Nq", "Nk", "d",
+        "q_sb", "q_sh", "q_sn", "k_sb", "k_sh", "k_sn",
+        "v_sb", "v_sh", "v_sn", "o_sb", "o_sh", "o_sn")]
+
+
+class Cert(ctypes.Structure):
+    _fields_ = [("certified", ctypes.c_int32), ("G", ctypes.c_int32), ("A", ctypes.c_int32),
+                ("C", ctypes.c_int32), ("reason", ctypes.c_int32), ("B_h", ctypes.c_float),
+                ("kappa", ctypes.c_float), ("qmax", ctypes.c_float)]
+
+
+CERT_WORDS = ctypes.sizeof(Cert) // 4  # a certificate is 8 32-bit words
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library():
+    """Load libclis.so (building it first when nvcc is available and it is stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path) or _build._stale():
+        _build.build()
+    lib = ctypes.CDLL(path)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    sp = ctypes.POINTER(Shape)
+    lib.clis_certify_workspace_size.argtypes = [sp, ctypes.POINTER(sz)]
+    lib.clis_certify_workspace_size.restype = i32
+    lib.clis_certify.argtypes = [sp, vp, vp, vp, f32, i32, i32, vp, vp, vp, sz, vp]
+    lib.clis_certify.restype = i32
+    lib.clis_attn_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp]
+    lib.clis_attn_fwd.restype = i32
+    lib.clis_status_string.argtypes = [i32]
+    lib.clis_status_string.restype = ctypes.c_char_p
+    lib.clis_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.clis_get_device_error.restype = i32
+    lib.clis_clear_device_error.argtypes = []
+    lib.clis_clear_device_error.restype = i32
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_shape(q, k, v, o=None) -> Shape:
+    """Shape and element strides of [B, H, N, d] tensors (d must be contiguous)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        if t is None:
+            continue
+        if t.dim() != 4 or t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be a 4-D bfloat16 tensor [B, H, N, d]")
+        if t.stride(-1) != 1:
+            raise ValueError(f"{name} must have a contiguous last dimension")
+    B, H, Nq, d = q.shape
+    s = Shape(B=B, H=H, Nq=Nq, Nk=k.shape[2], d=d,
+              q_sb=q.stride(0), q_sh=q.stride(1), q_sn=q.stride(2),
+              k_sb=k.stride(0), k_sh=k.stride(1), k_sn=k.stride(2),
+              v_sb=v.stride(0), v_sh=v.stride(1), v_sn=v.stride(2))
+    if o is not None:
+        s.o_sb, s.o_sh, s.o_sn = o.stride(0), o.stride(1), o.stride(2)
+    return s
+
+
+def clis_status_string(status: int) -> str:
+    return load_library().clis_status_string(int(status)).decode()
+
+
+def clis_certify_workspace_size(shape: Shape) -> int:
+    n = ctypes.c_size_t(0)
+    st = load_library().clis_certify_workspace_size(ctypes.byref(shape), ctypes.byref(n))
+    if st != 0:
+        raise ClisError("clis_certify_workspace_size", st)
+    return n.value
+
+
+def clis_certify(q, k, v, scale_log2: float, exp_fmt: str = "bf16", acc_fmt: str = "fp32",
+                 kbar=None, certs=None, workspace=None, stream=None):
+    """Certification pre-pass.  Returns (kbar float32 [B*H, d], certs int32 [B*H, 8]);
+    decode certificates with :func:`decode_certs`."""
+    lib = load_library()
+    shape = make_shape(q, k, v)
+    BH, d = shape.B * shape.H, shape.d
+    dev = q.device
+    if kbar is None:
+        kbar = torch.empty((max(BH, 1), d), dtype=torch.float32, device=dev)
+    if certs is None:
+        certs = torch.empty((max(BH, 1), CERT_WORDS), dtype=torch.int32, device=dev)
+    need = clis_certify_workspace_size(shape)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    st = lib.clis_certify(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), float(scale_log2),
+                          FMT[exp_fmt], FMT[acc_fmt], _ptr(kbar), _ptr(certs), _ptr(workspace),
+                          workspace.numel(), _stream(stream))
+    if st != 0:
+        raise ClisError("clis_certify", st)
+    return kbar, certs
+
+
+def clis_attn_fwd(q, k, v, scale_log2: float, kbar=None, certs=None, causal: bool = False,
+                  variant: str = "auto", out=None, lse2=None, stream=None):
+    """Fused attention forward; returns ``out`` (bf16, shape of q)."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    shape = make_shape(q, k, v, out)
+    st = lib.clis_attn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse2),
+                           _ptr(kbar), _ptr(certs), float(scale_log2), int(bool(causal)),
+                           VARIANT[variant], _stream(stream))
+    if st != 0:
+        raise ClisError("clis_attn_fwd", st)
+    return out
+
+
+def clis_get_device_error() -> int:
+    code = ctypes.c_uint32(0)
+    st = load_library().clis_get_device_error(ctypes.byref(code))
+    if st not in (0, 6):
+        raise ClisError("clis_get_device_error", st)
+    return code.value
+
+
+def clis_clear_device_error() -> None:
+    st = load_library().clis_clear_device_error()
+    if st != 0:
+        raise ClisError("clis_clear_device_error", st)
+
+
+def decode_certs(certs) -> list[dict]:
+    """int32 [BH, 8] certificate words -> list of dicts (host copy)."""
+    c = certs.detach().to("cpu").contiguous()
+    ints = c[:, :5].tolist()
+    floats = c[:, 5:8].view(torch.float32).tolist()
+    out = []
+    for i, f in zip(ints, floats):
+        out.append({"certified": i[0], "G": i[1], "A": i[2], "C": i[3], "reason": i[4],
+                    "B_h": f[0], "kappa": f[1], "qmax": f[2]})
+    return out
+
+
+def scale_log2_for(d: int, softmax_scale: float | None = None) -> float:
+    """scale_log2 = softmax_scale * log2(e), default softmax_scale = 1/sqrt(d)."""
+    s = (1.0 / math.sqrt(d)) if softmax_scale is None else softmax_scale
+    return s * LOG2E
+
+
+def certify(q, k, v, softmax_scale: float | None = None, **kw):
+    return clis_certify(q, k, v, scale_log2_for(q.shape[-1], softmax_scale), **kw)
+
+
+def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
+              variant: str = "auto", return_certs: bool = False, device=None):
+    """CLiS attention forward: certification pre-pass, then the fused kernel.
+
+    q, k, v: bf16 [B, H, N, d].  Host tensors (pinned or not) are copied to
+    ``device`` (default cuda:0) and the result is copied back to the host;
+    device tensors stay where they are.
+    """
+    on_host = q.device.type == "cpu"
+    if on_host:
+        dev = torch.device(device or "cuda:0")
+        q, k, v = (t.to(dev, non_blocking=True) for t in (q, k, v))
+    sl2 = scale_log2_for(q.shape[-1], softmax_scale)
+    kbar = certs = None
+    if variant != "online":
+        kbar, certs = clis_certify(q, k, v, sl2)
+    out = clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=causal, variant=variant)
+    if on_host:
+        out = out.to("cpu")
+    if return_certs:
+        return out, kbar, certs
+    return out
+
+
+load_library()

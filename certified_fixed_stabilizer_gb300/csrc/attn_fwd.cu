@@ -1,0 +1,661 @@
+// attn_fwd.cu -- fused attention forward for sm_103a with two softmax paths:
+//
+//  * certified (CLiS): the per-row stabiliser mu_i = scale_log2 * (q_i . kbar)
+//    is fixed before the KV loop ("CLiS: Plug-and-Play Attention Acceleration
+//    for Video Diffusion on TPUs via Certified Stabilization", abstract and
+//    Figure 5(a): a loop-invariant stabiliser removes the reduction and
+//    rescaling chain).  p_ij = exp2(scale_log2 * s_ij - mu_i) is accumulated
+//    directly: no row maximum, no alpha, no rescaling of O.  With the
+//    certificate of Algorithm 1 (B_h <= C) every exp2 argument lies in
+//    [-B_h, B_h], so p never overflows the BF16 P operand and the FP32
+//    accumulators stay below 2^(A + C).
+//  * online (fallback and baseline): running row maximum m_i, correction
+//    factor alpha = exp2(m_old - m_new) applied to the accumulator O before
+//    every P.V product after the first, and to the row sum.
+//
+// One persistent kernel runs both; every 256-row query block ("work tile")
+// of a head picks its path from the head's certificate (or from the forced
+// variant).  Per CTA (512 threads, 1 CTA per SM):
+//
+//   warps 0-3   softmax for query tile 0 (rows 0-127 of the work tile)
+//   warps 4-7   softmax for query tile 1 (rows 128-255)
+//   warps 8-11  correction: rescales O in TMEM (online tiles only)
+//   warp 12     TMA producer: Q tiles once per work tile, K and V tiles
+//               through an NSTAGE-deep shared-memory ring
+//   warp 13     MMA issuer: S = Q K^T (SMEM x SMEM -> TMEM) and
+//               O += P V (P from TMEM, V from SMEM -> TMEM); owns TMEM
+//
+// TMEM (512 columns x 128 lanes x 32 bit): S0 @0, S1 @128 (fp32 scores,
+// overwritten in place by P as packed bf16 in their first 64 columns),
+// O0 @256, O1 @256+D (fp32 accumulators).  Lane r holds row r of a tile.
+// The two query tiles ping-pong: while one softmax group turns S into P the
+// tensor cores run the other tile's matmuls.
+//
+// Every mbarrier wait is bounded (see mbar_wait): a stuck pipeline sets the
+// device error word and the CTA drains its in-flight copies and returns.
+#include <cuda_bf16.h>
+
+#include "clis_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace clis {
+
+__device__ unsigned int g_attn_error_word = 0;
+
+namespace {
+
+constexpr int BM = 128;            // rows per query tile
+constexpr int BN = 128;            // keys per KV tile
+constexpr int kThreads = 512;
+constexpr int kNStageMax = 6;
+
+// Error-word bits: which wait gave up.
+constexpr unsigned kErrProducer = 1u << 0;
+constexpr unsigned kErrMma = 1u << 1;
+constexpr unsigned kErrSoftmax = 1u << 2;
+constexpr unsigned kErrCorrection = 1u << 3;
+constexpr unsigned kErrDrain = 1u << 4;
+
+template <int D>
+struct Cfg {
+    static constexpr int NSTAGE = (D == 128) ? 4 : 6;
+    static constexpr int NBOX = D / 64;                 // 64-column (128-byte) TMA boxes per tile
+    static constexpr int BOX_BYTES = 128 * 128;         // 128 rows x 128 bytes
+    static constexpr int TILE_BYTES = NBOX * BOX_BYTES; // one Q, K or V tile
+    static constexpr int SMEM_BYTES = 2 * TILE_BYTES + NSTAGE * TILE_BYTES + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
+    static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false);  // Q K^T, both K-major
+    static constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, true);    // P V, V is MN-major
+};
+
+struct Params {
+    const uint16_t *q;
+    uint16_t *o;
+    float *lse2;
+    const float *kbar;
+    const clis_head_cert_t *certs;
+    int64_t q_sb, q_sh, q_sn, o_sb, o_sh, o_sn;
+    int B, H, Nq, Nk;
+    int nqb;        // 256-row query blocks per head
+    int n_kv_full;  // KV tiles per head, ceil(Nk / 128)
+    int num_tiles;  // B * H * nqb
+    float scale_log2;
+    int variant;
+};
+
+struct __align__(8) Ctl {
+    uint64_t q_full[2], q_empty[2];
+    uint64_t kv_full[kNStageMax], kv_empty[kNStageMax];
+    uint64_t s_full[2], p_full[2], pv_done[2];
+    uint64_t alpha_full[2], o_ready[2], o_free[2];
+    uint64_t drain;
+    float alpha[2][BM];
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+struct Tile {
+    int bh, b, h, qb, n_kv;
+    bool cert;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Tile decode_tile(const Params &p, int tile)
+{
+    Tile t;
+    t.bh = tile / p.nqb;
+    const int r = tile % p.nqb;
+    t.qb = CAUSAL ? (p.nqb - 1 - r) : r;  // causal: longest rows first
+    t.b = t.bh / p.H;
+    t.h = t.bh % p.H;
+    if (CAUSAL) {
+        const int last_row = min(p.Nq, (t.qb + 1) * 2 * BM) - 1;
+        t.n_kv = min(p.n_kv_full, last_row / BN + 1);
+    } else {
+        t.n_kv = p.n_kv_full;
+    }
+    if (p.variant == CLIS_ONLINE) t.cert = false;
+    else if (p.variant == CLIS_CERTIFIED_FORCED) t.cert = true;
+    else t.cert = __ldg(&p.certs[t.bh].certified) != 0;
+    return t;
+}
+
+// Wait ignoring the abort flag (used only while draining after an abort).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > 200000000ull) {
+            atomicOr(&g_attn_error_word, kErrDrain);
+            return;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ producer
+
+template <int D, bool CAUSAL>
+__device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
+                              const CUtensorMap *tm_v, uint32_t sQ0, uint32_t sKV)
+{
+    using C = Cfg<D>;
+    volatile int *ab = &c.abort_flag;
+    unsigned *err = &g_attn_error_word;
+    const uint64_t pol_kv = policy_evict_last();
+    const uint64_t pol_q = policy_evict_first();
+    uint32_t it = 0;
+    int w = 0;
+    int q_issued = -1;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
+        const Tile T = decode_tile<CAUSAL>(p, tile);
+        for (int t = 0; t < 2; t++) {
+            if (!mbar_wait(smem_u32(&c.q_empty[t]), (w & 1) ^ 1, ab, err, kErrProducer)) goto abort;
+            const uint32_t bar = smem_u32(&c.q_full[t]);
+            mbar_arrive_expect_tx(bar, C::TILE_BYTES);
+            const int row = T.qb * 2 * BM + t * BM;
+#pragma unroll
+            for (int bx = 0; bx < C::NBOX; bx++)
+                tma_load_4d_hint(sQ0 + t * C::TILE_BYTES + bx * C::BOX_BYTES, tm_q, bar, bx * 64, row, T.h, T.b,
+                                 pol_q);
+        }
+        q_issued = w;
+        for (int j = 0; j < T.n_kv; j++) {
+#pragma unroll
+            for (int kv = 0; kv < 2; kv++) {
+                const uint32_t stage = it % C::NSTAGE;
+                const uint32_t ph = (it / C::NSTAGE) & 1;
+                if (!mbar_wait(smem_u32(&c.kv_empty[stage]), ph ^ 1, ab, err, kErrProducer)) goto abort;
+                const uint32_t bar = smem_u32(&c.kv_full[stage]);
+                mbar_arrive_expect_tx(bar, C::TILE_BYTES);
+                const CUtensorMap *tm = kv ? tm_v : tm_k;
+#pragma unroll
+                for (int bx = 0; bx < C::NBOX; bx++)
+                    tma_load_4d_hint(sKV + stage * C::TILE_BYTES + bx * C::BOX_BYTES, tm, bar, bx * 64, j * BN,
+                                     T.h, T.b, pol_kv);
+                ++it;
+            }
+        }
+    }
+    return;
+abort:
+    // Let every copy already issued land before the CTA leaves.
+    for (uint32_t k = (it > C::NSTAGE ? it - C::NSTAGE : 0); k < it; k++)
+        drain_wait(smem_u32(&c.kv_full[k % C::NSTAGE]), (k / C::NSTAGE) & 1);
+    if (q_issued >= 0)
+        for (int t = 0; t < 2; t++) drain_wait(smem_u32(&c.q_full[t]), q_issued & 1);
+}
+
+// ----------------------------------------------------------------------- MMA
+
+// The start-address field (bits 0-13, address >> 4) of a descriptor is
+// advanced by adding (byte offset >> 4); every address stays below 256 KB, so
+// the field never carries into the next one.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk)
+{
+    using C = Cfg<D>;
+    const uint64_t qd = sdesc_sw128(sq, 16, 1024);
+    const uint64_t kd = sdesc_sw128(sk, 16, 1024);
+#pragma unroll 1
+    for (int kk = 0; kk < D / 16; kk++) {
+        // 16 elements = 32 bytes inside a 128-byte swizzle row; 4 steps per 64-column box.
+        const uint32_t off = ((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4;
+        umma_ss(d_tmem, qd + off, kd + off, C::IDESC_S, kk > 0 ? 1u : 0u);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t sv, bool accumulate)
+{
+    using C = Cfg<D>;
+    // V tile: keys x D, D contiguous (MN-major B operand).  LBO = distance
+    // between the 64-column boxes, SBO = 8 rows x 128 bytes; 16 keys = 2048 bytes.
+    const uint64_t vd = sdesc_sw128(sv, C::BOX_BYTES, 1024);
+#pragma unroll 1
+    for (int kk = 0; kk < BN / 16; kk++)
+        umma_ts(o_tmem, p_tmem + kk * 8, vd + ((kk * 2048) >> 4), C::IDESC_O, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+template <int D, bool CAUSAL>
+__device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, uint32_t sKV)
+{
+    using C = Cfg<D>;
+    volatile int *ab = &c.abort_flag;
+    unsigned *err = &g_attn_error_word;
+    uint32_t it = 0, g = 0, ncorr = 0;
+    int w = 0;
+    // Per-tile addresses are selected, not indexed, to keep them in registers.
+    auto tS = [&](int t) { return tmem + (t ? C::TM_S1 : C::TM_S0); };
+    auto tO = [&](int t) { return tmem + (t ? C::TM_O1 : C::TM_O0); };
+    auto sQ = [&](int t) { return sQ0 + (t ? C::TILE_BYTES : 0u); };
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
+        const Tile T = decode_tile<CAUSAL>(p, tile);
+        for (int t = 0; t < 2; t++)
+            if (!mbar_wait(smem_u32(&c.q_full[t]), w & 1, ab, err, kErrMma)) goto abort;
+        {
+            const uint32_t ks = it % C::NSTAGE;
+            if (!mbar_wait(smem_u32(&c.kv_full[ks]), (it / C::NSTAGE) & 1, ab, err, kErrMma)) goto abort;
+            tc_fence_after();
+            const uint32_t sk = sKV + ks * C::TILE_BYTES;
+            for (int t = 0; t < 2; t++) {
+                issue_qk<D>(tS(t), sQ(t), sk);
+                umma_commit(smem_u32(&c.s_full[t]));
+            }
+            umma_commit(smem_u32(&c.kv_empty[ks]));
+            if (T.n_kv == 1)
+                for (int t = 0; t < 2; t++) umma_commit(smem_u32(&c.q_empty[t]));
+            ++it;
+        }
+        for (int j = 0; j < T.n_kv; j++) {
+            const bool has_next = j + 1 < T.n_kv;
+            const uint32_t vs = it % C::NSTAGE;
+            if (!mbar_wait(smem_u32(&c.kv_full[vs]), (it / C::NSTAGE) & 1, ab, err, kErrMma)) goto abort;
+            const uint32_t sv = sKV + vs * C::TILE_BYTES;
+            const uint32_t kn = it + 1;
+            const uint32_t kns = kn % C::NSTAGE;
+            const uint32_t sk = sKV + kns * C::TILE_BYTES;
+#pragma unroll 1
+            for (int t = 0; t < 2; t++) {
+                if (!mbar_wait(smem_u32(&c.p_full[t]), g & 1, ab, err, kErrMma)) goto abort;
+                if (!T.cert && j > 0)
+                    if (!mbar_wait(smem_u32(&c.o_ready[t]), ncorr & 1, ab, err, kErrMma)) goto abort;
+                if (j == 0)
+                    if (!mbar_wait(smem_u32(&c.o_free[t]), (w & 1) ^ 1, ab, err, kErrMma)) goto abort;
+                tc_fence_after();
+                issue_pv<D>(tO(t), tS(t), sv, j > 0);
+                umma_commit(smem_u32(&c.pv_done[t]));
+                if (t == 1) umma_commit(smem_u32(&c.kv_empty[vs]));
+                if (has_next) {
+                    if (t == 0) {
+                        if (!mbar_wait(smem_u32(&c.kv_full[kns]), (kn / C::NSTAGE) & 1, ab, err, kErrMma))
+                            goto abort;
+                        tc_fence_after();
+                    }
+                    issue_qk<D>(tS(t), sQ(t), sk);
+                    umma_commit(smem_u32(&c.s_full[t]));
+                    if (t == 1) umma_commit(smem_u32(&c.kv_empty[kns]));
+                    if (j + 1 == T.n_kv - 1) umma_commit(smem_u32(&c.q_empty[t]));
+                }
+            }
+            it += has_next ? 2 : 1;
+            ++g;
+            if (!T.cert && j > 0) ++ncorr;
+        }
+    }
+    return;
+abort:
+    umma_commit(smem_u32(&c.drain));
+    drain_wait(smem_u32(&c.drain), 0);
+}
+
+// ------------------------------------------------------------------- softmax
+
+template <int D, bool CAUSAL>
+__device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, int lane)
+{
+    using C = Cfg<D>;
+    volatile int *ab = &c.abort_flag;
+    unsigned *err = &g_attn_error_word;
+    const int t = warp >> 2;
+    const int quarter = warp & 3;
+    const int rl = quarter * 32 + lane;                       // row within the query tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + (t ? C::TM_S1 : C::TM_S0) + lane_off;
+    const uint32_t tO = tmem + (t ? C::TM_O1 : C::TM_O0) + lane_off;
+    const float sl2 = p.scale_log2;
+    uint32_t g = 0;
+    int w = 0;
+
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
+        const Tile T = decode_tile<CAUSAL>(p, tile);
+        const int row = T.qb * 2 * BM + t * BM + rl;  // query index within the head
+        const bool row_ok = row < p.Nq;
+
+        // Certified path: mu_i = scale_log2 * (q_i . kbar), fixed for the whole KV loop.
+        float mu = 0.f;
+        if (T.cert && row_ok) {
+            const uint16_t *qr = p.q + T.b * p.q_sb + T.h * p.q_sh + static_cast<int64_t>(row) * p.q_sn;
+            const float *kb = p.kbar + static_cast<int64_t>(T.bh) * D;
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 4
+            for (int c8 = 0; c8 < D / 8; c8++) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(qr + c8 * 8);
+                const float4 k0 = __ldg(reinterpret_cast<const float4 *>(kb + c8 * 8));
+                const float4 k1 = __ldg(reinterpret_cast<const float4 *>(kb + c8 * 8 + 4));
+                acc0 = fmaf(__uint_as_float(u.x << 16), k0.x, acc0);
+                acc1 = fmaf(__uint_as_float(u.x & 0xFFFF0000u), k0.y, acc1);
+                acc0 = fmaf(__uint_as_float(u.y << 16), k0.z, acc0);
+                acc1 = fmaf(__uint_as_float(u.y & 0xFFFF0000u), k0.w, acc1);
+                acc0 = fmaf(__uint_as_float(u.z << 16), k1.x, acc0);
+                acc1 = fmaf(__uint_as_float(u.z & 0xFFFF0000u), k1.y, acc1);
+                acc0 = fmaf(__uint_as_float(u.w << 16), k1.z, acc0);
+                acc1 = fmaf(__uint_as_float(u.w & 0xFFFF0000u), k1.w, acc1);
+            }
+            mu = sl2 * (acc0 + acc1);
+        }
+
+        float m_run = -INFINITY;  // online: running max of scale_log2 * s
+        float l_run = 0.f;
+
+        for (int j = 0; j < T.n_kv; j++) {
+            if (!mbar_wait(smem_u32(&c.s_full[t]), g & 1, ab, err, kErrSoftmax)) goto abort;
+            tc_fence_after();
+            uint32_t s[BN];
+            tmem_ld32(tS + 0, s + 0);
+            tmem_ld32(tS + 32, s + 32);
+            tmem_ld32(tS + 64, s + 64);
+            tmem_ld32(tS + 96, s + 96);
+            tmem_wait_ld();
+
+            // Mask keys past Nk (ragged last tile) and, if causal, keys after the row.
+            const int key0 = j * BN;
+            const int lim = CAUSAL ? min(p.Nk, row + 1) : p.Nk;  // keys [0, lim) are visible
+            if (key0 + BN > lim) {
+#pragma unroll
+                for (int cc = 0; cc < BN; cc++)
+                    if (key0 + cc >= lim) s[cc] = 0xFF800000u;  // -inf
+            }
+
+            // P (bf16 pairs) overwrites the first 64 columns of S, 16 columns
+            // per 32 scores; all of S is already in registers.
+            float nshift;  // -(stabiliser) in scale_log2 * s units
+            float alpha = 1.f;
+            if (T.cert) {
+                nshift = -mu;
+            } else {
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int cc = 0; cc < BN; cc += 2) {
+                    mx0 = fmaxf(mx0, __uint_as_float(s[cc]));
+                    mx1 = fmaxf(mx1, __uint_as_float(s[cc + 1]));
+                }
+                const float m_tile = fmaxf(mx0, mx1) * sl2;
+                const float m_new = fmaxf(m_run, m_tile);
+                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                if (j > 0) {
+                    alpha = ex2_approx(m_run - m_use);
+                    c.alpha[t][rl] = alpha;
+                    mbar_arrive(smem_u32(&c.alpha_full[t]));
+                }
+                m_run = m_new;
+                nshift = -m_use;
+            }
+            float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+            for (int c32 = 0; c32 < BN / 32; c32++) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(s[c32 * 32 + 2 * e]), sl2, nshift));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(s[c32 * 32 + 2 * e + 1]), sl2, nshift));
+                    l0 += p0;
+                    l1 += p1;
+                    pk[e] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(tS + c32 * 16, pk);
+            }
+            l_run = l_run * alpha + (l0 + l1);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&c.p_full[t]));
+            ++g;
+        }
+
+        // Epilogue: O / l -> bf16, written straight from registers.
+        if (!mbar_wait(smem_u32(&c.pv_done[t]), (g - 1) & 1, ab, err, kErrSoftmax)) goto abort;
+        tc_fence_after();
+        {
+            const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+            uint16_t *orow = p.o + T.b * p.o_sb + T.h * p.o_sh + static_cast<int64_t>(row) * p.o_sn;
+#pragma unroll
+            for (int c32 = 0; c32 < D / 32; c32++) {
+                uint32_t r[32];
+                tmem_ld32(tO + c32 * 32, r);
+                tmem_wait_ld();
+                if (row_ok) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; e++)
+                        pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c32 * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; e++) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                }
+            }
+            if (p.lse2 && row_ok) {
+                const float base = T.cert ? mu : ((m_run == -INFINITY) ? 0.f : m_run);
+                p.lse2[static_cast<int64_t>(T.bh) * p.Nq + row] = base + log2f(l_run);
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&c.o_free[t]));
+    }
+abort:
+    return;
+}
+
+// ---------------------------------------------------------------- correction
+
+template <int D, bool CAUSAL>
+__device__ void correction_role(const Params &p, Ctl &c, uint32_t tmem, int warp, int lane)
+{
+    using C = Cfg<D>;
+    volatile int *ab = &c.abort_flag;
+    unsigned *err = &g_attn_error_word;
+    const int quarter = warp & 3;
+    const int rl = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t g = 0, ncorr = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+        const Tile T = decode_tile<CAUSAL>(p, tile);
+        if (T.cert) {
+            g += T.n_kv;
+            continue;
+        }
+        for (int j = 0; j < T.n_kv; j++) {
+            if (j > 0) {
+                for (int t = 0; t < 2; t++) {
+                    if (!mbar_wait(smem_u32(&c.alpha_full[t]), ncorr & 1, ab, err, kErrCorrection)) return;
+                    if (!mbar_wait(smem_u32(&c.pv_done[t]), (g - 1) & 1, ab, err, kErrCorrection)) return;
+                    tc_fence_after();
+                    const float alpha = c.alpha[t][rl];
+                    const uint32_t tO = tmem + (t ? C::TM_O1 : C::TM_O0) + lane_off;
+#pragma unroll
+                    for (int c32 = 0; c32 < D / 32; c32++) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + c32 * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; e++) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                        tmem_st32(tO + c32 * 32, r);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&c.o_ready[t]));
+                }
+                ++ncorr;
+            }
+            ++g;
+        }
+    }
+}
+
+// -------------------------------------------------------------------- kernel
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const Params p)
+{
+    using C = Cfg<D>;
+    extern __shared__ uint8_t dsmem[];
+    __shared__ Ctl ctl;
+    const uint32_t sbase = (smem_u32(dsmem) + 1023u) & ~1023u;
+    const uint32_t sQ0 = sbase;
+    const uint32_t sKV = sbase + 2 * C::TILE_BYTES;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; t++) {
+            mbar_init(smem_u32(&ctl.q_full[t]), 1);
+            mbar_init(smem_u32(&ctl.q_empty[t]), 1);
+            mbar_init(smem_u32(&ctl.s_full[t]), 1);
+            mbar_init(smem_u32(&ctl.p_full[t]), BM);
+            mbar_init(smem_u32(&ctl.pv_done[t]), 1);
+            mbar_init(smem_u32(&ctl.alpha_full[t]), BM);
+            mbar_init(smem_u32(&ctl.o_ready[t]), BM);
+            mbar_init(smem_u32(&ctl.o_free[t]), BM);
+        }
+        for (int s = 0; s < C::NSTAGE; s++) {
+            mbar_init(smem_u32(&ctl.kv_full[s]), 1);
+            mbar_init(smem_u32(&ctl.kv_empty[s]), 1);
+        }
+        mbar_init(smem_u32(&ctl.drain), 1);
+        ctl.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 12 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    if (warp == 13) {
+        tmem_alloc(smem_u32(&ctl.tmem_base), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl.tmem_base;
+
+    // Register split (launch: 512 threads x 128 = 65536): softmax 2 x 128 x 184,
+    // correction 128 x 88, producer/MMA group 128 x 56 -> 47104 + 11264 + 7168 = 65536.
+    if (warp < 8) {
+        setmaxnreg_inc<184>();
+        softmax_role<D, CAUSAL>(p, ctl, tmem, warp, lane);
+    } else if (warp < 12) {
+        setmaxnreg_dec<88>();
+        correction_role<D, CAUSAL>(p, ctl, tmem, warp, lane);
+    } else {
+        setmaxnreg_dec<56>();
+        if (warp == 12 && lane == 0) producer_role<D, CAUSAL>(p, ctl, &tm_q, &tm_k, &tm_v, sQ0, sKV);
+        if (warp == 13 && lane == 0) mma_role<D, CAUSAL>(p, ctl, tmem, sQ0, sKV);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 13) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult qres;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qres) ==
+                cudaSuccess &&
+            qres == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 4-D map over [B, H, N, d] (innermost first: d, N, H, B), 64 x 128 boxes, 128-byte swizzle.
+bool make_map(CUtensorMap *map, const void *base, int64_t B, int64_t H, int64_t N, int64_t d, int64_t sb,
+              int64_t sh, int64_t sn)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+    if (!enc) return false;
+    // A stride of a size-1 dimension is never used; give it a canonical value.
+    if (H == 1) sh = sn * N;
+    if (B == 1) sb = sh * H;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(sn * 2), static_cast<cuuint64_t>(sh * 2),
+                             static_cast<cuuint64_t>(sb * 2)};
+    cuuint32_t box[4] = {64, 128, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D, bool CAUSAL>
+clis_status_t launch_impl(const AttnArgs &a, cudaStream_t stream)
+{
+    using C = Cfg<D>;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CLIS_ERR_CUDA;
+    int nsm = 0;
+    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return CLIS_ERR_CUDA;
+    if (cudaFuncSetAttribute(attn_fwd_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
+        return CLIS_ERR_CUDA;
+
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, a.q, a.B, a.H, a.Nq, D, a.q_sb, a.q_sh, a.q_sn)) return CLIS_ERR_CUDA;
+    if (!make_map(&mk, a.k, a.B, a.H, a.Nk, D, a.k_sb, a.k_sh, a.k_sn)) return CLIS_ERR_CUDA;
+    if (!make_map(&mv, a.v, a.B, a.H, a.Nk, D, a.v_sb, a.v_sh, a.v_sn)) return CLIS_ERR_CUDA;
+
+    Params p;
+    p.q = a.q;
+    p.o = a.o;
+    p.lse2 = a.lse2;
+    p.kbar = a.kbar;
+    p.certs = a.certs;
+    p.q_sb = a.q_sb;
+    p.q_sh = a.q_sh;
+    p.q_sn = a.q_sn;
+    p.o_sb = a.o_sb;
+    p.o_sh = a.o_sh;
+    p.o_sn = a.o_sn;
+    p.B = a.B;
+    p.H = a.H;
+    p.Nq = a.Nq;
+    p.Nk = a.Nk;
+    p.nqb = (a.Nq + 2 * BM - 1) / (2 * BM);
+    p.n_kv_full = (a.Nk + BN - 1) / BN;
+    p.num_tiles = a.B * a.H * p.nqb;
+    p.scale_log2 = a.scale_log2;
+    p.variant = a.variant;
+    if (p.num_tiles == 0) return CLIS_OK;
+    const int grid = p.num_tiles < nsm ? p.num_tiles : nsm;
+    attn_fwd_kernel<D, CAUSAL><<<grid, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? CLIS_OK : CLIS_ERR_CUDA;
+}
+
+}  // namespace
+
+clis_status_t launch_attn_fwd(const AttnArgs &a, cudaStream_t stream)
+{
+    if (a.d == 128) return a.causal ? launch_impl<128, true>(a, stream) : launch_impl<128, false>(a, stream);
+    return a.causal ? launch_impl<64, true>(a, stream) : launch_impl<64, false>(a, stream);
+}
+
+clis_status_t read_device_error(uint32_t *code)
+{
+    unsigned int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return CLIS_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, g_attn_error_word, sizeof v) != cudaSuccess) return CLIS_ERR_CUDA;
+    *code = v;
+    return v ? CLIS_ERR_TIMEOUT : CLIS_OK;
+}
+
+clis_status_t clear_device_error()
+{
+    const unsigned int z = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return CLIS_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_attn_error_word, &z, sizeof z) != cudaSuccess) return CLIS_ERR_CUDA;
+    return CLIS_OK;
+}
+
+}  // namespace clis

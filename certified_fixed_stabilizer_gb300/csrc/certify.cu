@@ -1,0 +1,341 @@
+// certify.cu -- the CLiS certification pre-pass on the GPU.
+//
+// Implements Algorithm 1, steps 1-7, of "CLiS: Plug-and-Play Attention
+// Acceleration for Video Diffusion on TPUs via Certified Stabilization" for
+// every (b, h) head, plus the certification decision (finite inputs and
+// B_h <= C).  Four launches, all HBM-bandwidth bound:
+//
+//   certify_ksum      per 1024-row chunk of K: fp32 column sums (step 1) and
+//                     the max |k| bit pattern (non-finite detection)
+//   certify_kbar      kbar = (sum of chunk sums in chunk order) / Nk
+//   certify_norms     per chunk of K: max ||k - kbar||^2 (steps 2-3), of Q:
+//                     max ||q||^2 (step 4), of Q and V: max |x| bit patterns
+//                     (step 5 and non-finite detection)
+//   certify_finalize  one warp per head: kappa, B_h, G, A, C and the flag
+//
+// K~ = K - 1 kbar^T (step 2) is never materialised: it is only needed inside
+// the norm reduction, and the attention kernel moves kbar into the per-row
+// stabiliser instead (softmax is invariant to a common key shift).
+//
+// Conservativeness: every quantity that bounds a score (|k - kbar|, the
+// squares, their sums, the square roots and the products forming B_h) is
+// rounded upward, so kappa and B_h are upper bounds of the exact values for
+// the kbar this pass returns.  Determinism: sums run in a fixed order per
+// thread and are combined in a fixed order; maxima are order-independent.
+#include <cuda_bf16.h>
+
+#include "clis_internal.h"
+
+namespace clis {
+
+namespace {
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t abs_bits_max(uint32_t u, uint32_t m)
+{
+    m = max(m, u & 0x7FFFu);
+    m = max(m, (u >> 16) & 0x7FFFu);
+    return m;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint16_t *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red)
+{
+    __syncthreads();  // `red` may still be read by a previous call
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t x = (lane < (kCertThreads >> 5)) ? red[lane] : 0u;
+        x = __reduce_max_sync(0xFFFFFFFFu, x);
+        if (lane == 0) red[0] = x;
+    }
+    __syncthreads();
+    return red[0];
+}
+
+// Step 1 (partial): column sums of one chunk of K, plus max |k| bits.
+template <int D>
+__global__ void __launch_bounds__(kCertThreads) certify_ksum_kernel(CertArgs a, CertWorkspace ws)
+{
+    constexpr int VPR = D / 8;             // 16-byte vectors per row
+    constexpr int RPS = kCertThreads / VPR;  // rows per sweep
+    __shared__ float red[RPS * D];
+    __shared__ uint32_t redu[kCertThreads / 32];
+
+    const int chunk = blockIdx.x % a.nck;
+    const int bh = blockIdx.x / a.nck;
+    const int b = bh / a.H, h = bh % a.H;
+    const int cv = threadIdx.x % VPR, rp = threadIdx.x / VPR;
+    const int r0 = chunk * kCertChunkRows;
+    const int r1 = min(a.Nk, r0 + kCertChunkRows);
+    const uint16_t *base = a.k + b * a.k_sb + h * a.k_sh + cv * 8;
+
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; e++) acc[e] = 0.f;
+    uint32_t amax = 0;
+#pragma unroll 4
+    for (int r = r0 + rp; r < r1; r += RPS) {
+        const uint4 u = ld_stream(base + static_cast<int64_t>(r) * a.k_sn);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            acc[2 * e] += bf16_lo(w[e]);
+            acc[2 * e + 1] += bf16_hi(w[e]);
+            amax = abs_bits_max(w[e], amax);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; e++) red[rp * D + cv * 8 + e] = acc[e];
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += kCertThreads) {
+        float s = 0.f;
+        for (int p = 0; p < RPS; p++) s += red[p * D + c];
+        ws.ksum[(static_cast<int64_t>(bh) * a.nck + chunk) * D + c] = s;
+    }
+    const uint32_t m = block_max_u32(amax, redu);
+    if (threadIdx.x == 0) ws.kabs[static_cast<int64_t>(bh) * a.nck + chunk] = m;
+}
+
+// Step 1 (final): kbar = sum_chunks / Nk, round to nearest.
+__global__ void certify_kbar_kernel(CertArgs a, CertWorkspace ws)
+{
+    const int bh = blockIdx.x;
+    const int c = threadIdx.x;
+    if (c >= a.d) return;
+    float s = 0.f;
+    for (int ch = 0; ch < a.nck; ch++) s += ws.ksum[(static_cast<int64_t>(bh) * a.nck + ch) * a.d + c];
+    a.kbar[static_cast<int64_t>(bh) * a.d + c] = __fdiv_rn(s, static_cast<float>(a.Nk));
+}
+
+// Steps 2-5 (partial): one chunk of K (centred norms), Q (norms) or V (|v|).
+template <int D>
+__global__ void __launch_bounds__(kCertThreads) certify_norms_kernel(CertArgs a, CertWorkspace ws)
+{
+    constexpr int VPR = D / 8;
+    constexpr int RPS = kCertThreads / VPR;
+    __shared__ uint32_t redu[kCertThreads / 32];
+
+    const int per_head = 2 * a.nck + a.ncq;
+    const int bh = blockIdx.x / per_head;
+    int part = blockIdx.x % per_head;
+    const int b = bh / a.H, h = bh % a.H;
+    const int cv = threadIdx.x % VPR, rp = threadIdx.x / VPR;
+
+    int kind;  // 0 = K, 1 = Q, 2 = V
+    if (part < a.nck) {
+        kind = 0;
+    } else if (part < a.nck + a.ncq) {
+        kind = 1;
+        part -= a.nck;
+    } else {
+        kind = 2;
+        part -= a.nck + a.ncq;
+    }
+    const int nrows = (kind == 1) ? a.Nq : a.Nk;
+    const int r0 = part * kCertChunkRows;
+    const int r1 = min(nrows, r0 + kCertChunkRows);
+    const int nsweeps = (r1 - r0 + RPS - 1) / RPS;  // uniform across the block
+
+    if (kind == 0) {
+        float kb[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) kb[e] = a.kbar[static_cast<int64_t>(bh) * D + cv * 8 + e];
+        const uint16_t *base = a.k + b * a.k_sb + h * a.k_sh + cv * 8;
+        float mx = 0.f;
+#pragma unroll 4
+        for (int sw = 0; sw < nsweeps; sw++) {
+            const int r = r0 + sw * RPS + rp;
+            // Every lane runs the same number of sweeps (the shuffles below
+            // need all 32 lanes of the warp); rows past r1 contribute nothing.
+            float ss = 0.f;
+            if (r < r1) {
+                const uint4 u = ld_stream(base + static_cast<int64_t>(r) * a.k_sn);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const float x0 = bf16_lo(w[e]), x1 = bf16_hi(w[e]);
+                    const float d0 = (x0 >= kb[2 * e]) ? __fsub_ru(x0, kb[2 * e]) : __fsub_ru(kb[2 * e], x0);
+                    const float d1 = (x1 >= kb[2 * e + 1]) ? __fsub_ru(x1, kb[2 * e + 1])
+                                                           : __fsub_ru(kb[2 * e + 1], x1);
+                    ss = __fmaf_ru(d0, d0, ss);
+                    ss = __fmaf_ru(d1, d1, ss);
+                }
+            }
+#pragma unroll
+            for (int off = 1; off < VPR; off <<= 1) ss = __fadd_ru(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, off));
+            mx = fmaxf(mx, ss);
+        }
+        const uint32_t m = block_max_u32(__float_as_uint(mx), redu);
+        if (threadIdx.x == 0) ws.knorm2[static_cast<int64_t>(bh) * a.nck + part] = m;
+    } else if (kind == 1) {
+        const uint16_t *base = a.q + b * a.q_sb + h * a.q_sh + cv * 8;
+        float mx = 0.f;
+        uint32_t amax = 0;
+#pragma unroll 4
+        for (int sw = 0; sw < nsweeps; sw++) {
+            const int r = r0 + sw * RPS + rp;
+            float ss = 0.f;
+            if (r < r1) {
+                const uint4 u = ld_stream(base + static_cast<int64_t>(r) * a.q_sn);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const float x0 = bf16_lo(w[e]), x1 = bf16_hi(w[e]);
+                    ss = __fmaf_ru(x0, x0, ss);
+                    ss = __fmaf_ru(x1, x1, ss);
+                    amax = abs_bits_max(w[e], amax);
+                }
+            }
+#pragma unroll
+            for (int off = 1; off < VPR; off <<= 1) ss = __fadd_ru(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, off));
+            mx = fmaxf(mx, ss);
+        }
+        const uint32_t m = block_max_u32(__float_as_uint(mx), redu);
+        const uint32_t am = block_max_u32(amax, redu);
+        if (threadIdx.x == 0) {
+            ws.qnorm2[static_cast<int64_t>(bh) * a.ncq + part] = m;
+            ws.qabs[static_cast<int64_t>(bh) * a.ncq + part] = am;
+        }
+    } else {
+        const uint16_t *base = a.v + b * a.v_sb + h * a.v_sh + cv * 8;
+        uint32_t amax = 0;
+#pragma unroll 4
+        for (int r = r0 + rp; r < r1; r += RPS) {
+            const uint4 u = ld_stream(base + static_cast<int64_t>(r) * a.v_sn);
+            amax = abs_bits_max(u.x, amax);
+            amax = abs_bits_max(u.y, amax);
+            amax = abs_bits_max(u.z, amax);
+            amax = abs_bits_max(u.w, amax);
+        }
+        const uint32_t am = block_max_u32(amax, redu);
+        if (threadIdx.x == 0) ws.vabs[static_cast<int64_t>(bh) * a.nck + part] = am;
+    }
+}
+
+// ceil(log2 n) for n >= 1, in integers.
+__device__ __forceinline__ int ceil_log2_i64(int64_t n)
+{
+    return (n <= 1) ? 0 : 64 - __clzll(static_cast<unsigned long long>(n - 1));
+}
+
+// G = ceil(log2 max(1, m)) for the bf16 magnitude with bit pattern `bits`
+// (sign cleared, finite): m = (1 + f/128) 2^(e-127) for a normal number.
+__device__ __forceinline__ int v_exponent_from_bf16_bits(uint32_t bits)
+{
+    if (bits <= 0x3F80u) return 0;  // m <= 1 (includes zero and subnormals)
+    const int e = static_cast<int>(bits >> 7);
+    const uint32_t f = bits & 0x7Fu;
+    return (e - 127) + (f != 0u ? 1 : 0);
+}
+
+// Steps 3-7 and the decision: one warp per head.
+__global__ void certify_finalize_kernel(CertArgs a, CertWorkspace ws, int BH)
+{
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= BH) return;
+    const int64_t bh = warp;
+    uint32_t kn = 0, ka = 0, va = 0, qn = 0, qa = 0;
+    for (int c = lane; c < a.nck; c += 32) {
+        kn = max(kn, ws.knorm2[bh * a.nck + c]);
+        ka = max(ka, ws.kabs[bh * a.nck + c]);
+        va = max(va, ws.vabs[bh * a.nck + c]);
+    }
+    for (int c = lane; c < a.ncq; c += 32) {
+        qn = max(qn, ws.qnorm2[bh * a.ncq + c]);
+        qa = max(qa, ws.qabs[bh * a.ncq + c]);
+    }
+    kn = __reduce_max_sync(0xFFFFFFFFu, kn);
+    ka = __reduce_max_sync(0xFFFFFFFFu, ka);
+    va = __reduce_max_sync(0xFFFFFFFFu, va);
+    qn = __reduce_max_sync(0xFFFFFFFFu, qn);
+    qa = __reduce_max_sync(0xFFFFFFFFu, qa);
+    if (lane != 0) return;
+
+    clis_head_cert_t c;
+    const bool finite = ka < 0x7F80u && va < 0x7F80u && qa < 0x7F80u;
+    c.kappa = __fsqrt_ru(__uint_as_float(kn));   // step 3
+    c.qmax = __fsqrt_ru(__uint_as_float(qn));
+    if (!finite) {
+        c.certified = 0;
+        c.reason = 2;
+        c.G = c.A = c.C = 0;
+        c.B_h = __int_as_float(0x7F800000);
+    } else {
+        c.B_h = __fmul_ru(__fmul_ru(a.scale_log2, c.qmax), c.kappa);  // step 4
+        c.G = v_exponent_from_bf16_bits(va);                           // step 5
+        c.A = ceil_log2_i64(a.Nk) + c.G;                               // step 6
+        // step 7: floor(U_exp) = emax_exp and ceil(U_acc - A) - 1 = emax_acc - A,
+        // because log2 of a format's largest finite value lies in (emax, emax + 1).
+        c.C = min(a.emax_exp, a.emax_acc - c.A);
+        c.certified = (c.B_h <= static_cast<float>(c.C)) ? 1 : 0;
+        c.reason = c.certified ? 0 : 1;
+    }
+    a.certs[bh] = c;
+}
+
+}  // namespace
+
+size_t cert_workspace_layout(int64_t BH, int64_t nck, int64_t ncq, int64_t d, void *base, CertWorkspace *ws)
+{
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    size_t off = 0;
+    const size_t o_ksum = off;
+    off = up(off + static_cast<size_t>(BH * nck * d) * sizeof(float));
+    const size_t o_knorm = off;
+    off = up(off + static_cast<size_t>(BH * nck) * 4);
+    const size_t o_qnorm = off;
+    off = up(off + static_cast<size_t>(BH * ncq) * 4);
+    const size_t o_kabs = off;
+    off = up(off + static_cast<size_t>(BH * nck) * 4);
+    const size_t o_qabs = off;
+    off = up(off + static_cast<size_t>(BH * ncq) * 4);
+    const size_t o_vabs = off;
+    off = up(off + static_cast<size_t>(BH * nck) * 4);
+    if (ws && base) {
+        char *p = static_cast<char *>(base);
+        ws->ksum = reinterpret_cast<float *>(p + o_ksum);
+        ws->knorm2 = reinterpret_cast<uint32_t *>(p + o_knorm);
+        ws->qnorm2 = reinterpret_cast<uint32_t *>(p + o_qnorm);
+        ws->kabs = reinterpret_cast<uint32_t *>(p + o_kabs);
+        ws->qabs = reinterpret_cast<uint32_t *>(p + o_qabs);
+        ws->vabs = reinterpret_cast<uint32_t *>(p + o_vabs);
+    }
+    return off;
+}
+
+cudaError_t launch_certify(const CertArgs &a, const CertWorkspace &ws, cudaStream_t stream)
+{
+    const int BH = a.B * a.H;
+    if (BH == 0) return cudaSuccess;
+    const unsigned g1 = static_cast<unsigned>(BH) * static_cast<unsigned>(a.nck);
+    const unsigned g3 = static_cast<unsigned>(BH) * static_cast<unsigned>(2 * a.nck + a.ncq);
+    if (a.d == 128) {
+        certify_ksum_kernel<128><<<g1, kCertThreads, 0, stream>>>(a, ws);
+    } else {
+        certify_ksum_kernel<64><<<g1, kCertThreads, 0, stream>>>(a, ws);
+    }
+    certify_kbar_kernel<<<BH, 128, 0, stream>>>(a, ws);
+    if (a.d == 128) {
+        certify_norms_kernel<128><<<g3, kCertThreads, 0, stream>>>(a, ws);
+    } else {
+        certify_norms_kernel<64><<<g3, kCertThreads, 0, stream>>>(a, ws);
+    }
+    certify_finalize_kernel<<<(BH + 3) / 4, 128, 0, stream>>>(a, ws, BH);
+    return cudaGetLastError();
+}
+
+}  // namespace clis

@@ -1,0 +1,189 @@
+// clis_api.cu -- the extern "C" boundary declared in include/clis.h.
+//
+// Every entry point validates its arguments on the host before touching the
+// GPU; on any argument error it returns a status and launches nothing.
+#include <cmath>
+#include <cstdint>
+
+#include "clis_internal.h"
+
+namespace {
+
+constexpr int64_t kMaxN = (int64_t(1) << 31) - 1024;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+clis_status_t check_strides(int64_t sb, int64_t sh, int64_t sn, int64_t d)
+{
+    if (sb < 0 || sh < 0 || sn < d) return CLIS_ERR_INVALID_ARG;
+    if ((sb | sh | sn) & 7) return CLIS_ERR_MISALIGNED;
+    if (sb >= (int64_t(1) << 38) || sh >= (int64_t(1) << 38) || sn >= (int64_t(1) << 38))
+        return CLIS_ERR_UNSUPPORTED;
+    return CLIS_OK;
+}
+
+clis_status_t check_shape(const clis_shape_t *s, bool with_o)
+{
+    if (!s) return CLIS_ERR_INVALID_ARG;
+    if (s->B < 0 || s->H < 0 || s->Nq < 0 || s->Nk < 1 || s->d < 1) return CLIS_ERR_INVALID_ARG;
+    if (s->d != 64 && s->d != 128) return CLIS_ERR_UNSUPPORTED;
+    if (s->Nq > kMaxN || s->Nk > kMaxN || s->B * s->H > kMaxN || s->B > kMaxN || s->H > kMaxN)
+        return CLIS_ERR_UNSUPPORTED;
+    clis_status_t st;
+    if ((st = check_strides(s->q_sb, s->q_sh, s->q_sn, s->d)) != CLIS_OK) return st;
+    if ((st = check_strides(s->k_sb, s->k_sh, s->k_sn, s->d)) != CLIS_OK) return st;
+    if ((st = check_strides(s->v_sb, s->v_sh, s->v_sn, s->d)) != CLIS_OK) return st;
+    if (with_o && (st = check_strides(s->o_sb, s->o_sh, s->o_sn, s->d)) != CLIS_OK) return st;
+    return CLIS_OK;
+}
+
+bool valid_fmt(int f) { return f == CLIS_FMT_FP16 || f == CLIS_FMT_BF16 || f == CLIS_FMT_FP32; }
+
+// floor(log2 of the largest finite value) = the format's maximum exponent.
+int fmt_emax(int f) { return f == CLIS_FMT_FP16 ? 15 : 127; }
+
+int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" {
+
+clis_status_t clis_certify_workspace_size(const clis_shape_t *shape, size_t *bytes)
+{
+    if (!shape || !bytes) return CLIS_ERR_INVALID_ARG;
+    if (shape->B < 0 || shape->H < 0 || shape->Nq < 0 || shape->Nk < 1 || shape->d < 1)
+        return CLIS_ERR_INVALID_ARG;
+    const int64_t BH = shape->B * shape->H;
+    const int64_t nck = div_up(shape->Nk, clis::kCertChunkRows);
+    const int64_t ncq = div_up(shape->Nq, clis::kCertChunkRows);
+    *bytes = clis::cert_workspace_layout(BH, nck, ncq, shape->d, nullptr, nullptr);
+    return CLIS_OK;
+}
+
+clis_status_t clis_certify(const clis_shape_t *shape, const void *q, const void *k, const void *v,
+                           float scale_log2, clis_fmt_t exp_fmt, clis_fmt_t acc_fmt, float *kbar,
+                           clis_head_cert_t *certs, void *workspace, size_t ws_bytes, clis_stream_t stream)
+{
+    clis_status_t st = check_shape(shape, false);
+    if (st != CLIS_OK) return st;
+    // q is never read when Nq == 0 and may then be NULL.
+    if ((!q && shape->Nq > 0) || !k || !v || !kbar || !certs) return CLIS_ERR_INVALID_ARG;
+    if (!std::isfinite(scale_log2) || !(scale_log2 > 0.f)) return CLIS_ERR_INVALID_ARG;
+    if (!valid_fmt(exp_fmt) || !valid_fmt(acc_fmt)) return CLIS_ERR_INVALID_ARG;
+    if ((q && !aligned16(q)) || !aligned16(k) || !aligned16(v) || !aligned16(kbar) || !aligned16(certs))
+        return CLIS_ERR_MISALIGNED;
+    size_t need = 0;
+    clis_certify_workspace_size(shape, &need);
+    if (need > 0 && (!workspace || ws_bytes < need)) return CLIS_ERR_WORKSPACE;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return CLIS_ERR_MISALIGNED;
+    const int64_t BH = shape->B * shape->H;
+    if (BH == 0) return CLIS_OK;
+
+    clis::CertArgs a;
+    a.q = static_cast<const uint16_t *>(q);
+    a.k = static_cast<const uint16_t *>(k);
+    a.v = static_cast<const uint16_t *>(v);
+    a.q_sb = shape->q_sb;
+    a.q_sh = shape->q_sh;
+    a.q_sn = shape->q_sn;
+    a.k_sb = shape->k_sb;
+    a.k_sh = shape->k_sh;
+    a.k_sn = shape->k_sn;
+    a.v_sb = shape->v_sb;
+    a.v_sh = shape->v_sh;
+    a.v_sn = shape->v_sn;
+    a.B = static_cast<int>(shape->B);
+    a.H = static_cast<int>(shape->H);
+    a.Nq = static_cast<int>(shape->Nq);
+    a.Nk = static_cast<int>(shape->Nk);
+    a.d = static_cast<int>(shape->d);
+    a.nck = static_cast<int>(div_up(shape->Nk, clis::kCertChunkRows));
+    a.ncq = static_cast<int>(div_up(shape->Nq, clis::kCertChunkRows));
+    a.scale_log2 = scale_log2;
+    a.emax_exp = fmt_emax(exp_fmt);
+    a.emax_acc = fmt_emax(acc_fmt);
+    a.kbar = kbar;
+    a.certs = certs;
+    if (BH * (2 * a.nck + a.ncq) > kMaxN) return CLIS_ERR_UNSUPPORTED;
+    clis::CertWorkspace ws;
+    clis::cert_workspace_layout(BH, a.nck, a.ncq, a.d, workspace, &ws);
+    return clis::launch_certify(a, ws, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? CLIS_OK
+                                                                                              : CLIS_ERR_CUDA;
+}
+
+clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, const void *k, const void *v, void *o,
+                            float *lse2, const float *kbar, const clis_head_cert_t *certs, float scale_log2,
+                            int causal, clis_variant_t variant, clis_stream_t stream)
+{
+    clis_status_t st = check_shape(shape, true);
+    if (st != CLIS_OK) return st;
+    if (shape->B * shape->H == 0 || shape->Nq == 0) return CLIS_OK;  // nothing to compute
+    if (!q || !k || !v || !o) return CLIS_ERR_INVALID_ARG;
+    if (!std::isfinite(scale_log2) || !(scale_log2 > 0.f)) return CLIS_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return CLIS_ERR_INVALID_ARG;
+    if (variant != CLIS_AUTO && variant != CLIS_ONLINE && variant != CLIS_CERTIFIED_FORCED)
+        return CLIS_ERR_INVALID_ARG;
+    if (variant != CLIS_ONLINE && !kbar) return CLIS_ERR_INVALID_ARG;
+    if (variant == CLIS_AUTO && !certs) return CLIS_ERR_INVALID_ARG;
+    if (causal && shape->Nq != shape->Nk) return CLIS_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return CLIS_ERR_MISALIGNED;
+    if ((kbar && !aligned16(kbar)) || (certs && !aligned16(certs)) ||
+        (lse2 && (reinterpret_cast<uintptr_t>(lse2) & 3u)))
+        return CLIS_ERR_MISALIGNED;
+
+    clis::AttnArgs a;
+    a.q = static_cast<const uint16_t *>(q);
+    a.k = static_cast<const uint16_t *>(k);
+    a.v = static_cast<const uint16_t *>(v);
+    a.o = static_cast<uint16_t *>(o);
+    a.lse2 = lse2;
+    a.kbar = kbar;
+    a.certs = certs;
+    a.q_sb = shape->q_sb;
+    a.q_sh = shape->q_sh;
+    a.q_sn = shape->q_sn;
+    a.k_sb = shape->k_sb;
+    a.k_sh = shape->k_sh;
+    a.k_sn = shape->k_sn;
+    a.v_sb = shape->v_sb;
+    a.v_sh = shape->v_sh;
+    a.v_sn = shape->v_sn;
+    a.o_sb = shape->o_sb;
+    a.o_sh = shape->o_sh;
+    a.o_sn = shape->o_sn;
+    a.B = static_cast<int>(shape->B);
+    a.H = static_cast<int>(shape->H);
+    a.Nq = static_cast<int>(shape->Nq);
+    a.Nk = static_cast<int>(shape->Nk);
+    a.d = static_cast<int>(shape->d);
+    a.scale_log2 = scale_log2;
+    a.causal = causal;
+    a.variant = variant;
+    const int64_t tiles = shape->B * shape->H * div_up(shape->Nq, 256);
+    if (tiles > kMaxN) return CLIS_ERR_UNSUPPORTED;
+    return clis::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char *clis_status_string(clis_status_t s)
+{
+    switch (s) {
+    case CLIS_OK: return "ok";
+    case CLIS_ERR_INVALID_ARG: return "invalid argument";
+    case CLIS_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case CLIS_ERR_MISALIGNED: return "pointer or stride not 16-byte aligned";
+    case CLIS_ERR_WORKSPACE: return "workspace missing or too small";
+    case CLIS_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case CLIS_ERR_TIMEOUT: return "a kernel pipeline wait timed out";
+    }
+    return "unknown status";
+}
+
+clis_status_t clis_get_device_error(uint32_t *code)
+{
+    if (!code) return CLIS_ERR_INVALID_ARG;
+    return clis::read_device_error(code);
+}
+
+clis_status_t clis_clear_device_error(void) { return clis::clear_device_error(); }
+
+}  // extern "C"

@@ -1,0 +1,67 @@
+// clis_internal.h -- declarations shared by the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/clis.h"
+
+namespace clis {
+
+// ----------------------------------------------------------- certification
+
+constexpr int kCertChunkRows = 1024;  // rows per partial-reduction chunk
+constexpr int kCertThreads = 256;
+
+struct CertWorkspace {
+    float *ksum;       // [BH][nck][d]  per-chunk column sums of K
+    uint32_t *knorm2;  // [BH][nck]     per-chunk max of ||k - kbar||^2 (fp32 bits, rounded up)
+    uint32_t *qnorm2;  // [BH][ncq]     per-chunk max of ||q||^2 (fp32 bits, rounded up)
+    uint32_t *kabs;    // [BH][nck]     per-chunk max of |k| as bf16 bits (& 0x7FFF)
+    uint32_t *qabs;    // [BH][ncq]
+    uint32_t *vabs;    // [BH][nck]
+};
+
+struct CertArgs {
+    const uint16_t *q, *k, *v;  // bf16 bits
+    int64_t q_sb, q_sh, q_sn, k_sb, k_sh, k_sn, v_sb, v_sh, v_sn;
+    int B, H, Nq, Nk, d;
+    int nck, ncq;
+    float scale_log2;
+    int emax_exp, emax_acc;  // floor(U) of the exp2-output and accumulator formats
+    float *kbar;
+    clis_head_cert_t *certs;
+};
+
+// Carves the workspace for the given sizes; returns the bytes needed.
+size_t cert_workspace_layout(int64_t BH, int64_t nck, int64_t ncq, int64_t d, void *base,
+                             CertWorkspace *ws);
+
+cudaError_t launch_certify(const CertArgs &a, const CertWorkspace &ws, cudaStream_t stream);
+
+// ---------------------------------------------------------------- attention
+
+struct AttnArgs {
+    const uint16_t *q, *k, *v;
+    uint16_t *o;
+    float *lse2;
+    const float *kbar;
+    const clis_head_cert_t *certs;
+    int64_t q_sb, q_sh, q_sn, k_sb, k_sh, k_sn, v_sb, v_sh, v_sn, o_sb, o_sh, o_sn;
+    int B, H, Nq, Nk, d;
+    float scale_log2;
+    int causal;
+    int variant;
+};
+
+// Builds the tensor maps and launches the persistent attention kernel.
+// Returns CLIS_OK, CLIS_ERR_CUDA (tensor-map encode or launch failure).
+clis_status_t launch_attn_fwd(const AttnArgs &a, cudaStream_t stream);
+
+clis_status_t read_device_error(uint32_t *code);
+clis_status_t clear_device_error();
+
+}  // namespace clis

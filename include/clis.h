@@ -1,0 +1,159 @@
+/*
+ * clis.h -- C ABI of the CLiS attention-forward library (libclis.so), sm_103a.
+ *
+ * CLiS ("CLiS: Plug-and-Play Attention Acceleration for Video Diffusion on
+ * TPUs via Certified Stabilization", Tsai et al., 2026) fixes one softmax
+ * stabiliser per query row before the KV loop, so the fused attention kernel
+ * needs no running row maximum and no accumulator rescaling.  A per-head
+ * certificate (Algorithm 1) proves that doing so cannot overflow; heads that
+ * fail certification run standard online softmax instead (abstract).
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are bf16 in layout [B, H, N, d] with element strides given in
+ *    clis_shape_t; the d dimension is contiguous (stride 1).
+ *  - Device pointers must be 16-byte aligned and every stride (n, h, b) a
+ *    multiple of 8 elements (16 bytes); otherwise CLIS_ERR_MISALIGNED.
+ *  - d must be 64 or 128 (CLIS_ERR_UNSUPPORTED otherwise).
+ *  - The caller owns every buffer.  The library allocates no device memory;
+ *    scratch space is passed in as `workspace`.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and never synchronise the host.  The returned status
+ *    covers argument checks and launch errors only: on any argument error
+ *    nothing is launched.  Faults found inside a kernel (a pipeline wait
+ *    that exceeded its time limit) are recorded in a device-side error word
+ *    read by clis_get_device_error().
+ *  - All results are deterministic: no floating-point atomics, fixed
+ *    reduction orders.
+ */
+#ifndef CLIS_H
+#define CLIS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CLIS_API __attribute__((visibility("default")))
+#else
+#define CLIS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle, ABI-compatible with cudaStream_t. */
+typedef struct CUstream_st *clis_stream_t;
+
+typedef enum {
+    CLIS_OK = 0,
+    CLIS_ERR_INVALID_ARG = 1,  /* null pointer, negative/zero size, bad enum, non-finite or <= 0 scale */
+    CLIS_ERR_UNSUPPORTED = 2,  /* head dim not in {64, 128}, causal with Nq != Nk, sizes beyond int32 */
+    CLIS_ERR_MISALIGNED = 3,   /* pointer not 16-byte aligned or stride not a multiple of 8 elements */
+    CLIS_ERR_WORKSPACE = 4,    /* workspace null or smaller than clis_certify_workspace_size() */
+    CLIS_ERR_CUDA = 5,         /* a CUDA runtime/driver call or a kernel launch failed */
+    CLIS_ERR_TIMEOUT = 6       /* a kernel pipeline wait exceeded its limit (device error word) */
+} clis_status_t;
+
+/* Floating-point formats of Figure 3 ("Approximate numerical limits of
+ * exp2(x) = 2^x for FP16, BF16, and FP32").  U_exp and U_acc of Algorithm 1
+ * step 7 are the exp2 overflow limits of these formats. */
+typedef enum { CLIS_FMT_FP16 = 0, CLIS_FMT_BF16 = 1, CLIS_FMT_FP32 = 2 } clis_fmt_t;
+
+/* Which softmax the attention kernel runs per head:
+ *  CLIS_AUTO              certified heads use the fixed stabiliser, the rest
+ *                         fall back to online softmax (abstract: "falling back
+ *                         to online softmax when certification fails");
+ *  CLIS_ONLINE            every head uses online softmax (the baseline);
+ *  CLIS_CERTIFIED_FORCED  every head uses the fixed stabiliser, ignoring the
+ *                         flags (benchmarks and tests only: output of a head
+ *                         that did not certify is then unspecified). */
+typedef enum { CLIS_AUTO = 0, CLIS_ONLINE = 1, CLIS_CERTIFIED_FORCED = 2 } clis_variant_t;
+
+/* Problem shape and element strides (elements, not bytes).  K and V share
+ * Nk; Q and O share Nq.  O strides are ignored by clis_certify. */
+typedef struct {
+    int64_t B, H, Nq, Nk, d;
+    int64_t q_sb, q_sh, q_sn;
+    int64_t k_sb, k_sh, k_sn;
+    int64_t v_sb, v_sh, v_sn;
+    int64_t o_sb, o_sh, o_sn;
+} clis_shape_t;
+
+/* Per-head certificate, Algorithm 1 (one per (b, h) pair, index b*H + h).
+ *  certified  1 if every input of the head is finite and B_h <= C
+ *  G          step 5: ceil(log2 max(1, max |V|))
+ *  A          step 6: ceil(log2 Nk) + G
+ *  C          step 7: min(floor(U_exp), ceil(U_acc - A) - 1)
+ *  reason     0 certified, 1 B_h > C, 2 a non-finite value in Q, K or V
+ *             (then G = A = C = 0 and B_h = +inf)
+ *  B_h        step 4 with BoundUp(q, kappa) = scale_log2 * ||q||_2 * kappa,
+ *             rounded upward (exp2-argument units)
+ *  kappa      step 3: an upper bound on max_r ||k_r - kbar||_2 computed
+ *             with upward rounding about the kbar returned by clis_certify
+ *  qmax       an upper bound on max_r ||q_r||_2 */
+typedef struct {
+    int32_t certified, G, A, C, reason;
+    float B_h, kappa, qmax;
+} clis_head_cert_t;
+
+/* Bytes of device workspace clis_certify needs for this shape.
+ * Host-only; never touches the GPU.  Errors: CLIS_ERR_INVALID_ARG for a
+ * null argument or a negative size. */
+CLIS_API clis_status_t clis_certify_workspace_size(const clis_shape_t *shape, size_t *bytes);
+
+/* Certification pre-pass, Algorithm 1 steps 1-7 plus the decision, for all
+ * B*H heads (paper: Algorithm 1 "CLiS forward pass for one dense attention
+ * head", steps 1-7; the decision after step 7 is lost from the text and is
+ * read here as "finite inputs and B_h <= C").
+ *   q, k, v     device bf16 [B,H,Nq,d] / [B,H,Nk,d] / [B,H,Nk,d]
+ *   scale_log2  softmax scale times log2(e) (> 0, finite); scores enter
+ *               exp2 as scale_log2 * q.k
+ *   exp_fmt     format that holds exp2 outputs (U_exp); the attention
+ *               kernel feeds P to the tensor cores as BF16
+ *   acc_fmt     accumulator format (U_acc); the kernel accumulates in FP32
+ *   kbar        device fp32 out [B*H, d]: step 1 key mean, round-to-nearest
+ *   certs       device out [B*H]
+ *   workspace   device scratch of at least clis_certify_workspace_size()
+ *               bytes, 256-byte aligned; contents need no initialisation
+ * Launches four kernels on `stream`.  Nk must be >= 1; Nq may be 0. */
+CLIS_API clis_status_t clis_certify(const clis_shape_t *shape, const void *q, const void *k,
+                           const void *v, float scale_log2, clis_fmt_t exp_fmt,
+                           clis_fmt_t acc_fmt, float *kbar, clis_head_cert_t *certs,
+                           void *workspace, size_t ws_bytes, clis_stream_t stream);
+
+/* Fused attention forward O = softmax(scale * Q K^T) V (paper: abstract and
+ * Figure 5(a), "a loop-invariant stabilizer mu_i removes the reduction and
+ * rescaling chain").  One persistent kernel; each 256-row query block of a
+ * head runs either
+ *   - the certified path: mu_i = scale_log2 * (q_i . kbar) fixed before the
+ *     KV loop, p_ij = exp2(scale_log2 * s_ij - mu_i), no row maximum, no
+ *     rescaling; or
+ *   - the online path: running row maximum and accumulator rescaling.
+ *   o       device bf16 out [B,H,Nq,d] (strides from shape)
+ *   lse2    optional device fp32 out [B*H*Nq] (contiguous, index
+ *           (b*H + h)*Nq + i): log2 sum_j exp2(scale_log2 * s_ij); NULL = skip
+ *   kbar, certs  outputs of clis_certify (may be NULL for CLIS_ONLINE)
+ *   causal  0 or 1; 1 requires Nq == Nk (key j visible to query i iff j <= i)
+ * Nq == 0 or B*H == 0 launches nothing and returns CLIS_OK. */
+CLIS_API clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, const void *k,
+                            const void *v, void *o, float *lse2, const float *kbar,
+                            const clis_head_cert_t *certs, float scale_log2, int causal,
+                            clis_variant_t variant, clis_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+CLIS_API const char *clis_status_string(clis_status_t status);
+
+/* Reads the device error word of the current device (synchronises the
+ * device).  *code = 0 when no kernel recorded a fault; otherwise bit flags of
+ * the pipeline waits that timed out.  Returns CLIS_ERR_TIMEOUT if *code != 0,
+ * CLIS_ERR_CUDA if the read failed. */
+CLIS_API clis_status_t clis_get_device_error(uint32_t *code);
+
+/* Resets the device error word of the current device to 0 (synchronous). */
+CLIS_API clis_status_t clis_clear_device_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CLIS_H */

@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+symbol include/clis.h declares, and rejects bad arguments with the documented
+status codes before touching the GPU (every call here fails validation, so
+nothing is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "clis.h")
+
+
+@pytest.fixture(scope="module")
+def clis():
+    from certified_fixed_stabilizer_gb300 import clis as mod
+    return mod
+
+
+def _declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"CLIS_API\s+[\w\s\*]*?\b(clis_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_symbols()
+    for n in ("clis_certify_workspace_size", "clis_certify", "clis_attn_fwd", "clis_status_string",
+              "clis_get_device_error", "clis_clear_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(clis):
+    lib = ctypes.CDLL(clis.library_path())
+    for n in _declared_symbols():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(clis):
+    for code in range(7):
+        s = clis.clis_status_string(code)
+        assert isinstance(s, str) and s and s != "unknown status"
+    assert clis.clis_status_string(99) == "unknown status"
+
+
+def _shape(clis, B=1, H=2, Nq=300, Nk=300, d=128):
+    s = clis.Shape(B=B, H=H, Nq=Nq, Nk=Nk, d=d)
+    for t in "qkvo":
+        setattr(s, f"{t}_sn", d)
+        setattr(s, f"{t}_sh", (Nq if t in "qo" else Nk) * d)
+        setattr(s, f"{t}_sb", H * (Nq if t in "qo" else Nk) * d)
+    return s
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def _certify(clis, shape, q=FAKE, k=FAKE, v=FAKE, scale=0.1, ef=1, af=2, kbar=FAKE, certs=FAKE,
+             ws=FAKE, ws_bytes=1 << 30):
+    lib = clis.load_library()
+    vp = ctypes.c_void_p
+    return lib.clis_certify(ctypes.byref(shape) if shape is not None else None, vp(q), vp(k), vp(v), scale,
+                            ef, af, vp(kbar), vp(certs), vp(ws), ws_bytes, None)
+
+
+def _attn(clis, shape, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse2=None, kbar=FAKE, certs=FAKE, scale=0.1,
+          causal=0, variant=0):
+    lib = clis.load_library()
+    vp = ctypes.c_void_p
+    return lib.clis_attn_fwd(ctypes.byref(shape) if shape is not None else None, vp(q), vp(k), vp(v), vp(o),
+                             vp(lse2), vp(kbar), vp(certs), scale, causal, variant, None)
+
+
+def test_workspace_size_is_host_only_and_grows(clis):
+    a = clis.clis_certify_workspace_size(_shape(clis, Nk=1000))
+    b = clis.clis_certify_workspace_size(_shape(clis, Nk=100000))
+    assert 0 < a < b
+    assert a % 256 == 0
+
+
+def test_certify_rejects_bad_arguments(clis):
+    OK_INVALID, UNSUP, MIS, WS = 1, 2, 3, 4
+    assert _certify(clis, None) == OK_INVALID
+    assert _certify(clis, _shape(clis), q=0) == OK_INVALID
+    assert _certify(clis, _shape(clis), scale=0.0) == OK_INVALID
+    assert _certify(clis, _shape(clis), scale=float("nan")) == OK_INVALID
+    assert _certify(clis, _shape(clis), scale=-1.0) == OK_INVALID
+    assert _certify(clis, _shape(clis), ef=7) == OK_INVALID
+    assert _certify(clis, _shape(clis, Nk=0)) == OK_INVALID
+    assert _certify(clis, _shape(clis, d=96)) == UNSUP
+    assert _certify(clis, _shape(clis), k=FAKE + 8) == MIS
+    s = _shape(clis)
+    s.k_sn = 132
+    assert _certify(clis, s) == MIS
+    assert _certify(clis, _shape(clis), ws=0) == WS
+    assert _certify(clis, _shape(clis), ws_bytes=16) == WS
+    assert _certify(clis, _shape(clis), ws=FAKE + 16) == MIS
+
+
+def test_attn_rejects_bad_arguments(clis):
+    INV, UNSUP, MIS = 1, 2, 3
+    assert _attn(clis, None) == INV
+    assert _attn(clis, _shape(clis), o=0) == INV
+    assert _attn(clis, _shape(clis), kbar=0) == INV               # AUTO needs kbar
+    assert _attn(clis, _shape(clis), certs=0) == INV              # AUTO needs certificates
+    assert _attn(clis, _shape(clis), certs=0, variant=2, scale=0) == INV
+    assert _attn(clis, _shape(clis), variant=5) == INV
+    assert _attn(clis, _shape(clis), causal=2) == INV
+    assert _attn(clis, _shape(clis, Nq=300, Nk=400), causal=1) == UNSUP
+    assert _attn(clis, _shape(clis, d=256)) == UNSUP
+    assert _attn(clis, _shape(clis), o=FAKE + 2) == MIS
+    assert _attn(clis, _shape(clis), lse2=FAKE + 2) == MIS
+    s = _shape(clis)
+    s.o_sn = 129
+    assert _attn(clis, s) == INV or _attn(clis, s) == MIS
+    s = _shape(clis)
+    s.q_sh = 12
+    assert _attn(clis, s) == MIS
+
+
+def test_binding_has_no_cpu_fallback(clis):
+    """The binding exposes only library calls: no torch or numpy attention."""
+    src = open(os.path.join(ROOT, "certified_fixed_stabilizer_gb300", "clis.py")).read()
+    assert "oracle" not in src
+    assert "softmax" not in src.replace("softmax_scale", "")

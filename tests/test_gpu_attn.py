@@ -1,0 +1,182 @@
+"""GPU attention forward vs the fp64 oracle, through the C ABI.
+
+Bar (per head, errors divided by max(1, max |O_ref|)): max-abs <= 1e-2 and
+mean-abs <= 1e-3 against the fp64 two-pass softmax; the certified (CLiS) and
+online paths must also agree with each other on certified heads.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from certified_fixed_stabilizer_gb300 import clis
+from certified_fixed_stabilizer_gb300.workloads import (WORKLOADS, injected_heads, make_inputs,
+                                                        sample_rows)
+from gpu_util import MAX_ABS, MEAN_ABS, assert_close_to_oracle, flat, head_errors, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    need_gpu()
+    oracle.set_num_threads(os.cpu_count() or 1)
+    clis.clis_clear_device_error()
+    yield
+    assert clis.clis_get_device_error() == 0
+
+
+def _run(q, k, v, causal, variant, lse2=False, softmax_scale=None):
+    sl2 = clis.scale_log2_for(q.shape[-1], softmax_scale)
+    kbar, certs = clis.clis_certify(q, k, v, sl2)
+    l2 = None
+    if lse2:
+        l2 = torch.full((q.shape[0] * q.shape[1] * q.shape[2],), float("nan"), device=q.device)
+    out = clis.clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=causal, variant=variant, lse2=l2)
+    torch.cuda.synchronize()
+    return out, l2, certs
+
+
+def _oracle(q, k, v, causal, rows=None, softmax_scale=None):
+    scale = (1.0 / np.sqrt(q.shape[-1])) if softmax_scale is None else softmax_scale
+    return oracle.attention(flat(q), flat(k), flat(v), scale, causal=causal, rows=rows, with_lse2=True)
+
+
+@pytest.mark.parametrize("variant", ["auto", "online", "certified"])
+def test_tiny_full_parity(variant):
+    dev = need_gpu()
+    w = WORKLOADS["tiny"]
+    q, k, v = make_inputs(w, device=dev)
+    out, l2, certs = _run(q, k, v, w.causal, variant, lse2=True)
+    ref, rlse = _oracle(q, k, v, w.causal)
+    assert_close_to_oracle(out.float().cpu().numpy(), ref, f"tiny/{variant}")
+    np.testing.assert_allclose(l2.cpu().numpy().reshape(rlse.shape), rlse, atol=1e-3, rtol=0)
+    assert all(c["certified"] for c in clis.decode_certs(certs))
+
+
+@pytest.mark.parametrize("name,rows_per_head", [("480p", 48), ("720p", 24), ("mixed", 48), ("causal", 64)])
+def test_workload_sampled_parity(name, rows_per_head):
+    """Full-size workloads, the launch configuration the benchmark times;
+    the oracle evaluates seed-chosen rows (always 0, N-1 and the ragged tail)."""
+    dev = need_gpu()
+    w = WORKLOADS[name]
+    q, k, v = make_inputs(w, device=dev)
+    rows = sample_rows(w.N, rows_per_head, seed=1)
+    ref, rlse = _oracle(q, k, v, w.causal, rows=rows)
+    for variant in ("auto", "online"):
+        out, l2, certs = _run(q, k, v, w.causal, variant, lse2=True)
+        got = flat(out)[:, rows].float().cpu().numpy()
+        assert_close_to_oracle(got, ref, f"{name}/{variant}")
+        g2 = l2.reshape(w.heads, w.N)[:, rows].cpu().numpy()
+        np.testing.assert_allclose(g2, rlse, atol=2e-3, rtol=0)
+        assert torch.isfinite(out).all()
+        if variant == "auto":
+            auto_out = out
+    flags = [c["certified"] for c in clis.decode_certs(certs)]
+    if name == "mixed":
+        assert sum(flags) == 48
+        for h in injected_heads(w):
+            assert flags[h] == 0
+    else:
+        assert all(flags)
+    # certified and online paths agree on certified heads (whole tensors)
+    cert_heads = [h for h, f in enumerate(flags) if f]
+    a = flat(auto_out)[cert_heads].float()
+    b = flat(out)[cert_heads].float()
+    diff = (a - b).abs()
+    assert diff.max().item() <= MAX_ABS and diff.mean().item() <= MEAN_ABS
+
+
+CASES = [
+    # (B, H, Nq, Nk, d, causal)
+    (1, 2, 1, 1, 64, False),
+    (1, 2, 1, 1, 128, True),
+    (2, 3, 129, 129, 64, True),
+    (1, 2, 257, 1000, 128, False),
+    (1, 2, 1000, 257, 128, False),
+    (2, 2, 700, 700, 128, True),
+    (1, 3, 513, 513, 64, False),
+    (1, 1, 2000, 2000, 128, True),
+    (3, 1, 300, 4097, 64, False),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal", CASES)
+@pytest.mark.parametrize("variant", ["auto", "online"])
+def test_ragged_shapes(B, H, Nq, Nk, d, causal, variant):
+    dev = need_gpu()
+    g = torch.Generator(device=dev)
+    g.manual_seed(B * 1000003 + H * 1009 + Nq * 31 + Nk + d)
+    q = torch.randn(B, H, Nq, d, generator=g, device=dev).to(torch.bfloat16)
+    k = (torch.randn(B, H, Nk, d, generator=g, device=dev) + torch.randn(d, generator=g, device=dev)).to(
+        torch.bfloat16)
+    v = torch.randn(B, H, Nk, d, generator=g, device=dev).to(torch.bfloat16)
+    out, l2, _ = _run(q, k, v, causal, variant, lse2=True)
+    ref, rlse = _oracle(q, k, v, causal)
+    assert_close_to_oracle(out.float().cpu().numpy(), ref, f"{(B, H, Nq, Nk, d, causal)}/{variant}")
+    np.testing.assert_allclose(l2.cpu().numpy().reshape(rlse.shape), rlse, atol=2e-3, rtol=0)
+
+
+def test_strided_tensors_and_guard_bands():
+    """Q/K/V/O stored as [B, N, H, d] (non-default strides) with O inside a larger
+    buffer whose canary bytes must survive: no write outside O's rows."""
+    dev = need_gpu()
+    B, H, N, d = 2, 3, 777, 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    q = torch.randn(B, N, H, d, generator=g, device=dev).to(torch.bfloat16).permute(0, 2, 1, 3)
+    k = (torch.randn(B, N, H, d, generator=g, device=dev) + 2).to(torch.bfloat16).permute(0, 2, 1, 3)
+    v = torch.randn(B, N, H, d, generator=g, device=dev).to(torch.bfloat16).permute(0, 2, 1, 3)
+    pad = 4096
+    canary = torch.full((pad * 2 + B * N * H * d,), -12345.0, device=dev).to(torch.bfloat16)
+    o = canary[pad:pad + B * N * H * d].view(B, N, H, d).permute(0, 2, 1, 3)
+    o.fill_(0)
+    sl2 = clis.scale_log2_for(d)
+    kbar, certs = clis.clis_certify(q, k, v, sl2)
+    clis.clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, out=o)
+    torch.cuda.synchronize()
+    assert torch.all(canary[:pad] == -12345.0) and torch.all(canary[-pad:] == -12345.0)
+    ref, _ = _oracle(q, k, v, False)
+    assert_close_to_oracle(o.float().cpu().numpy().reshape(ref.shape), ref, "strided")
+
+
+def test_empty_query_launches_nothing():
+    dev = need_gpu()
+    q = torch.empty(1, 2, 0, 64, dtype=torch.bfloat16, device=dev)
+    k = torch.randn(1, 2, 10, 64, device=dev).to(torch.bfloat16)
+    out = clis.clis_attn_fwd(q, k, k, clis.scale_log2_for(64), variant="online")
+    assert out.shape == q.shape
+
+
+def test_softmax_scale_is_honoured():
+    dev = need_gpu()
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    q = torch.randn(1, 2, 300, 64, generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn(1, 2, 300, 64, generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn(1, 2, 300, 64, generator=g, device=dev).to(torch.bfloat16)
+    out, _, _ = _run(q, k, v, False, "auto", softmax_scale=0.5)
+    ref, _ = _oracle(q, k, v, False, softmax_scale=0.5)
+    assert_close_to_oracle(out.float().cpu().numpy(), ref, "scale=0.5")
+
+
+def test_host_tensors_end_to_end():
+    """The public attention() call with pinned host tensors (the e2e path)."""
+    need_gpu()
+    w = WORKLOADS["tiny"]
+    q, k, v = (t.pin_memory() for t in make_inputs(w, device="cpu"))
+    out = clis.attention(q, k, v)
+    assert out.device.type == "cpu"
+    ref, _ = _oracle(q, k, v, False)
+    assert_close_to_oracle(out.float().numpy(), ref, "host e2e")
+
+
+def test_outputs_are_deterministic():
+    dev = need_gpu()
+    w = WORKLOADS["mixed"]
+    q, k, v = make_inputs(w, device=dev, N=3000)
+    a, _, _ = _run(q, k, v, False, "auto")
+    b, _, _ = _run(q, k, v, False, "auto")
+    assert torch.equal(a, b)
