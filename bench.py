@@ -1,0 +1,384 @@
+"""Benchmark of the CLiS attention-forward hot path on GB300.
+
+One step = the whole path over one batch of synthetic inputs resident in HBM:
+clis_certify (Algorithm 1, four kernels) + clis_attn_fwd (AUTO: certified
+heads on the fixed-stabiliser path, the rest on online softmax).  The metric
+is attention-forward TFLOP/s, FLOP = 4 B H Nq Nk d (halved for causal).
+
+Prints ONE JSON line (rank 0).  Default workload: the 720p Wan-2.2-shaped DiT
+self-attention (B=1, H=40, N=75,600, d=128, non-causal).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...   # the CPU fp64 oracle on a sample
+
+Under torchrun each rank runs its own copy of the workload on its own GPU
+(heads are independent: no collective on the data path; weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from certified_fixed_stabilizer_gb300.workloads import WORKLOADS, make_inputs, sample_rows  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "attention fwd TFLOP/s (BF16, 1xGB300); CLiS step = certification + fused attention (AUTO)"
+
+
+def config_dict(w, H, variant):
+    in_bytes = 3 * w.B * H * w.N * w.d * 2
+    l2 = ("flushed between steps (256 MB write)" if in_bytes < 2 * L2_BYTES
+          else "inputs larger than L2 (Q, K, V %.0f MB each)" % (in_bytes / 3 / 1e6))
+    return {"workload": workload_desc(w, H), "B": w.B, "H": H, "N": w.N, "d": w.d,
+            "causal": w.causal, "variant": variant, "seed": w.seed, "l2": l2}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="720p", choices=sorted(WORKLOADS))
+    ap.add_argument("--heads", type=int, default=None, help="override H (profiling runs)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--variant", default="auto", choices=["auto", "online", "certified"])
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the online-variant, e2e and CPU-baseline legs (profiling runs)")
+    return ap.parse_args()
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_desc(w, H):
+    return (f"{w.name}: B={w.B} H={H} N={w.N} d={w.d} causal={w.causal} "
+            f"({w.note})")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------------ CPU legs
+
+def oracle_sample_step(q, k, v, w, heads, rows):
+    """Oracle work for one sampled step: certification of the sampled heads
+    (full length) and attention on `rows` of each sampled head."""
+    import oracle
+    from certified_fixed_stabilizer_gb300.clis import LOG2E
+    sl2 = w.softmax_scale() * LOG2E
+    qs, ks, vs = (t.reshape(-1, t.shape[2], t.shape[3])[heads] for t in (q, k, v))
+    oracle.certify(qs, ks, vs, sl2)
+    oracle.attention(qs, ks, vs, w.softmax_scale(), causal=w.causal, rows=rows)
+
+
+def sample_flops(w, n_heads, rows):
+    if w.causal:
+        return sum(4.0 * (r + 1) * w.d for r in rows) * n_heads
+    return 4.0 * len(rows) * w.N * w.d * n_heads
+
+
+def cpu_sample_plan(q, k, v, w, target_s):
+    """Pick a bounded sample (heads 0..1, seed-chosen rows) taking about target_s."""
+    import oracle
+    oracle.build()
+    oracle.set_num_threads(os.cpu_count() or 1)
+    heads = [0, 1] if w.heads > 1 else [0]
+    probe = sample_rows(w.N, 32, seed=2)
+    t0 = time.perf_counter()
+    oracle_sample_step(q, k, v, w, heads, probe)
+    dt = time.perf_counter() - t0
+    n = int(min(w.N, max(32, 32 * target_s / max(dt, 1e-3))))
+    return heads, sample_rows(w.N, n, seed=2)
+
+
+def run_reference(args, w, H):
+    """--impl reference: the CPU oracle, as it stands, on a bounded sample."""
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import oracle
+    q, k, v = make_inputs(w, device="cuda" if torch.cuda.is_available() else "cpu", H=H)
+    q, k, v = (t.cpu() for t in (q, k, v))
+    heads, rows = cpu_sample_plan(q, k, v, w, target_s=4.0)
+    for _ in range(args.warmup):
+        oracle_sample_step(q, k, v, w, heads, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_step(q, k, v, w, heads, rows)
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = sample_flops(w, len(heads), rows)
+    val = flops / dt / 1e12
+    sample = (f"certification of heads {heads} over all {w.N} keys + attention rows "
+              f"({len(rows)} seed-chosen query rows per head incl. 0 and N-1) of those heads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w, H, args.variant),
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU legs
+
+def main():
+    args = parse()
+    w = WORKLOADS[args.config]
+    H = args.heads or w.H
+    if args.impl == "reference":
+        return run_reference(args, w, H)
+
+    from certified_fixed_stabilizer_gb300 import clis
+    ws, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    q, k, v = make_inputs(w, device=dev, H=H)
+    heads = w.B * H
+    flops = w.flops() * H / w.H
+    sl2 = clis.scale_log2_for(w.d)
+    shape = clis.make_shape(q, k, v)
+    kbar = torch.empty((heads, w.d), dtype=torch.float32, device=dev)
+    certs = torch.empty((heads, clis.CERT_WORDS), dtype=torch.int32, device=dev)
+    wsp = torch.empty(max(256, clis.clis_certify_workspace_size(shape)), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    in_bytes = 3 * q.numel() * q.element_size()
+    needs_flush = in_bytes < 2 * L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if needs_flush else None
+
+    def step(variant):
+        if variant != "online":
+            clis.clis_certify(q, k, v, sl2, kbar=kbar, certs=certs, workspace=wsp)
+        clis.clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=w.causal, variant=variant, out=out)
+
+    def timed_loop(variant, steps, warmup):
+        for _ in range(warmup):
+            step(variant)
+        torch.cuda.synchronize()
+        barrier(ws)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e0, e1, e2 in ev:
+            if flush_buf is not None:
+                flush_buf.zero_()
+            e0.record(stream)
+            if variant != "online":
+                clis.clis_certify(q, k, v, sl2, kbar=kbar, certs=certs, workspace=wsp)
+            e1.record(stream)
+            clis.clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=w.causal, variant=variant,
+                               out=out)
+            e2.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        torch.cuda.synchronize()
+        step_ms = [e0.elapsed_time(e2) for e0, _, e2 in ev]
+        cert_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev]
+        attn_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev]
+        return sum(step_ms), cert_ms, attn_ms
+
+    clis.clis_clear_device_error()
+    with ClockSampler(local) as cs:
+        total_ms, cert_ms, attn_ms = timed_loop(args.variant, args.steps, args.warmup)
+    clocks = cs.summary()
+    total_ms = max_over_ranks(total_ms, ws)
+    ms_per_step = total_ms / args.steps
+    value = ws * flops / (ms_per_step * 1e-3) / 1e12
+    attn_avg_ms = statistics.mean(attn_ms)
+    cert_avg_ms = statistics.mean(cert_ms)
+    n_cert = sum(c["certified"] for c in clis.decode_certs(certs))
+    dev_err = clis.clis_get_device_error()
+
+    peaks, peak_src = measured_peaks()
+    peak_tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    achieved = flops / (attn_avg_ms * 1e-3) / 1e12
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            tinfo = json.load(f)
+        if tinfo.get("config") == args.config and tinfo.get("kernel_rev") == kernel_rev():
+            traffic = tinfo.get("bytes_per_launch")
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(w, H, args.variant),
+        "gpu_launches": args.steps * (5 if args.variant != "online" else 1),
+        "certified_heads": f"{n_cert}/{heads}",
+        "device_error_word": dev_err,
+        "attention_only": {"value": achieved, "unit": "TFLOP/s", "ms": attn_avg_ms},
+        "certify": {"ms": cert_avg_ms,
+                    "gbs_algorithmic": in_bytes / (cert_avg_ms * 1e-3) / 1e9,
+                    "gbs_moved": (in_bytes * 4 / 3) / (cert_avg_ms * 1e-3) / 1e9},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": traffic,
+                     "kernel": "attn_fwd_kernel<128,%s>" % ("true" if w.causal else "false"),
+                     "peak_source": f"{peak_src} bf16_tflops_sustained (cuBLAS, seconds-long loop)"},
+        "clocks": clocks,
+    }
+
+    if not args.no_extras:
+        # Online-softmax baseline (same kernel skeleton, every head on the online path).
+        on_total, _, on_attn = timed_loop("online", args.steps, args.warmup)
+        line["online"] = {"value": flops / (statistics.mean(on_attn) * 1e-3) / 1e12, "unit": "TFLOP/s",
+                          "ms": statistics.mean(on_attn)}
+        line["certified_speedup_vs_online"] = statistics.mean(on_attn) / attn_avg_ms
+        # End to end through the public call with pinned host buffers.
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        oh = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+
+        def e2e_step():
+            dq.copy_(qh, non_blocking=True)
+            dk.copy_(kh, non_blocking=True)
+            dv.copy_(vh, non_blocking=True)
+            clis.clis_certify(dq, dk, dv, sl2, kbar=kbar, certs=certs, workspace=wsp)
+            clis.clis_attn_fwd(dq, dk, dv, sl2, kbar=kbar, certs=certs, causal=w.causal, variant=args.variant,
+                               out=out)
+            oh.copy_(out, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(args.steps, 5))
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, ws)
+        line["e2e"] = {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out.numel() * out.element_size(),
+                       "ms_per_step": e2e_ms}
+        del qh, kh, vh, oh, dq, dk, dv
+        if rank == 0 and ws == 1:
+            import oracle
+            qc, kc, vc = (t.cpu() for t in (q, k, v))
+            hs, rows = cpu_sample_plan(qc, kc, vc, w, target_s=15.0)
+            t0 = time.perf_counter()
+            oracle_sample_step(qc, kc, vc, w, hs, rows)
+            dt = time.perf_counter() - t0
+            line["cpu_baseline"] = {
+                "value": sample_flops(w, len(hs), rows) / dt / 1e12, "unit": "TFLOP/s",
+                "cores": oracle.num_threads(), "kind": "oracle",
+                "sample": (f"heads {hs}: certification over all {w.N} keys + attention for "
+                           f"{len(rows)} seed-chosen query rows per head; {dt:.1f} s")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def kernel_rev() -> str:
+    """Hash of the attention kernel source: a stored traffic figure only applies
+    to the kernel it was captured from."""
+    import hashlib
+    p = os.path.join(ROOT, "certified_fixed_stabilizer_gb300", "csrc", "attn_fwd.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+if __name__ == "__main__":
+    main()

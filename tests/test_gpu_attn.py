@@ -14,7 +14,7 @@ import oracle
 from certified_fixed_stabilizer_gb300 import clis
 from certified_fixed_stabilizer_gb300.workloads import (WORKLOADS, injected_heads, make_inputs,
                                                         sample_rows)
-from gpu_util import MAX_ABS, MEAN_ABS, assert_close_to_oracle, flat, head_errors, need_gpu
+from gpu_util import assert_close_to_oracle, assert_paths_agree, flat, need_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -83,10 +83,7 @@ def test_workload_sampled_parity(name, rows_per_head):
         assert all(flags)
     # certified and online paths agree on certified heads (whole tensors)
     cert_heads = [h for h, f in enumerate(flags) if f]
-    a = flat(auto_out)[cert_heads].float()
-    b = flat(out)[cert_heads].float()
-    diff = (a - b).abs()
-    assert diff.max().item() <= MAX_ABS and diff.mean().item() <= MEAN_ABS
+    assert_paths_agree(flat(auto_out)[cert_heads], flat(out)[cert_heads], name)
 
 
 CASES = [
