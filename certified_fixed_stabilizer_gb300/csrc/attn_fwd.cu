@@ -24,6 +24,7 @@
 //               through an NSTAGE-deep shared-memory ring
 //   warp 13     MMA issuer: S = Q K^T (SMEM x SMEM -> TMEM) and
 //               O += P V (P from TMEM, V from SMEM -> TMEM); owns TMEM
+//   (warps 12 and 13 run warp-uniform code; one elected lane issues)
 //
 // TMEM (512 columns x 128 lanes x 32 bit): S0 @0, S1 @128 (fp32 scores,
 // overwritten in place by P as packed bf16 in their first 64 columns),
@@ -134,6 +135,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
 }
 
 // ------------------------------------------------------------------ producer
+//
+// Runs on all 32 lanes of its warp (warp-uniform control flow); one elected
+// lane issues the copies.
 
 template <int D, bool CAUSAL>
 __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
@@ -142,6 +146,7 @@ __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, 
     using C = Cfg<D>;
     volatile int *ab = &c.abort_flag;
     unsigned *err = &g_attn_error_word;
+    const bool leader = elect_one();
     const uint64_t pol_kv = policy_evict_last();
     const uint64_t pol_q = policy_evict_first();
     uint32_t it = 0;
@@ -150,14 +155,17 @@ __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, 
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
         const Tile T = decode_tile<CAUSAL>(p, tile);
         for (int t = 0; t < 2; t++) {
-            if (!mbar_wait(smem_u32(&c.q_empty[t]), (w & 1) ^ 1, ab, err, kErrProducer)) goto abort;
-            const uint32_t bar = smem_u32(&c.q_full[t]);
-            mbar_arrive_expect_tx(bar, C::TILE_BYTES);
-            const int row = T.qb * 2 * BM + t * BM;
+            if (!mbar_wait_warp(smem_u32(&c.q_empty[t]), (w & 1) ^ 1, ab, err, kErrProducer)) goto abort;
+            if (leader) {
+                const uint32_t bar = smem_u32(&c.q_full[t]);
+                mbar_arrive_expect_tx(bar, C::TILE_BYTES);
+                const int row = T.qb * 2 * BM + t * BM;
 #pragma unroll
-            for (int bx = 0; bx < C::NBOX; bx++)
-                tma_load_4d_hint(sQ0 + t * C::TILE_BYTES + bx * C::BOX_BYTES, tm_q, bar, bx * 64, row, T.h, T.b,
-                                 pol_q);
+                for (int bx = 0; bx < C::NBOX; bx++)
+                    tma_load_4d_hint(sQ0 + t * C::TILE_BYTES + bx * C::BOX_BYTES, tm_q, bar, bx * 64, row, T.h,
+                                     T.b, pol_q);
+            }
+            __syncwarp();
         }
         q_issued = w;
         for (int j = 0; j < T.n_kv; j++) {
@@ -165,14 +173,17 @@ __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, 
             for (int kv = 0; kv < 2; kv++) {
                 const uint32_t stage = it % C::NSTAGE;
                 const uint32_t ph = (it / C::NSTAGE) & 1;
-                if (!mbar_wait(smem_u32(&c.kv_empty[stage]), ph ^ 1, ab, err, kErrProducer)) goto abort;
-                const uint32_t bar = smem_u32(&c.kv_full[stage]);
-                mbar_arrive_expect_tx(bar, C::TILE_BYTES);
-                const CUtensorMap *tm = kv ? tm_v : tm_k;
+                if (!mbar_wait_warp(smem_u32(&c.kv_empty[stage]), ph ^ 1, ab, err, kErrProducer)) goto abort;
+                if (leader) {
+                    const uint32_t bar = smem_u32(&c.kv_full[stage]);
+                    mbar_arrive_expect_tx(bar, C::TILE_BYTES);
+                    const CUtensorMap *tm = kv ? tm_v : tm_k;
 #pragma unroll
-                for (int bx = 0; bx < C::NBOX; bx++)
-                    tma_load_4d_hint(sKV + stage * C::TILE_BYTES + bx * C::BOX_BYTES, tm, bar, bx * 64, j * BN,
-                                     T.h, T.b, pol_kv);
+                    for (int bx = 0; bx < C::NBOX; bx++)
+                        tma_load_4d_hint(sKV + stage * C::TILE_BYTES + bx * C::BOX_BYTES, tm, bar, bx * 64,
+                                         j * BN, T.h, T.b, pol_kv);
+                }
+                __syncwarp();
                 ++it;
             }
         }
@@ -187,17 +198,18 @@ abort:
 }
 
 // ----------------------------------------------------------------------- MMA
+//
+// Also warp-uniform: descriptors are built by every lane (so they stay in
+// uniform registers) and one elected lane issues each group of MMAs and its
+// commit.  The start-address field (bits 0-13, address >> 4) of a descriptor
+// is advanced by adding (byte offset >> 4); every address stays below
+// 256 KB, so the field never carries into the next one.
 
-// The start-address field (bits 0-13, address >> 4) of a descriptor is
-// advanced by adding (byte offset >> 4); every address stays below 256 KB, so
-// the field never carries into the next one.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk)
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qd, uint64_t kd)
 {
     using C = Cfg<D>;
-    const uint64_t qd = sdesc_sw128(sq, 16, 1024);
-    const uint64_t kd = sdesc_sw128(sk, 16, 1024);
-#pragma unroll 1
+#pragma unroll
     for (int kk = 0; kk < D / 16; kk++) {
         // 16 elements = 32 bytes inside a 128-byte swizzle row; 4 steps per 64-column box.
         const uint32_t off = ((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4;
@@ -206,15 +218,13 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t 
 }
 
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t sv, bool accumulate)
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t vd, uint32_t accumulate)
 {
     using C = Cfg<D>;
-    // V tile: keys x D, D contiguous (MN-major B operand).  LBO = distance
-    // between the 64-column boxes, SBO = 8 rows x 128 bytes; 16 keys = 2048 bytes.
-    const uint64_t vd = sdesc_sw128(sv, C::BOX_BYTES, 1024);
-#pragma unroll 1
+    // V tile: keys x D, D contiguous (MN-major B operand); 16 keys = 2048 bytes.
+#pragma unroll
     for (int kk = 0; kk < BN / 16; kk++)
-        umma_ts(o_tmem, p_tmem + kk * 8, vd + ((kk * 2048) >> 4), C::IDESC_O, (accumulate || kk > 0) ? 1u : 0u);
+        umma_ts(o_tmem, p_tmem + kk * 8, vd + ((kk * 2048) >> 4), C::IDESC_O, (accumulate | kk) ? 1u : 0u);
 }
 
 template <int D, bool CAUSAL>
@@ -223,59 +233,75 @@ __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, u
     using C = Cfg<D>;
     volatile int *ab = &c.abort_flag;
     unsigned *err = &g_attn_error_word;
+    const bool leader = elect_one();
     uint32_t it = 0, g = 0, ncorr = 0;
     int w = 0;
-    // Per-tile addresses are selected, not indexed, to keep them in registers.
-    auto tS = [&](int t) { return tmem + (t ? C::TM_S1 : C::TM_S0); };
-    auto tO = [&](int t) { return tmem + (t ? C::TM_O1 : C::TM_O0); };
-    auto sQ = [&](int t) { return sQ0 + (t ? C::TILE_BYTES : 0u); };
+    // Q/K descriptors: LBO unused for K-major swizzled operands, SBO = 8 rows x 128 B.
+    // V descriptor: LBO = distance between the 64-column boxes, SBO = 8 rows x 128 B.
+    const uint64_t qd0 = sdesc_sw128(sQ0, 16, 1024);
+    const uint64_t qd1 = sdesc_sw128(sQ0 + C::TILE_BYTES, 16, 1024);
+    const uint64_t kvd_k = sdesc_sw128(sKV, 16, 1024);
+    const uint64_t kvd_v = sdesc_sw128(sKV, C::BOX_BYTES, 1024);
+    auto stage_off = [](uint32_t s) -> uint64_t { return (s * C::TILE_BYTES) >> 4; };
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
         const Tile T = decode_tile<CAUSAL>(p, tile);
         for (int t = 0; t < 2; t++)
-            if (!mbar_wait(smem_u32(&c.q_full[t]), w & 1, ab, err, kErrMma)) goto abort;
+            if (!mbar_wait_warp(smem_u32(&c.q_full[t]), w & 1, ab, err, kErrMma)) goto abort;
         {
             const uint32_t ks = it % C::NSTAGE;
-            if (!mbar_wait(smem_u32(&c.kv_full[ks]), (it / C::NSTAGE) & 1, ab, err, kErrMma)) goto abort;
+            if (!mbar_wait_warp(smem_u32(&c.kv_full[ks]), (it / C::NSTAGE) & 1, ab, err, kErrMma)) goto abort;
             tc_fence_after();
-            const uint32_t sk = sKV + ks * C::TILE_BYTES;
-            for (int t = 0; t < 2; t++) {
-                issue_qk<D>(tS(t), sQ(t), sk);
-                umma_commit(smem_u32(&c.s_full[t]));
+            const uint64_t kd = kvd_k + stage_off(ks);
+            if (leader) {
+                issue_qk<D>(tmem + C::TM_S0, qd0, kd);
+                umma_commit(smem_u32(&c.s_full[0]));
+                issue_qk<D>(tmem + C::TM_S1, qd1, kd);
+                umma_commit(smem_u32(&c.s_full[1]));
+                umma_commit(smem_u32(&c.kv_empty[ks]));
+                if (T.n_kv == 1) {
+                    umma_commit(smem_u32(&c.q_empty[0]));
+                    umma_commit(smem_u32(&c.q_empty[1]));
+                }
             }
-            umma_commit(smem_u32(&c.kv_empty[ks]));
-            if (T.n_kv == 1)
-                for (int t = 0; t < 2; t++) umma_commit(smem_u32(&c.q_empty[t]));
+            __syncwarp();
             ++it;
         }
         for (int j = 0; j < T.n_kv; j++) {
             const bool has_next = j + 1 < T.n_kv;
             const uint32_t vs = it % C::NSTAGE;
-            if (!mbar_wait(smem_u32(&c.kv_full[vs]), (it / C::NSTAGE) & 1, ab, err, kErrMma)) goto abort;
-            const uint32_t sv = sKV + vs * C::TILE_BYTES;
+            if (!mbar_wait_warp(smem_u32(&c.kv_full[vs]), (it / C::NSTAGE) & 1, ab, err, kErrMma)) goto abort;
+            const uint64_t vd = kvd_v + stage_off(vs);
             const uint32_t kn = it + 1;
             const uint32_t kns = kn % C::NSTAGE;
-            const uint32_t sk = sKV + kns * C::TILE_BYTES;
-#pragma unroll 1
+            const uint64_t kd = kvd_k + stage_off(kns);
+#pragma unroll
             for (int t = 0; t < 2; t++) {
-                if (!mbar_wait(smem_u32(&c.p_full[t]), g & 1, ab, err, kErrMma)) goto abort;
+                if (!mbar_wait_warp(smem_u32(&c.p_full[t]), g & 1, ab, err, kErrMma)) goto abort;
                 if (!T.cert && j > 0)
-                    if (!mbar_wait(smem_u32(&c.o_ready[t]), ncorr & 1, ab, err, kErrMma)) goto abort;
+                    if (!mbar_wait_warp(smem_u32(&c.o_ready[t]), ncorr & 1, ab, err, kErrMma)) goto abort;
                 if (j == 0)
-                    if (!mbar_wait(smem_u32(&c.o_free[t]), (w & 1) ^ 1, ab, err, kErrMma)) goto abort;
+                    if (!mbar_wait_warp(smem_u32(&c.o_free[t]), (w & 1) ^ 1, ab, err, kErrMma)) goto abort;
                 tc_fence_after();
-                issue_pv<D>(tO(t), tS(t), sv, j > 0);
-                umma_commit(smem_u32(&c.pv_done[t]));
-                if (t == 1) umma_commit(smem_u32(&c.kv_empty[vs]));
+                if (leader) {
+                    issue_pv<D>(tmem + (t ? C::TM_O1 : C::TM_O0), tmem + (t ? C::TM_S1 : C::TM_S0), vd,
+                                j > 0 ? 1u : 0u);
+                    umma_commit(smem_u32(&c.pv_done[t]));
+                    if (t == 1) umma_commit(smem_u32(&c.kv_empty[vs]));
+                }
+                __syncwarp();
                 if (has_next) {
                     if (t == 0) {
-                        if (!mbar_wait(smem_u32(&c.kv_full[kns]), (kn / C::NSTAGE) & 1, ab, err, kErrMma))
+                        if (!mbar_wait_warp(smem_u32(&c.kv_full[kns]), (kn / C::NSTAGE) & 1, ab, err, kErrMma))
                             goto abort;
                         tc_fence_after();
                     }
-                    issue_qk<D>(tS(t), sQ(t), sk);
-                    umma_commit(smem_u32(&c.s_full[t]));
-                    if (t == 1) umma_commit(smem_u32(&c.kv_empty[kns]));
-                    if (j + 1 == T.n_kv - 1) umma_commit(smem_u32(&c.q_empty[t]));
+                    if (leader) {
+                        issue_qk<D>(tmem + (t ? C::TM_S1 : C::TM_S0), t ? qd1 : qd0, kd);
+                        umma_commit(smem_u32(&c.s_full[t]));
+                        if (t == 1) umma_commit(smem_u32(&c.kv_empty[kns]));
+                        if (j + 1 == T.n_kv - 1) umma_commit(smem_u32(&c.q_empty[t]));
+                    }
+                    __syncwarp();
                 }
             }
             it += has_next ? 2 : 1;
@@ -285,7 +311,8 @@ __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, u
     }
     return;
 abort:
-    umma_commit(smem_u32(&c.drain));
+    if (leader) umma_commit(smem_u32(&c.drain));
+    __syncwarp();
     drain_wait(smem_u32(&c.drain), 0);
 }
 
@@ -530,18 +557,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = ctl.tmem_base;
 
-    // Register split (launch: 512 threads x 128 = 65536): softmax 2 x 128 x 184,
-    // correction 128 x 88, producer/MMA group 128 x 56 -> 47104 + 11264 + 7168 = 65536.
+    // Register split (launch: 512 threads x 128 = 65536): softmax 2 x 128 x 168,
+    // correction 128 x 96, producer/MMA group 128 x 80 -> 43008 + 12288 + 10240 = 65536.
     if (warp < 8) {
-        setmaxnreg_inc<184>();
+        setmaxnreg_inc<168>();
         softmax_role<D, CAUSAL>(p, ctl, tmem, warp, lane);
     } else if (warp < 12) {
-        setmaxnreg_dec<88>();
+        setmaxnreg_dec<96>();
         correction_role<D, CAUSAL>(p, ctl, tmem, warp, lane);
     } else {
-        setmaxnreg_dec<56>();
-        if (warp == 12 && lane == 0) producer_role<D, CAUSAL>(p, ctl, &tm_q, &tm_k, &tm_v, sQ0, sKV);
-        if (warp == 13 && lane == 0) mma_role<D, CAUSAL>(p, ctl, tmem, sQ0, sKV);
+        setmaxnreg_dec<80>();
+        if (warp == 12) producer_role<D, CAUSAL>(p, ctl, &tm_q, &tm_k, &tm_v, sQ0, sKV);
+        if (warp == 13) mma_role<D, CAUSAL>(p, ctl, tmem, sQ0, sKV);
     }
 
     tc_fence_before();

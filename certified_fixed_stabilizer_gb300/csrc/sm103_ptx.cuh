@@ -80,6 +80,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Warp-uniform form: every lane of the warp calls it; the result is the same
+// in all lanes (false as soon as one lane gave up).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                               unsigned int *err_word, unsigned int site)
+{
+    const bool ok = mbar_wait(bar, parity, abort_flag, err_word, site);
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// One lane of a converged warp gets true.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, e;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ----------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap)

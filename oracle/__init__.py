@@ -119,6 +119,12 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def _heads_first(a: np.ndarray) -> np.ndarray:
+    """[..., N, d] -> contiguous [prod(...), N, d] (works for N = 0)."""
+    lead = int(np.prod(a.shape[:-2])) if a.ndim > 2 else 1
+    return np.ascontiguousarray(a.reshape(lead, a.shape[-2], a.shape[-1]))
+
+
 # --- Figure 3 limits and Algorithm 1 steps 5-7 as scalar functions ----------
 
 def format_log2_max(fmt: str) -> float:
@@ -149,10 +155,8 @@ def certify(q, k, v, scale_log2: float, exp_fmt: str = "bf16", acc_fmt: str = "f
     list of dicts with certified, G, A, C, reason, band, B_h, kappa, qmax, vmax).
     """
     qb, kb, vb = (as_bf16_bits(t) for t in (q, k, v))
+    qb, kb, vb = (_heads_first(a) for a in (qb, kb, vb))
     d = qb.shape[-1]
-    qb = qb.reshape(-1, qb.shape[-2], d)
-    kb = kb.reshape(-1, kb.shape[-2], d)
-    vb = vb.reshape(-1, vb.shape[-2], d)
     BH, Nq, Nk = qb.shape[0], qb.shape[1], kb.shape[1]
     kbar = np.zeros((BH, d), dtype=np.float64)
     certs = (OracleCert * max(BH, 1))()
@@ -185,10 +189,8 @@ def attention(q, k, v, scale: float, causal: bool = False, rows=None,
     else:
         qa, ka, va = (as_bf16_bits(t) for t in (q, k, v))
         fn = _load().oracle_attn_bf16
+    qa, ka, va = (_heads_first(a) for a in (qa, ka, va))
     d = qa.shape[-1]
-    qa = qa.reshape(-1, qa.shape[-2], d)
-    ka = ka.reshape(-1, ka.shape[-2], d)
-    va = va.reshape(-1, va.shape[-2], d)
     BH, Nq, Nk = qa.shape[0], qa.shape[1], ka.shape[1]
     if rows is None:
         n_rows, rows_arr = Nq, None
