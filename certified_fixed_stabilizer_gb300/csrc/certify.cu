@@ -24,9 +24,17 @@
 // thread and are combined in a fixed order; maxima are order-independent.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "clis_internal.h"
 
 namespace clis {
+
+// Scratch for clis_certify_noalloc: a fixed array owned by the library, so
+// callers that cannot allocate still get a workspace.  Host code must not pass
+// the symbol itself to a kernel (on the host it is only a stand-in); it uses
+// the device address returned by certify_static_scratch().
+static __device__ __align__(256) unsigned char g_certify_scratch[CLIS_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
@@ -315,6 +323,22 @@ size_t cert_workspace_layout(int64_t BH, int64_t nck, int64_t ncq, int64_t d, vo
         ws->vabs = reinterpret_cast<uint32_t *>(p + o_vabs);
     }
     return off;
+}
+
+void *certify_static_scratch()
+{
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static void *addr[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_certify_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = ptr;
+    }
+    return addr[dev];
 }
 
 cudaError_t launch_certify(const CertArgs &a, const CertWorkspace &ws, cudaStream_t stream)

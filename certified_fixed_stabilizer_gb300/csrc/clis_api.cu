@@ -164,6 +164,20 @@ clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, const void
     return clis::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+clis_status_t clis_certify_noalloc(const clis_shape_t *shape, const void *q, const void *k, const void *v,
+                                   float scale_log2, clis_fmt_t exp_fmt, clis_fmt_t acc_fmt, float *kbar,
+                                   clis_head_cert_t *certs, clis_stream_t stream)
+{
+    size_t need = 0;
+    const clis_status_t st = clis_certify_workspace_size(shape, &need);
+    if (st != CLIS_OK) return st;
+    if (need > CLIS_NOALLOC_SCRATCH_BYTES) return CLIS_ERR_WORKSPACE;
+    void *scratch = clis::certify_static_scratch();
+    if (!scratch) return CLIS_ERR_CUDA;
+    return clis_certify(shape, q, k, v, scale_log2, exp_fmt, acc_fmt, kbar, certs, scratch,
+                        CLIS_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 const char *clis_status_string(clis_status_t s)
 {
     switch (s) {

@@ -42,6 +42,10 @@ size_t cert_workspace_layout(int64_t BH, int64_t nck, int64_t ncq, int64_t d, vo
 
 cudaError_t launch_certify(const CertArgs &a, const CertWorkspace &ws, cudaStream_t stream);
 
+// Device address of the library-owned certification scratch array on the
+// current device (looked up once per device); nullptr on failure.
+void *certify_static_scratch();
+
 // ---------------------------------------------------------------- attention
 
 struct AttnArgs {

@@ -121,6 +121,41 @@ CLIS_API clis_status_t clis_certify(const clis_shape_t *shape, const void *q, co
                            clis_fmt_t acc_fmt, float *kbar, clis_head_cert_t *certs,
                            void *workspace, size_t ws_bytes, clis_stream_t stream);
 
+/* Size in bytes of the scratch buffer that clis_certify_noalloc uses instead
+ * of a caller workspace (a fixed array inside the library). */
+#define CLIS_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* clis_certify for callers that must not allocate device memory.  The paper
+ * has no counterpart to this entry point: it exists for code that runs where
+ * cudaMalloc is off limits -- a plugin or custom operator inside another
+ * runtime that owns all device memory and hands out no workspace, a serving
+ * loop whose memory was planned up front, or any caller for whom an
+ * allocation would synchronise the device or break the host's accounting.
+ *
+ * Same arguments and results as clis_certify minus the workspace: the
+ * scratch lives in one library-owned device array of
+ * CLIS_NOALLOC_SCRATCH_BYTES, which every GPU that loads the library keeps
+ * until the process exits.  The caller still provides q, k, v, kbar and
+ * certs.  Nothing is allocated or freed, by this call or by any routine it
+ * uses.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address with cudaGetSymbolAddress; make that first call
+ *     before starting any stream capture on that device.
+ *   - All calls share the one array and it keeps what the last call left in
+ *     it.  The kernels overwrite every scratch word they read, so nothing
+ *     needs clearing between calls, but calls that overlap on the GPU (two
+ *     streams, two host threads) race on it: serialise them.
+ *   - Shapes whose clis_certify_workspace_size() exceeds
+ *     CLIS_NOALLOC_SCRATCH_BYTES return CLIS_ERR_WORKSPACE before anything
+ *     is launched (about B*H*ceil(Nk/1024)*d*4 bytes; B*H = 40 heads of
+ *     75,600 keys at d = 128 need 1.6 MB).
+ *   - CLIS_ERR_CUDA if the address lookup fails; argument errors as in
+ *     clis_certify. */
+CLIS_API clis_status_t clis_certify_noalloc(const clis_shape_t *shape, const void *q, const void *k,
+                                   const void *v, float scale_log2, clis_fmt_t exp_fmt,
+                                   clis_fmt_t acc_fmt, float *kbar, clis_head_cert_t *certs,
+                                   clis_stream_t stream);
+
 /* Fused attention forward O = softmax(scale * Q K^T) V (paper: abstract and
  * Figure 5(a), "a loop-invariant stabilizer mu_i removes the reduction and
  * rescaling chain").  One persistent kernel; each 256-row query block of a
