@@ -48,7 +48,7 @@ namespace {
 constexpr int BM = 128;            // rows per query tile
 constexpr int BN = 128;            // keys per KV tile
 constexpr int kThreads = 512;
-constexpr int kNStageMax = 6;
+constexpr int kNStageMax = 8;
 
 // Error-word bits: which wait gave up.
 constexpr unsigned kErrProducer = 1u << 0;
@@ -59,7 +59,7 @@ constexpr unsigned kErrDrain = 1u << 4;
 
 template <int D>
 struct Cfg {
-    static constexpr int NSTAGE = (D == 128) ? 4 : 6;
+    static constexpr int NSTAGE = (D == 128) ? 5 : 8;
     static constexpr int NBOX = D / 64;                 // 64-column (128-byte) TMA boxes per tile
     static constexpr int BOX_BYTES = 128 * 128;         // 128 rows x 128 bytes
     static constexpr int TILE_BYTES = NBOX * BOX_BYTES; // one Q, K or V tile
@@ -391,13 +391,15 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
             if (T.cert) {
                 nshift = -mu;
             } else {
-                float mx0 = -INFINITY, mx1 = -INFINITY;
+                // Row maximum: four independent chains of 3-input max.
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int cc = 0; cc < BN; cc += 2) {
-                    mx0 = fmaxf(mx0, __uint_as_float(s[cc]));
-                    mx1 = fmaxf(mx1, __uint_as_float(s[cc + 1]));
+                for (int cc = 0; cc < BN; cc += 8) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; q4++)
+                        mx[q4] = fmax3(mx[q4], __uint_as_float(s[cc + 2 * q4]), __uint_as_float(s[cc + 2 * q4 + 1]));
                 }
-                const float m_tile = fmaxf(mx0, mx1) * sl2;
+                const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
                 const float m_new = fmaxf(m_run, m_tile);
                 const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
                 if (j > 0) {
@@ -408,21 +410,27 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
                 m_run = m_new;
                 nshift = -m_use;
             }
-            float l0 = 0.f, l1 = 0.f;
+            // p = exp2(scale_log2 * s - shift): one packed FMA per two scores,
+            // two MUFU ex2, one packed add into the row sum, one bf16x2 pack.
+            const float2 sc2 = make_float2(sl2, sl2), sh2 = make_float2(nshift, nshift);
+            float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
 #pragma unroll
             for (int c32 = 0; c32 < BN / 32; c32++) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; e++) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(s[c32 * 32 + 2 * e]), sl2, nshift));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(s[c32 * 32 + 2 * e + 1]), sl2, nshift));
-                    l0 += p0;
-                    l1 += p1;
-                    pk[e] = pack_bf16x2(p0, p1);
+                    const float2 x = ffma2(make_float2(__uint_as_float(s[c32 * 32 + 2 * e]),
+                                                       __uint_as_float(s[c32 * 32 + 2 * e + 1])),
+                                           sc2, sh2);
+                    const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    if (e & 1) lb = fadd2(lb, pp);
+                    else la = fadd2(la, pp);
+                    pk[e] = pack_bf16x2(pp.x, pp.y);
                 }
                 tmem_st16(tS + c32 * 16, pk);
             }
-            l_run = l_run * alpha + (l0 + l1);
+            const float2 lab = fadd2(la, lb);
+            l_run = l_run * alpha + (lab.x + lab.y);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&c.p_full[t]));
@@ -442,9 +450,13 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
                 tmem_wait_ld();
                 if (row_ok) {
                     uint32_t pk[16];
+                    const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-                    for (int e = 0; e < 16; e++)
-                        pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+                    for (int e = 0; e < 16; e++) {
+                        const float2 o2 =
+                            fmul2(make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), inv2);
+                        pk[e] = pack_bf16x2(o2.x, o2.y);
+                    }
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c32 * 32);
 #pragma unroll
                     for (int e = 0; e < 4; e++) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
@@ -493,8 +505,13 @@ __device__ void correction_role(const Params &p, Ctl &c, uint32_t tmem, int warp
                         uint32_t r[32];
                         tmem_ld32(tO + c32 * 32, r);
                         tmem_wait_ld();
+                        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                        for (int e = 0; e < 32; e++) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 o2 = fmul2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), a2);
+                            r[e] = __float_as_uint(o2.x);
+                            r[e + 1] = __float_as_uint(o2.y);
+                        }
                         tmem_st32(tO + c32 * 32, r);
                     }
                     tmem_wait_st();
