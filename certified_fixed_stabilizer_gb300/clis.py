@@ -18,7 +18,7 @@ from . import build as _build
 LOG2E = 1.4426950408889634
 
 FMT = {"fp16": 0, "bf16": 1, "fp32": 2}
-VARIANT = {"auto": 0, "online": 1, "certified": 2}
+VARIANT = {"auto": 0, "online": 1, "certified": 2, "online_lazy": 3}
 STATUS = {0: "CLIS_OK", 1: "CLIS_ERR_INVALID_ARG", 2: "CLIS_ERR_UNSUPPORTED", 3: "CLIS_ERR_MISALIGNED",
           4: "CLIS_ERR_WORKSPACE", 5: "CLIS_ERR_CUDA", 6: "CLIS_ERR_TIMEOUT"}
 
@@ -207,7 +207,7 @@ def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
         q, k, v = (t.to(dev, non_blocking=True) for t in (q, k, v))
     sl2 = scale_log2_for(q.shape[-1], softmax_scale)
     kbar = certs = None
-    if variant != "online":
+    if variant in ("auto", "certified"):
         kbar, certs = clis_certify(q, k, v, sl2)
     out = clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=causal, variant=variant)
     if on_host:

@@ -49,6 +49,9 @@ constexpr int BM = 128;            // rows per query tile
 constexpr int BN = 128;            // keys per KV tile
 constexpr int kThreads = 512;
 constexpr int kNStageMax = 8;
+// Lazy online softmax keeps a stale row maximum until the true one exceeds it
+// by more than this (exp2 units), so p <= 2^kLazyTau; FlashAttention-4 uses 8.
+constexpr float kLazyTau = 8.0f;
 
 // Error-word bits: which wait gave up.
 constexpr unsigned kErrProducer = 1u << 0;
@@ -79,6 +82,7 @@ struct Params {
     int64_t q_sb, q_sh, q_sn, o_sb, o_sh, o_sn;
     int B, H, Nq, Nk;
     int nqb;        // 256-row query blocks per head
+    int grp;        // causal: heads per scheduling group
     int n_kv_full;  // KV tiles per head, ceil(Nk / 128)
     int num_tiles;  // B * H * nqb
     float scale_log2;
@@ -98,25 +102,41 @@ struct __align__(8) Ctl {
 
 struct Tile {
     int bh, b, h, qb, n_kv;
-    bool cert;
+    bool cert;  // fixed stabiliser, no rescale
+    bool lazy;  // online, rescale only when the row maximum grows by more than kLazyTau
 };
 
+// Work-tile order.  Non-causal: head-major, query blocks ascending (every
+// tile costs the same; the CTAs working at one time share a head's K and V in
+// L2).  Causal: tile cost grows with the query block, so heads are taken in
+// groups of p.grp and, inside a group, query blocks run longest first on even
+// groups and shortest first on odd groups; with static round-robin assignment
+// this keeps the per-CTA work within about 1% while the K/V of one group of
+// heads stays in L2.
 template <bool CAUSAL>
 __device__ __forceinline__ Tile decode_tile(const Params &p, int tile)
 {
     Tile t;
-    t.bh = tile / p.nqb;
-    const int r = tile % p.nqb;
-    t.qb = CAUSAL ? (p.nqb - 1 - r) : r;  // causal: longest rows first
-    t.b = t.bh / p.H;
-    t.h = t.bh % p.H;
     if (CAUSAL) {
+        const int per_grp = p.grp * p.nqb;
+        const int gi = tile / per_grp;
+        const int r = tile % per_grp;
+        const int BH = p.B * p.H;
+        const int heads = min(p.grp, BH - gi * p.grp);
+        const int qi = r / heads;
+        t.bh = gi * p.grp + r % heads;
+        t.qb = (gi & 1) ? qi : (p.nqb - 1 - qi);
         const int last_row = min(p.Nq, (t.qb + 1) * 2 * BM) - 1;
         t.n_kv = min(p.n_kv_full, last_row / BN + 1);
     } else {
+        t.bh = tile / p.nqb;
+        t.qb = tile % p.nqb;
         t.n_kv = p.n_kv_full;
     }
-    if (p.variant == CLIS_ONLINE) t.cert = false;
+    t.b = t.bh / p.H;
+    t.h = t.bh % p.H;
+    t.lazy = p.variant == CLIS_ONLINE_LAZY;
+    if (p.variant == CLIS_ONLINE || p.variant == CLIS_ONLINE_LAZY) t.cert = false;
     else if (p.variant == CLIS_CERTIFIED_FORCED) t.cert = true;
     else t.cert = __ldg(&p.certs[t.bh].certified) != 0;
     return t;
@@ -277,7 +297,7 @@ __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, u
 #pragma unroll
             for (int t = 0; t < 2; t++) {
                 if (!mbar_wait_warp(smem_u32(&c.p_full[t]), g & 1, ab, err, kErrMma)) goto abort;
-                if (!T.cert && j > 0)
+                if (!T.cert && !T.lazy && j > 0)
                     if (!mbar_wait_warp(smem_u32(&c.o_ready[t]), ncorr & 1, ab, err, kErrMma)) goto abort;
                 if (j == 0)
                     if (!mbar_wait_warp(smem_u32(&c.o_free[t]), (w & 1) ^ 1, ab, err, kErrMma)) goto abort;
@@ -306,7 +326,7 @@ __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, u
             }
             it += has_next ? 2 : 1;
             ++g;
-            if (!T.cert && j > 0) ++ncorr;
+            if (!T.cert && !T.lazy && j > 0) ++ncorr;
         }
     }
     return;
@@ -388,6 +408,7 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
             // per 32 scores; all of S is already in registers.
             float nshift;  // -(stabiliser) in scale_log2 * s units
             float alpha = 1.f;
+            bool lazy_rescale = false;
             if (T.cert) {
                 nshift = -mu;
             } else {
@@ -400,15 +421,27 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
                         mx[q4] = fmax3(mx[q4], __uint_as_float(s[cc + 2 * q4]), __uint_as_float(s[cc + 2 * q4 + 1]));
                 }
                 const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
-                const float m_new = fmaxf(m_run, m_tile);
-                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                if (j > 0) {
-                    alpha = ex2_approx(m_run - m_use);
-                    c.alpha[t][rl] = alpha;
-                    mbar_arrive(smem_u32(&c.alpha_full[t]));
+                if (!T.lazy) {
+                    const float m_new = fmaxf(m_run, m_tile);
+                    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                    if (j > 0) {
+                        alpha = ex2_approx(m_run - m_use);
+                        c.alpha[t][rl] = alpha;
+                        mbar_arrive(smem_u32(&c.alpha_full[t]));
+                    }
+                    m_run = m_new;
+                    nshift = -m_use;
+                } else {
+                    // Keep the stale maximum unless the row's maximum outgrew it by kLazyTau.
+                    const bool grow = m_tile > m_run + kLazyTau;  // always true on the first block
+                    if (grow) {
+                        const float m_new = m_tile;
+                        if (j > 0) alpha = ex2_approx(m_run - m_new);
+                        m_run = m_new;
+                    }
+                    lazy_rescale = j > 0 && __any_sync(0xFFFFFFFFu, grow);
+                    nshift = (m_run == -INFINITY) ? 0.f : -m_run;
                 }
-                m_run = m_new;
-                nshift = -m_use;
             }
             // p = exp2(scale_log2 * s - shift): one packed FMA per two scores,
             // two MUFU ex2, one packed add into the row sum, one bf16x2 pack.
@@ -431,6 +464,28 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
             }
             const float2 lab = fadd2(la, lb);
             l_run = l_run * alpha + (lab.x + lab.y);
+            if (lazy_rescale) {
+                // Lazy online path: the warp rescales its 32 rows of O in TMEM when any
+                // of them raised its maximum, after the previous O_t += P V completed
+                // (rows that did not grow multiply by 1).  This precedes the p_full
+                // arrival, so the next O_t += P V sees the rescaled O.
+                if (!mbar_wait(smem_u32(&c.pv_done[t]), (g - 1) & 1, ab, err, kErrSoftmax)) goto abort;
+                tc_fence_after();
+                const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll 1
+                for (int c32 = 0; c32 < D / 32; c32++) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + c32 * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float2 o2 = fmul2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), a2);
+                        r[e] = __float_as_uint(o2.x);
+                        r[e + 1] = __float_as_uint(o2.y);
+                    }
+                    tmem_st32(tO + c32 * 32, r);
+                }
+            }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&c.p_full[t]));
@@ -488,7 +543,7 @@ __device__ void correction_role(const Params &p, Ctl &c, uint32_t tmem, int warp
     uint32_t g = 0, ncorr = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
         const Tile T = decode_tile<CAUSAL>(p, tile);
-        if (T.cert) {
+        if (T.cert || T.lazy) {
             g += T.n_kv;
             continue;
         }
@@ -574,13 +629,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = ctl.tmem_base;
 
-    // Register split (launch: 512 threads x 128 = 65536): softmax 2 x 128 x 168,
-    // correction 128 x 96, producer/MMA group 128 x 80 -> 43008 + 12288 + 10240 = 65536.
+    // Register split (launch: 512 threads x 128 = 65536): softmax 2 x 128 x 176,
+    // correction 128 x 80, producer/MMA group 128 x 80 -> 45056 + 10240 + 10240 = 65536.
     if (warp < 8) {
-        setmaxnreg_inc<168>();
+        setmaxnreg_inc<176>();
         softmax_role<D, CAUSAL>(p, ctl, tmem, warp, lane);
     } else if (warp < 12) {
-        setmaxnreg_dec<96>();
+        setmaxnreg_dec<80>();
         correction_role<D, CAUSAL>(p, ctl, tmem, warp, lane);
     } else {
         setmaxnreg_dec<80>();
@@ -669,6 +724,11 @@ clis_status_t launch_impl(const AttnArgs &a, cudaStream_t stream)
     p.nqb = (a.Nq + 2 * BM - 1) / (2 * BM);
     p.n_kv_full = (a.Nk + BN - 1) / BN;
     p.num_tiles = a.B * a.H * p.nqb;
+    // Causal scheduling groups: enough heads that a group spans about two
+    // waves of CTAs.
+    p.grp = (2 * nsm + p.nqb - 1) / p.nqb;
+    if (p.grp > a.B * a.H) p.grp = a.B * a.H;
+    if (p.grp < 1) p.grp = 1;
     p.scale_log2 = a.scale_log2;
     p.variant = a.variant;
     if (p.num_tiles == 0) return CLIS_OK;

@@ -121,9 +121,10 @@ clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, const void
     if (!q || !k || !v || !o) return CLIS_ERR_INVALID_ARG;
     if (!std::isfinite(scale_log2) || !(scale_log2 > 0.f)) return CLIS_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return CLIS_ERR_INVALID_ARG;
-    if (variant != CLIS_AUTO && variant != CLIS_ONLINE && variant != CLIS_CERTIFIED_FORCED)
+    if (variant != CLIS_AUTO && variant != CLIS_ONLINE && variant != CLIS_CERTIFIED_FORCED &&
+        variant != CLIS_ONLINE_LAZY)
         return CLIS_ERR_INVALID_ARG;
-    if (variant != CLIS_ONLINE && !kbar) return CLIS_ERR_INVALID_ARG;
+    if ((variant == CLIS_AUTO || variant == CLIS_CERTIFIED_FORCED) && !kbar) return CLIS_ERR_INVALID_ARG;
     if (variant == CLIS_AUTO && !certs) return CLIS_ERR_INVALID_ARG;
     if (causal && shape->Nq != shape->Nk) return CLIS_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return CLIS_ERR_MISALIGNED;

@@ -63,11 +63,22 @@ typedef enum { CLIS_FMT_FP16 = 0, CLIS_FMT_BF16 = 1, CLIS_FMT_FP32 = 2 } clis_fm
  *  CLIS_AUTO              certified heads use the fixed stabiliser, the rest
  *                         fall back to online softmax (abstract: "falling back
  *                         to online softmax when certification fails");
- *  CLIS_ONLINE            every head uses online softmax (the baseline);
+ *  CLIS_ONLINE            every head uses online softmax that rescales the
+ *                         accumulator after every KV block (the baseline);
  *  CLIS_CERTIFIED_FORCED  every head uses the fixed stabiliser, ignoring the
  *                         flags (benchmarks and tests only: output of a head
- *                         that did not certify is then unspecified). */
-typedef enum { CLIS_AUTO = 0, CLIS_ONLINE = 1, CLIS_CERTIFIED_FORCED = 2 } clis_variant_t;
+ *                         that did not certify is then unspecified);
+ *  CLIS_ONLINE_LAZY       every head uses online softmax that rescales only
+ *                         when a row maximum grows by more than 8 (exp2 units),
+ *                         the FlashAttention-4-style baseline the paper adapts
+ *                         as "FA4-style (row)" (Tables 5 and 8); needs no
+ *                         certificate. */
+typedef enum {
+    CLIS_AUTO = 0,
+    CLIS_ONLINE = 1,
+    CLIS_CERTIFIED_FORCED = 2,
+    CLIS_ONLINE_LAZY = 3
+} clis_variant_t;
 
 /* Problem shape and element strides (elements, not bytes).  K and V share
  * Nk; Q and O share Nq.  O strides are ignored by clis_certify. */
@@ -167,7 +178,8 @@ CLIS_API clis_status_t clis_certify_noalloc(const clis_shape_t *shape, const voi
  *   o       device bf16 out [B,H,Nq,d] (strides from shape)
  *   lse2    optional device fp32 out [B*H*Nq] (contiguous, index
  *           (b*H + h)*Nq + i): log2 sum_j exp2(scale_log2 * s_ij); NULL = skip
- *   kbar, certs  outputs of clis_certify (may be NULL for CLIS_ONLINE)
+ *   kbar, certs  outputs of clis_certify (may be NULL for CLIS_ONLINE and
+ *           CLIS_ONLINE_LAZY)
  *   causal  0 or 1; 1 requires Nq == Nk (key j visible to query i iff j <= i)
  * Nq == 0 or B*H == 0 launches nothing and returns CLIS_OK. */
 CLIS_API clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, const void *k,

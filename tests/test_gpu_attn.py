@@ -44,7 +44,7 @@ def _oracle(q, k, v, causal, rows=None, softmax_scale=None):
     return oracle.attention(flat(q), flat(k), flat(v), scale, causal=causal, rows=rows, with_lse2=True)
 
 
-@pytest.mark.parametrize("variant", ["auto", "online", "certified"])
+@pytest.mark.parametrize("variant", ["auto", "online", "certified", "online_lazy"])
 def test_tiny_full_parity(variant):
     dev = need_gpu()
     w = WORKLOADS["tiny"]
@@ -65,7 +65,7 @@ def test_workload_sampled_parity(name, rows_per_head):
     q, k, v = make_inputs(w, device=dev)
     rows = sample_rows(w.N, rows_per_head, seed=1)
     ref, rlse = _oracle(q, k, v, w.causal, rows=rows)
-    for variant in ("auto", "online"):
+    for variant in ("online_lazy", "auto", "online"):
         out, l2, certs = _run(q, k, v, w.causal, variant, lse2=True)
         got = flat(out)[:, rows].float().cpu().numpy()
         assert_close_to_oracle(got, ref, f"{name}/{variant}")
@@ -101,7 +101,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk,d,causal", CASES)
-@pytest.mark.parametrize("variant", ["auto", "online"])
+@pytest.mark.parametrize("variant", ["auto", "online", "online_lazy"])
 def test_ragged_shapes(B, H, Nq, Nk, d, causal, variant):
     dev = need_gpu()
     g = torch.Generator(device=dev)
@@ -168,6 +168,27 @@ def test_host_tensors_end_to_end():
     assert out.device.type == "cpu"
     ref, _ = _oracle(q, k, v, False)
     assert_close_to_oracle(out.float().numpy(), ref, "host e2e")
+
+
+def test_lazy_rescale_with_growing_maxima():
+    """Keys whose scores grow along the sequence force the lazy online path to
+    rescale in many blocks (the row maximum keeps outgrowing the stale one by
+    more than 8): parity must hold there too, and in causal rows."""
+    dev = need_gpu()
+    g = torch.Generator(device=dev)
+    g.manual_seed(21)
+    B, H, N, d = 1, 2, 1500, 128
+    q = torch.randn(B, H, N, d, generator=g, device=dev)
+    ramp = torch.linspace(0, 6, N, device=dev)[:, None]
+    k = torch.randn(B, H, N, d, generator=g, device=dev) * ramp + q.mean(dim=2, keepdim=True) * ramp
+    v = torch.randn(B, H, N, d, generator=g, device=dev)
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    for causal in (False, True):
+        for variant in ("online_lazy", "online"):
+            out, l2, _ = _run(q, k, v, causal, variant, lse2=True)
+            ref, rlse = _oracle(q, k, v, causal)
+            assert_close_to_oracle(out.float().cpu().numpy(), ref, f"growing/{variant}/{causal}")
+            np.testing.assert_allclose(l2.cpu().numpy().reshape(rlse.shape), rlse, atol=2e-3, rtol=0)
 
 
 def test_outputs_are_deterministic():
