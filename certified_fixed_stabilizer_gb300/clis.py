@@ -74,6 +74,8 @@ def load_library():
     lib.clis_get_device_error.restype = i32
     lib.clis_clear_device_error.argtypes = []
     lib.clis_clear_device_error.restype = i32
+    lib.clis_debug_wait_selftest.argtypes = [ctypes.c_uint32, vp]
+    lib.clis_debug_wait_selftest.restype = i32
     _lib = lib
     return lib
 
@@ -169,6 +171,13 @@ def clis_clear_device_error() -> None:
     st = load_library().clis_clear_device_error()
     if st != 0:
         raise ClisError("clis_clear_device_error", st)
+
+
+def clis_debug_wait_selftest(limit_us: int = 1000, stream=None) -> None:
+    """Launch the bounded-wait self-test kernel (see include/clis.h)."""
+    st = load_library().clis_debug_wait_selftest(int(limit_us), _stream(stream))
+    if st != 0:
+        raise ClisError("clis_debug_wait_selftest", st)
 
 
 def decode_certs(certs) -> list[dict]:

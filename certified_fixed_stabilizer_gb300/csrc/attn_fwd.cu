@@ -737,7 +737,28 @@ clis_status_t launch_impl(const AttnArgs &a, cudaStream_t stream)
     return cudaGetLastError() == cudaSuccess ? CLIS_OK : CLIS_ERR_CUDA;
 }
 
+// One warp waits on a barrier that nothing arrives on; the bounded wait must
+// give up after limit_ns, set the error word and let the kernel return.
+__global__ void wait_selftest_kernel(uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    mbar_wait_warp(smem_u32(&bar), 0, &abort_flag, &g_attn_error_word, CLIS_WAIT_SELFTEST_BIT, limit_ns);
+}
+
 }  // namespace
+
+clis_status_t launch_wait_selftest(uint32_t limit_us, cudaStream_t stream)
+{
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(static_cast<uint64_t>(limit_us) * 1000ull);
+    return cudaGetLastError() == cudaSuccess ? CLIS_OK : CLIS_ERR_CUDA;
+}
 
 clis_status_t launch_attn_fwd(const AttnArgs &a, cudaStream_t stream)
 {

@@ -201,4 +201,10 @@ clis_status_t clis_get_device_error(uint32_t *code)
 
 clis_status_t clis_clear_device_error(void) { return clis::clear_device_error(); }
 
+clis_status_t clis_debug_wait_selftest(uint32_t limit_us, clis_stream_t stream)
+{
+    if (limit_us < 1 || limit_us > 1000000) return CLIS_ERR_INVALID_ARG;
+    return clis::launch_wait_selftest(limit_us, reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

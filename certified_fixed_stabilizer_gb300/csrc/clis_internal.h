@@ -65,6 +65,7 @@ struct AttnArgs {
 // Returns CLIS_OK, CLIS_ERR_CUDA (tensor-map encode or launch failure).
 clis_status_t launch_attn_fwd(const AttnArgs &a, cudaStream_t stream);
 
+clis_status_t launch_wait_selftest(uint32_t limit_us, cudaStream_t stream);
 clis_status_t read_device_error(uint32_t *code);
 clis_status_t clear_device_error();
 

@@ -83,9 +83,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // Warp-uniform form: every lane of the warp calls it; the result is the same
 // in all lanes (false as soon as one lane gave up).
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                               unsigned int *err_word, unsigned int site)
+                                               unsigned int *err_word, unsigned int site,
+                                               uint64_t limit_ns = (1ull << 31))
 {
-    const bool ok = mbar_wait(bar, parity, abort_flag, err_word, site);
+    const bool ok = mbar_wait(bar, parity, abort_flag, err_word, site, limit_ns);
     return __all_sync(0xFFFFFFFFu, ok);
 }
 

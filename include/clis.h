@@ -199,6 +199,15 @@ CLIS_API clis_status_t clis_get_device_error(uint32_t *code);
 /* Resets the device error word of the current device to 0 (synchronous). */
 CLIS_API clis_status_t clis_clear_device_error(void);
 
+/* Self-test of the kernels' bounded waits (no counterpart in the paper).
+ * Launches one small kernel whose single wait is on a barrier that nothing
+ * ever arrives on, with a limit of limit_us microseconds (1..1,000,000): the
+ * wait gives up, records CLIS_WAIT_SELFTEST_BIT in the device error word and
+ * the kernel returns, leaving the context usable.  Read the word with
+ * clis_get_device_error() and reset it with clis_clear_device_error(). */
+#define CLIS_WAIT_SELFTEST_BIT (1u << 8)
+CLIS_API clis_status_t clis_debug_wait_selftest(uint32_t limit_us, clis_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,7 +26,7 @@ def _declared_symbols():
 def test_header_declares_the_boundary():
     names = _declared_symbols()
     for n in ("clis_certify_workspace_size", "clis_certify", "clis_attn_fwd", "clis_status_string",
-              "clis_get_device_error", "clis_clear_device_error"):
+              "clis_get_device_error", "clis_clear_device_error", "clis_debug_wait_selftest"):
         assert n in names
 
 
@@ -34,6 +34,12 @@ def test_library_exports_every_declared_symbol(clis):
     lib = ctypes.CDLL(clis.library_path())
     for n in _declared_symbols():
         assert hasattr(lib, n), n
+
+
+def test_wait_selftest_rejects_bad_limits(clis):
+    lib = clis.load_library()
+    assert lib.clis_debug_wait_selftest(0, None) == 1
+    assert lib.clis_debug_wait_selftest(2_000_000, None) == 1
 
 
 def test_status_strings(clis):

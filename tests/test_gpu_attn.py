@@ -198,3 +198,22 @@ def test_outputs_are_deterministic():
     a, _, _ = _run(q, k, v, False, "auto")
     b, _, _ = _run(q, k, v, False, "auto")
     assert torch.equal(a, b)
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """A kernel wait on a barrier that nothing arrives on gives up after its
+    limit, reports through the device error word, and the next launches run
+    normally (failure detection without a GPU fault)."""
+    dev = need_gpu()
+    clis.clis_clear_device_error()
+    clis.clis_debug_wait_selftest(2000)
+    code = clis.clis_get_device_error()
+    assert code & (1 << 8), code
+    clis.clis_clear_device_error()
+    assert clis.clis_get_device_error() == 0
+    w = WORKLOADS["tiny"]
+    q, k, v = make_inputs(w, device=dev)
+    out, _, _ = _run(q, k, v, False, "auto")
+    ref, _ = _oracle(q, k, v, False)
+    assert_close_to_oracle(out.float().cpu().numpy(), ref, "after selftest")
+    assert clis.clis_get_device_error() == 0
