@@ -328,6 +328,40 @@ def main():
         line["online_lazy"] = {"value": flops / (statistics.mean(lz_attn) * 1e-3) / 1e12, "unit": "TFLOP/s",
                                "ms": statistics.mean(lz_attn)}
         line["certified_speedup_vs_online_lazy"] = statistics.mean(lz_attn) / attn_avg_ms
+        # Ring-step form: K/V in 8 chunks, each merged into fp32 accumulators
+        # (clis_attn_fwd_chunk), then clis_attn_chunk_finalize.  Certified heads
+        # add their partials with no rescaling; online heads rescale per chunk.
+        if not w.causal:
+            n_chunks = 8
+            bounds = [round(i * w.N / n_chunks) for i in range(n_chunks + 1)]
+            bounds = [b - b % 8 if 0 < b < w.N else b for b in bounds]
+            o_acc = torch.empty((heads * w.N, w.d), dtype=torch.float32, device=dev)
+            l_acc = torch.empty((heads * w.N,), dtype=torch.float32, device=dev)
+            m_acc = torch.empty((heads * w.N,), dtype=torch.float32, device=dev)
+
+            def chunk_pass(variant):
+                for i, (a, b) in enumerate(zip(bounds[:-1], bounds[1:])):
+                    clis.clis_attn_fwd_chunk(q, k[:, :, a:b], v[:, :, a:b], sl2, o_acc, l_acc, m_acc, kbar=kbar,
+                                             certs=certs, first=(i == 0), variant=variant)
+                clis.clis_attn_chunk_finalize(q, o_acc, l_acc, m_acc, out=out)
+
+            chunked = {"chunks": n_chunks}
+            for variant in ("auto", "online"):
+                for _ in range(args.warmup):
+                    chunk_pass(variant)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(args.steps):
+                    chunk_pass(variant)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / args.steps
+                chunked["certified" if variant == "auto" else "online"] = {
+                    "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms": ms}
+            chunked["certified_speedup_vs_online"] = chunked["online"]["ms"] / chunked["certified"]["ms"]
+            line["chunked"] = chunked
+            del o_acc, l_acc, m_acc
         # End to end through the public call with pinned host buffers.
         qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
         oh = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)

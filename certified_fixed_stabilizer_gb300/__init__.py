@@ -16,7 +16,7 @@ _BINDING_NAMES = {
     "clis_status_string", "clis_get_device_error", "clis_clear_device_error",
     "ClisError", "attention", "certify", "Cert", "VARIANT", "FMT", "STATUS",
     "library_path", "load_library", "decode_certs", "make_shape", "scale_log2_for",
-    "Shape", "CERT_WORDS", "LOG2E", "clis_debug_wait_selftest",
+    "Shape", "CERT_WORDS", "LOG2E", "clis_debug_wait_selftest", "clis_attn_fwd_chunk", "clis_attn_chunk_finalize",
 }
 
 

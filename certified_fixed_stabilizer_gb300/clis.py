@@ -74,6 +74,10 @@ def load_library():
     lib.clis_get_device_error.restype = i32
     lib.clis_clear_device_error.argtypes = []
     lib.clis_clear_device_error.restype = i32
+    lib.clis_attn_fwd_chunk.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp]
+    lib.clis_attn_fwd_chunk.restype = i32
+    lib.clis_attn_chunk_finalize.argtypes = [sp, vp, vp, vp, vp, vp, vp]
+    lib.clis_attn_chunk_finalize.restype = i32
     lib.clis_debug_wait_selftest.argtypes = [ctypes.c_uint32, vp]
     lib.clis_debug_wait_selftest.restype = i32
     _lib = lib
@@ -156,6 +160,32 @@ def clis_attn_fwd(q, k, v, scale_log2: float, kbar=None, certs=None, causal: boo
                            VARIANT[variant], _stream(stream))
     if st != 0:
         raise ClisError("clis_attn_fwd", st)
+    return out
+
+
+def clis_attn_fwd_chunk(q, k, v, scale_log2: float, o_acc, l_acc, m_acc, kbar=None, certs=None,
+                        first: bool = False, variant: str = "auto", stream=None):
+    """Merge one KV chunk (k, v: [B, H, Nk_chunk, d]) into fp32 accumulators
+    o_acc [B*H*Nq, d], l_acc [B*H*Nq], m_acc [B*H*Nq]."""
+    lib = load_library()
+    shape = make_shape(q, k, v)
+    st = lib.clis_attn_fwd_chunk(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(o_acc), _ptr(l_acc),
+                                 _ptr(m_acc), _ptr(kbar), _ptr(certs), float(scale_log2), int(bool(first)),
+                                 VARIANT[variant], _stream(stream))
+    if st != 0:
+        raise ClisError("clis_attn_fwd_chunk", st)
+
+
+def clis_attn_chunk_finalize(q, o_acc, l_acc, m_acc, out=None, lse2=None, stream=None):
+    """o = o_acc / l_acc (bf16, shape of q), optional lse2 = m_acc + log2 l_acc."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    shape = make_shape(q, q, q, out)
+    st = lib.clis_attn_chunk_finalize(ctypes.byref(shape), _ptr(o_acc), _ptr(l_acc), _ptr(m_acc), _ptr(out),
+                                      _ptr(lse2), _stream(stream))
+    if st != 0:
+        raise ClisError("clis_attn_chunk_finalize", st)
     return out
 
 

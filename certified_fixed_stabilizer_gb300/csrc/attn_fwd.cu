@@ -87,6 +87,11 @@ struct Params {
     int num_tiles;  // B * H * nqb
     float scale_log2;
     int variant;
+    // KV-chunk mode (0 = off): the epilogue merges this chunk's unnormalised
+    // partial into fp32 accumulators instead of writing O.  1 = merge, 2 = first
+    // chunk (overwrite).
+    int chunk_mode;
+    float *o_acc, *l_acc, *m_acc;
 };
 
 struct __align__(8) Ctl {
@@ -495,7 +500,51 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
         // Epilogue: O / l -> bf16, written straight from registers.
         if (!mbar_wait(smem_u32(&c.pv_done[t]), (g - 1) & 1, ab, err, kErrSoftmax)) goto abort;
         tc_fence_after();
-        {
+        if (p.chunk_mode) {
+            // KV-chunk merge.  The accumulator of row i holds sum_j 2^(x_ij - m_i) v_j and
+            // sum_j 2^(x_ij - m_i) over the chunks merged so far, x = scale_log2 * s.  A
+            // certified head uses the same shift mu_i in every chunk, so its partials add
+            // with no exponentials; an online head rescales to the larger maximum.
+            const float m_c = T.cert ? mu : ((m_run == -INFINITY) ? 0.f : m_run);
+            const int64_t ridx = static_cast<int64_t>(T.bh) * p.Nq + row;
+            float a_old = 0.f, a_new = 1.f;
+            if (row_ok && p.chunk_mode == 1) {
+                const float m_old = p.m_acc[ridx];
+                if (m_old == m_c) {
+                    a_old = 1.f;
+                } else {
+                    const float m_new = fmaxf(m_old, m_c);
+                    a_old = ex2_approx(m_old - m_new);
+                    a_new = ex2_approx(m_c - m_new);
+                    p.m_acc[ridx] = m_new;
+                }
+            } else if (row_ok) {
+                p.m_acc[ridx] = m_c;
+            }
+            float4 *oa = reinterpret_cast<float4 *>(p.o_acc + ridx * D);
+#pragma unroll 1
+            for (int c32 = 0; c32 < D / 32; c32++) {
+                uint32_t r[32];
+                tmem_ld32(tO + c32 * 32, r);
+                tmem_wait_ld();
+                if (row_ok) {
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (p.chunk_mode == 1) acc = oa[c32 * 8 + e];
+                        acc.x = fmaf(a_new, __uint_as_float(r[4 * e + 0]), a_old * acc.x);
+                        acc.y = fmaf(a_new, __uint_as_float(r[4 * e + 1]), a_old * acc.y);
+                        acc.z = fmaf(a_new, __uint_as_float(r[4 * e + 2]), a_old * acc.z);
+                        acc.w = fmaf(a_new, __uint_as_float(r[4 * e + 3]), a_old * acc.w);
+                        oa[c32 * 8 + e] = acc;
+                    }
+                }
+            }
+            if (row_ok) {
+                const float l_old = (p.chunk_mode == 1) ? p.l_acc[ridx] : 0.f;
+                p.l_acc[ridx] = fmaf(a_new, l_run, a_old * l_old);
+            }
+        } else {
             const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
             uint16_t *orow = p.o + T.b * p.o_sb + T.h * p.o_sh + static_cast<int64_t>(row) * p.o_sn;
 #pragma unroll
@@ -731,6 +780,10 @@ clis_status_t launch_impl(const AttnArgs &a, cudaStream_t stream)
     if (p.grp < 1) p.grp = 1;
     p.scale_log2 = a.scale_log2;
     p.variant = a.variant;
+    p.chunk_mode = a.chunk_mode;
+    p.o_acc = a.o_acc;
+    p.l_acc = a.l_acc;
+    p.m_acc = a.m_acc;
     if (p.num_tiles == 0) return CLIS_OK;
     const int grid = p.num_tiles < nsm ? p.num_tiles : nsm;
     attn_fwd_kernel<D, CAUSAL><<<grid, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
@@ -752,7 +805,42 @@ __global__ void wait_selftest_kernel(uint64_t limit_ns)
     mbar_wait_warp(smem_u32(&bar), 0, &abort_flag, &g_attn_error_word, CLIS_WAIT_SELFTEST_BIT, limit_ns);
 }
 
+// O = O_acc / l (bf16) and lse2 = m + log2 l after the last KV chunk;
+// one thread per 8 output columns of a row.
+__global__ void chunk_finalize_kernel(ChunkFinalizeArgs a)
+{
+    const int per_row = a.d / 8;
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t n = static_cast<int64_t>(a.B) * a.H * a.Nq * per_row;
+    if (idx >= n) return;
+    const int c8 = static_cast<int>(idx % per_row);
+    const int64_t ridx = idx / per_row;
+    const int row = static_cast<int>(ridx % a.Nq);
+    const int bh = static_cast<int>(ridx / a.Nq);
+    const int b = bh / a.H, h = bh % a.H;
+    const float l = a.l_acc[ridx];
+    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+    const float4 *src = reinterpret_cast<const float4 *>(a.o_acc + ridx * a.d + c8 * 8);
+    const float4 x0 = src[0], x1 = src[1];
+    uint4 out;
+    out.x = pack_bf16x2(x0.x * inv, x0.y * inv);
+    out.y = pack_bf16x2(x0.z * inv, x0.w * inv);
+    out.z = pack_bf16x2(x1.x * inv, x1.y * inv);
+    out.w = pack_bf16x2(x1.z * inv, x1.w * inv);
+    *reinterpret_cast<uint4 *>(a.o + b * a.o_sb + h * a.o_sh + static_cast<int64_t>(row) * a.o_sn + c8 * 8) = out;
+    if (a.lse2 && c8 == 0) a.lse2[ridx] = a.m_acc[ridx] + log2f(l);
+}
+
 }  // namespace
+
+clis_status_t launch_chunk_finalize(const ChunkFinalizeArgs &a, cudaStream_t stream)
+{
+    const int64_t n = static_cast<int64_t>(a.B) * a.H * a.Nq * (a.d / 8);
+    if (n == 0) return CLIS_OK;
+    const int threads = 256;
+    chunk_finalize_kernel<<<static_cast<unsigned>((n + threads - 1) / threads), threads, 0, stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? CLIS_OK : CLIS_ERR_CUDA;
+}
 
 clis_status_t launch_wait_selftest(uint32_t limit_us, cudaStream_t stream)
 {

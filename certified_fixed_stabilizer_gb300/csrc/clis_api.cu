@@ -179,6 +179,92 @@ clis_status_t clis_certify_noalloc(const clis_shape_t *shape, const void *q, con
                         CLIS_NOALLOC_SCRATCH_BYTES, stream);
 }
 
+clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void *q, const void *k, const void *v,
+                                  float *o_acc, float *l_acc, float *m_acc, const float *kbar,
+                                  const clis_head_cert_t *certs, float scale_log2, int first, clis_variant_t variant,
+                                  clis_stream_t stream)
+{
+    clis_status_t st = check_shape(shape, false);
+    if (st != CLIS_OK) return st;
+    if (shape->B * shape->H == 0 || shape->Nq == 0) return CLIS_OK;
+    if (!q || !k || !v || !o_acc || !l_acc || !m_acc) return CLIS_ERR_INVALID_ARG;
+    if (!std::isfinite(scale_log2) || !(scale_log2 > 0.f)) return CLIS_ERR_INVALID_ARG;
+    if (first != 0 && first != 1) return CLIS_ERR_INVALID_ARG;
+    if (variant != CLIS_AUTO && variant != CLIS_ONLINE && variant != CLIS_CERTIFIED_FORCED &&
+        variant != CLIS_ONLINE_LAZY)
+        return CLIS_ERR_INVALID_ARG;
+    if ((variant == CLIS_AUTO || variant == CLIS_CERTIFIED_FORCED) && !kbar) return CLIS_ERR_INVALID_ARG;
+    if (variant == CLIS_AUTO && !certs) return CLIS_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_acc)) return CLIS_ERR_MISALIGNED;
+    if ((kbar && !aligned16(kbar)) || (certs && !aligned16(certs)) ||
+        (reinterpret_cast<uintptr_t>(l_acc) & 3u) || (reinterpret_cast<uintptr_t>(m_acc) & 3u))
+        return CLIS_ERR_MISALIGNED;
+    const int64_t tiles = shape->B * shape->H * div_up(shape->Nq, 256);
+    if (tiles > kMaxN) return CLIS_ERR_UNSUPPORTED;
+
+    clis::AttnArgs a;
+    a.q = static_cast<const uint16_t *>(q);
+    a.k = static_cast<const uint16_t *>(k);
+    a.v = static_cast<const uint16_t *>(v);
+    a.o = nullptr;
+    a.lse2 = nullptr;
+    a.kbar = kbar;
+    a.certs = certs;
+    a.q_sb = shape->q_sb;
+    a.q_sh = shape->q_sh;
+    a.q_sn = shape->q_sn;
+    a.k_sb = shape->k_sb;
+    a.k_sh = shape->k_sh;
+    a.k_sn = shape->k_sn;
+    a.v_sb = shape->v_sb;
+    a.v_sh = shape->v_sh;
+    a.v_sn = shape->v_sn;
+    a.o_sb = a.o_sh = a.o_sn = 0;
+    a.B = static_cast<int>(shape->B);
+    a.H = static_cast<int>(shape->H);
+    a.Nq = static_cast<int>(shape->Nq);
+    a.Nk = static_cast<int>(shape->Nk);
+    a.d = static_cast<int>(shape->d);
+    a.scale_log2 = scale_log2;
+    a.causal = 0;
+    a.variant = variant;
+    a.chunk_mode = first ? 2 : 1;
+    a.o_acc = o_acc;
+    a.l_acc = l_acc;
+    a.m_acc = m_acc;
+    return clis::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+clis_status_t clis_attn_chunk_finalize(const clis_shape_t *shape, const float *o_acc, const float *l_acc,
+                                       const float *m_acc, void *o, float *lse2, clis_stream_t stream)
+{
+    if (!shape) return CLIS_ERR_INVALID_ARG;
+    if (shape->B < 0 || shape->H < 0 || shape->Nq < 0) return CLIS_ERR_INVALID_ARG;
+    if (shape->d != 64 && shape->d != 128) return CLIS_ERR_UNSUPPORTED;
+    if (shape->Nq > kMaxN || shape->B * shape->H > kMaxN) return CLIS_ERR_UNSUPPORTED;
+    if (shape->B * shape->H == 0 || shape->Nq == 0) return CLIS_OK;
+    if (!o_acc || !l_acc || !m_acc || !o) return CLIS_ERR_INVALID_ARG;
+    clis_status_t st = check_strides(shape->o_sb, shape->o_sh, shape->o_sn, shape->d);
+    if (st != CLIS_OK) return st;
+    if (!aligned16(o_acc) || !aligned16(o) || (reinterpret_cast<uintptr_t>(l_acc) & 3u) ||
+        (reinterpret_cast<uintptr_t>(m_acc) & 3u) || (lse2 && (reinterpret_cast<uintptr_t>(lse2) & 3u)))
+        return CLIS_ERR_MISALIGNED;
+    clis::ChunkFinalizeArgs a;
+    a.o_acc = o_acc;
+    a.l_acc = l_acc;
+    a.m_acc = m_acc;
+    a.o = static_cast<uint16_t *>(o);
+    a.lse2 = lse2;
+    a.o_sb = shape->o_sb;
+    a.o_sh = shape->o_sh;
+    a.o_sn = shape->o_sn;
+    a.B = static_cast<int>(shape->B);
+    a.H = static_cast<int>(shape->H);
+    a.Nq = static_cast<int>(shape->Nq);
+    a.d = static_cast<int>(shape->d);
+    return clis::launch_chunk_finalize(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 const char *clis_status_string(clis_status_t s)
 {
     switch (s) {

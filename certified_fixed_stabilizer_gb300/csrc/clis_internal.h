@@ -59,7 +59,19 @@ struct AttnArgs {
     float scale_log2;
     int causal;
     int variant;
+    int chunk_mode = 0;  // 0 off, 1 merge into the accumulators, 2 first chunk
+    float *o_acc = nullptr, *l_acc = nullptr, *m_acc = nullptr;
 };
+
+struct ChunkFinalizeArgs {
+    const float *o_acc, *l_acc, *m_acc;
+    uint16_t *o;
+    float *lse2;
+    int64_t o_sb, o_sh, o_sn;
+    int B, H, Nq, d;
+};
+
+clis_status_t launch_chunk_finalize(const ChunkFinalizeArgs &a, cudaStream_t stream);
 
 // Builds the tensor maps and launches the persistent attention kernel.
 // Returns CLIS_OK, CLIS_ERR_CUDA (tensor-map encode or launch failure).

@@ -187,6 +187,34 @@ CLIS_API clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, c
                             const clis_head_cert_t *certs, float scale_log2, int causal,
                             clis_variant_t variant, clis_stream_t stream);
 
+/* One KV chunk of a ring / context-parallel attention step (paper: Table 7,
+ * the ring and 2D-ring columns, and Figure 6, one ring attention step).  The
+ * keys and values of a head are split into chunks that arrive one at a time;
+ * each call runs the fused kernel over one chunk (shape->Nk = its length, k and
+ * v point at it) and merges the chunk's partial result into fp32 accumulators
+ * kept by the caller (contiguous, index (b*H + h)*Nq + i):
+ *   o_acc [B*H*Nq*d]  sum_j 2^(x_ij - m_i) v_j over the keys merged so far
+ *   l_acc [B*H*Nq]    sum_j 2^(x_ij - m_i)
+ *   m_acc [B*H*Nq]    the shift m_i (exp2 units), x_ij = scale_log2 * q_i . k_j
+ * first = 1 overwrites the accumulators (first chunk), 0 merges.  A certified
+ * head's shift is its fixed stabiliser mu_i in every chunk, so its partials
+ * add with no exponentials and no rescaling; other heads merge by rescaling
+ * to the larger maximum.  kbar and certs must come from clis_certify over the
+ * whole key sequence (for a ring: the k-bar partials and norm maxima of all
+ * chunks reduced before the first step).  Non-causal only; shape->o_* ignored.
+ * Errors as clis_attn_fwd. */
+CLIS_API clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void *q, const void *k,
+                                  const void *v, float *o_acc, float *l_acc, float *m_acc,
+                                  const float *kbar, const clis_head_cert_t *certs,
+                                  float scale_log2, int first, clis_variant_t variant,
+                                  clis_stream_t stream);
+
+/* After the last chunk: o = o_acc / l_acc (bf16, strides shape->o_*) and, if
+ * lse2 is not NULL, lse2 = m_acc + log2(l_acc). */
+CLIS_API clis_status_t clis_attn_chunk_finalize(const clis_shape_t *shape, const float *o_acc,
+                                       const float *l_acc, const float *m_acc, void *o,
+                                       float *lse2, clis_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 CLIS_API const char *clis_status_string(clis_status_t status);
 

@@ -26,7 +26,8 @@ def _declared_symbols():
 def test_header_declares_the_boundary():
     names = _declared_symbols()
     for n in ("clis_certify_workspace_size", "clis_certify", "clis_attn_fwd", "clis_status_string",
-              "clis_get_device_error", "clis_clear_device_error", "clis_debug_wait_selftest"):
+              "clis_get_device_error", "clis_clear_device_error", "clis_debug_wait_selftest",
+              "clis_attn_fwd_chunk", "clis_attn_chunk_finalize", "clis_certify_noalloc"):
         assert n in names
 
 
@@ -122,6 +123,25 @@ def test_attn_rejects_bad_arguments(clis):
     s = _shape(clis)
     s.q_sh = 12
     assert _attn(clis, s) == MIS
+
+
+def test_chunk_entry_points_reject_bad_arguments(clis):
+    lib = clis.load_library()
+    vp = ctypes.c_void_p
+    s = _shape(clis)
+    call = lambda **kw: lib.clis_attn_fwd_chunk(ctypes.byref(s), vp(kw.get("q", FAKE)), vp(FAKE), vp(FAKE),
+                                                vp(kw.get("oa", FAKE)), vp(kw.get("la", FAKE)), vp(FAKE), vp(FAKE),
+                                                vp(FAKE), kw.get("scale", 0.1), kw.get("first", 0),
+                                                kw.get("variant", 0), None)
+    assert call(oa=0) == 1
+    assert call(first=3) == 1
+    assert call(scale=-1.0) == 1
+    assert call(variant=9) == 1
+    assert call(oa=FAKE + 4) == 3
+    assert call(la=FAKE + 2) == 3
+    assert lib.clis_attn_chunk_finalize(ctypes.byref(s), vp(FAKE), vp(FAKE), vp(FAKE), vp(0), None, None) == 1
+    s2 = _shape(clis, d=80)
+    assert lib.clis_attn_chunk_finalize(ctypes.byref(s2), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, None) == 2
 
 
 def test_binding_has_no_cpu_fallback(clis):
