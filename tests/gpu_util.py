@@ -31,8 +31,19 @@ def head_errors(got: np.ndarray, ref: np.ndarray):
     return err.max(axis=1), err.mean(axis=1)
 
 
+def report(what: str, **values):
+    """Append measured errors to the JSON-lines file named by CLIS_PARITY_REPORT (if set)."""
+    import json
+    import os
+    path = os.environ.get("CLIS_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": what, **values}) + "\n")
+
+
 def assert_close_to_oracle(got: np.ndarray, ref: np.ndarray, what: str = ""):
     mx, mn = head_errors(got, ref)
+    report(what, max_abs=float(mx.max()), mean_abs=float(mn.max()))
     assert np.all(np.isfinite(got)), f"{what}: non-finite outputs"
     assert mx.max() <= MAX_ABS, f"{what}: max abs err {mx.max():.3e} (head {mx.argmax()})"
     assert mn.max() <= MEAN_ABS, f"{what}: mean abs err {mn.max():.3e} (head {mn.argmax()})"
