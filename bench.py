@@ -240,14 +240,16 @@ def main():
     certs = torch.empty((heads, clis.CERT_WORDS), dtype=torch.int32, device=dev)
     wsp = torch.empty(max(256, clis.clis_certify_workspace_size(shape)), dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
+    mu = torch.empty(heads * w.N, dtype=torch.float32, device=dev)  # per-row stabilisers
     in_bytes = 3 * q.numel() * q.element_size()
     needs_flush = in_bytes < 2 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if needs_flush else None
 
     def step(variant):
         if variant in ("auto", "certified"):
-            clis.clis_certify(q, k, v, sl2, kbar=kbar, certs=certs, workspace=wsp)
-        clis.clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=w.causal, variant=variant, out=out)
+            clis.clis_certify(q, k, v, sl2, kbar=kbar, certs=certs, workspace=wsp, mu=mu)
+        clis.clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=w.causal, variant=variant, out=out,
+                           mu=mu)
 
     def timed_loop(variant, steps, warmup):
         for _ in range(warmup):
@@ -262,10 +264,10 @@ def main():
                 flush_buf.zero_()
             e0.record(stream)
             if variant in ("auto", "certified"):
-                clis.clis_certify(q, k, v, sl2, kbar=kbar, certs=certs, workspace=wsp)
+                clis.clis_certify(q, k, v, sl2, kbar=kbar, certs=certs, workspace=wsp, mu=mu)
             e1.record(stream)
             clis.clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=w.causal, variant=variant,
-                               out=out)
+                               out=out, mu=mu)
             e2.record(stream)
         torch.cuda.synchronize()
         barrier(ws)
@@ -342,7 +344,7 @@ def main():
             def chunk_pass(variant):
                 for i, (a, b) in enumerate(zip(bounds[:-1], bounds[1:])):
                     clis.clis_attn_fwd_chunk(q, k[:, :, a:b], v[:, :, a:b], sl2, o_acc, l_acc, m_acc, kbar=kbar,
-                                             certs=certs, first=(i == 0), variant=variant)
+                                             certs=certs, first=(i == 0), variant=variant, mu=mu)
                 clis.clis_attn_chunk_finalize(q, o_acc, l_acc, m_acc, out=out)
 
             chunked = {"chunks": n_chunks}
@@ -371,9 +373,9 @@ def main():
             dq.copy_(qh, non_blocking=True)
             dk.copy_(kh, non_blocking=True)
             dv.copy_(vh, non_blocking=True)
-            clis.clis_certify(dq, dk, dv, sl2, kbar=kbar, certs=certs, workspace=wsp)
+            clis.clis_certify(dq, dk, dv, sl2, kbar=kbar, certs=certs, workspace=wsp, mu=mu)
             clis.clis_attn_fwd(dq, dk, dv, sl2, kbar=kbar, certs=certs, causal=w.causal, variant=args.variant,
-                               out=out)
+                               out=out, mu=mu)
             oh.copy_(out, non_blocking=True)
 
         for _ in range(max(1, args.warmup)):

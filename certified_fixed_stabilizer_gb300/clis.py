@@ -64,9 +64,9 @@ def load_library():
     sp = ctypes.POINTER(Shape)
     lib.clis_certify_workspace_size.argtypes = [sp, ctypes.POINTER(sz)]
     lib.clis_certify_workspace_size.restype = i32
-    lib.clis_certify.argtypes = [sp, vp, vp, vp, f32, i32, i32, vp, vp, vp, sz, vp]
+    lib.clis_certify.argtypes = [sp, vp, vp, vp, f32, i32, i32, vp, vp, vp, vp, sz, vp]
     lib.clis_certify.restype = i32
-    lib.clis_attn_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp]
+    lib.clis_attn_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp]
     lib.clis_attn_fwd.restype = i32
     lib.clis_status_string.argtypes = [i32]
     lib.clis_status_string.restype = ctypes.c_char_p
@@ -74,7 +74,7 @@ def load_library():
     lib.clis_get_device_error.restype = i32
     lib.clis_clear_device_error.argtypes = []
     lib.clis_clear_device_error.restype = i32
-    lib.clis_attn_fwd_chunk.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp]
+    lib.clis_attn_fwd_chunk.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp]
     lib.clis_attn_fwd_chunk.restype = i32
     lib.clis_attn_chunk_finalize.argtypes = [sp, vp, vp, vp, vp, vp, vp]
     lib.clis_attn_chunk_finalize.restype = i32
@@ -126,9 +126,10 @@ def clis_certify_workspace_size(shape: Shape) -> int:
 
 
 def clis_certify(q, k, v, scale_log2: float, exp_fmt: str = "bf16", acc_fmt: str = "fp32",
-                 kbar=None, certs=None, workspace=None, stream=None):
+                 kbar=None, certs=None, workspace=None, stream=None, mu=None):
     """Certification pre-pass.  Returns (kbar float32 [B*H, d], certs int32 [B*H, 8]);
-    decode certificates with :func:`decode_certs`."""
+    decode certificates with :func:`decode_certs`.  If ``mu`` (float32 [B*H*Nq])
+    is given it receives the per-row stabilisers."""
     lib = load_library()
     shape = make_shape(q, k, v)
     BH, d = shape.B * shape.H, shape.d
@@ -141,7 +142,7 @@ def clis_certify(q, k, v, scale_log2: float, exp_fmt: str = "bf16", acc_fmt: str
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     st = lib.clis_certify(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), float(scale_log2),
-                          FMT[exp_fmt], FMT[acc_fmt], _ptr(kbar), _ptr(certs), _ptr(workspace),
+                          FMT[exp_fmt], FMT[acc_fmt], _ptr(kbar), _ptr(certs), _ptr(mu), _ptr(workspace),
                           workspace.numel(), _stream(stream))
     if st != 0:
         raise ClisError("clis_certify", st)
@@ -149,14 +150,14 @@ def clis_certify(q, k, v, scale_log2: float, exp_fmt: str = "bf16", acc_fmt: str
 
 
 def clis_attn_fwd(q, k, v, scale_log2: float, kbar=None, certs=None, causal: bool = False,
-                  variant: str = "auto", out=None, lse2=None, stream=None):
+                  variant: str = "auto", out=None, lse2=None, stream=None, mu=None):
     """Fused attention forward; returns ``out`` (bf16, shape of q)."""
     lib = load_library()
     if out is None:
         out = torch.empty_like(q, memory_format=torch.contiguous_format)
     shape = make_shape(q, k, v, out)
     st = lib.clis_attn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse2),
-                           _ptr(kbar), _ptr(certs), float(scale_log2), int(bool(causal)),
+                           _ptr(kbar), _ptr(certs), _ptr(mu), float(scale_log2), int(bool(causal)),
                            VARIANT[variant], _stream(stream))
     if st != 0:
         raise ClisError("clis_attn_fwd", st)
@@ -164,13 +165,14 @@ def clis_attn_fwd(q, k, v, scale_log2: float, kbar=None, certs=None, causal: boo
 
 
 def clis_attn_fwd_chunk(q, k, v, scale_log2: float, o_acc, l_acc, m_acc, kbar=None, certs=None,
-                        first: bool = False, variant: str = "auto", stream=None):
+                        first: bool = False, variant: str = "auto", stream=None, mu=None):
     """Merge one KV chunk (k, v: [B, H, Nk_chunk, d]) into fp32 accumulators
     o_acc [B*H*Nq, d], l_acc [B*H*Nq], m_acc [B*H*Nq]."""
     lib = load_library()
     shape = make_shape(q, k, v)
     st = lib.clis_attn_fwd_chunk(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(o_acc), _ptr(l_acc),
-                                 _ptr(m_acc), _ptr(kbar), _ptr(certs), float(scale_log2), int(bool(first)),
+                                 _ptr(m_acc), _ptr(kbar), _ptr(certs), _ptr(mu), float(scale_log2),
+                                 int(bool(first)),
                                  VARIANT[variant], _stream(stream))
     if st != 0:
         raise ClisError("clis_attn_fwd_chunk", st)
@@ -245,10 +247,11 @@ def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
         dev = torch.device(device or "cuda:0")
         q, k, v = (t.to(dev, non_blocking=True) for t in (q, k, v))
     sl2 = scale_log2_for(q.shape[-1], softmax_scale)
-    kbar = certs = None
+    kbar = certs = mu = None
     if variant in ("auto", "certified"):
-        kbar, certs = clis_certify(q, k, v, sl2)
-    out = clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=causal, variant=variant)
+        mu = torch.empty(q.shape[0] * q.shape[1] * q.shape[2], dtype=torch.float32, device=q.device)
+        kbar, certs = clis_certify(q, k, v, sl2, mu=mu)
+    out = clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=causal, variant=variant, mu=mu)
     if on_host:
         out = out.to("cpu")
     if return_certs:

@@ -79,6 +79,7 @@ struct Params {
     float *lse2;
     const float *kbar;
     const clis_head_cert_t *certs;
+    const float *mu;  // optional per-row stabilisers [B*H*Nq]
     int64_t q_sb, q_sh, q_sn, o_sb, o_sh, o_sn;
     int B, H, Nq, Nk;
     int nqb;        // 256-row query blocks per head
@@ -366,7 +367,9 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
 
         // Certified path: mu_i = scale_log2 * (q_i . kbar), fixed for the whole KV loop.
         float mu = 0.f;
-        if (T.cert && row_ok) {
+        if (T.cert && row_ok && p.mu) {
+            mu = __ldg(p.mu + static_cast<int64_t>(T.bh) * p.Nq + row);
+        } else if (T.cert && row_ok) {
             const uint16_t *qr = p.q + T.b * p.q_sb + T.h * p.q_sh + static_cast<int64_t>(row) * p.q_sn;
             const float *kb = p.kbar + static_cast<int64_t>(T.bh) * D;
             float acc0 = 0.f, acc1 = 0.f;
@@ -760,6 +763,7 @@ clis_status_t launch_impl(const AttnArgs &a, cudaStream_t stream)
     p.lse2 = a.lse2;
     p.kbar = a.kbar;
     p.certs = a.certs;
+    p.mu = a.mu;
     p.q_sb = a.q_sb;
     p.q_sh = a.q_sh;
     p.q_sn = a.q_sn;

@@ -192,10 +192,15 @@ __global__ void __launch_bounds__(kCertThreads) certify_norms_kernel(CertArgs a,
         const uint16_t *base = a.q + b * a.q_sb + h * a.q_sh + cv * 8;
         float mx = 0.f;
         uint32_t amax = 0;
+        // Optional per-row stabiliser mu_i = scale_log2 * (q_i . kbar) for the
+        // attention kernel (the shift Figure 5(a) fixes before the KV loop).
+        float kb[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) kb[e] = a.mu ? a.kbar[static_cast<int64_t>(bh) * D + cv * 8 + e] : 0.f;
 #pragma unroll 4
         for (int sw = 0; sw < nsweeps; sw++) {
             const int r = r0 + sw * RPS + rp;
-            float ss = 0.f;
+            float ss = 0.f, dot = 0.f;
             if (r < r1) {
                 const uint4 u = ld_stream(base + static_cast<int64_t>(r) * a.q_sn);
                 const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -204,12 +209,18 @@ __global__ void __launch_bounds__(kCertThreads) certify_norms_kernel(CertArgs a,
                     const float x0 = bf16_lo(w[e]), x1 = bf16_hi(w[e]);
                     ss = __fmaf_ru(x0, x0, ss);
                     ss = __fmaf_ru(x1, x1, ss);
+                    dot = fmaf(x0, kb[2 * e], dot);
+                    dot = fmaf(x1, kb[2 * e + 1], dot);
                     amax = abs_bits_max(w[e], amax);
                 }
             }
 #pragma unroll
-            for (int off = 1; off < VPR; off <<= 1) ss = __fadd_ru(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, off));
+            for (int off = 1; off < VPR; off <<= 1) {
+                ss = __fadd_ru(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, off));
+                dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
+            }
             mx = fmaxf(mx, ss);
+            if (a.mu && cv == 0 && r < r1) a.mu[static_cast<int64_t>(bh) * a.Nq + r] = a.scale_log2 * dot;
         }
         const uint32_t m = block_max_u32(__float_as_uint(mx), redu);
         const uint32_t am = block_max_u32(amax, redu);

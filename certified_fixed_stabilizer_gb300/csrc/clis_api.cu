@@ -62,7 +62,8 @@ clis_status_t clis_certify_workspace_size(const clis_shape_t *shape, size_t *byt
 
 clis_status_t clis_certify(const clis_shape_t *shape, const void *q, const void *k, const void *v,
                            float scale_log2, clis_fmt_t exp_fmt, clis_fmt_t acc_fmt, float *kbar,
-                           clis_head_cert_t *certs, void *workspace, size_t ws_bytes, clis_stream_t stream)
+                           clis_head_cert_t *certs, float *mu, void *workspace, size_t ws_bytes,
+                           clis_stream_t stream)
 {
     clis_status_t st = check_shape(shape, false);
     if (st != CLIS_OK) return st;
@@ -70,7 +71,8 @@ clis_status_t clis_certify(const clis_shape_t *shape, const void *q, const void 
     if ((!q && shape->Nq > 0) || !k || !v || !kbar || !certs) return CLIS_ERR_INVALID_ARG;
     if (!std::isfinite(scale_log2) || !(scale_log2 > 0.f)) return CLIS_ERR_INVALID_ARG;
     if (!valid_fmt(exp_fmt) || !valid_fmt(acc_fmt)) return CLIS_ERR_INVALID_ARG;
-    if ((q && !aligned16(q)) || !aligned16(k) || !aligned16(v) || !aligned16(kbar) || !aligned16(certs))
+    if ((q && !aligned16(q)) || !aligned16(k) || !aligned16(v) || !aligned16(kbar) || !aligned16(certs) ||
+        (mu && (reinterpret_cast<uintptr_t>(mu) & 3u)))
         return CLIS_ERR_MISALIGNED;
     size_t need = 0;
     clis_certify_workspace_size(shape, &need);
@@ -104,6 +106,7 @@ clis_status_t clis_certify(const clis_shape_t *shape, const void *q, const void 
     a.emax_acc = fmt_emax(acc_fmt);
     a.kbar = kbar;
     a.certs = certs;
+    a.mu = mu;
     if (BH * (2 * a.nck + a.ncq) > kMaxN) return CLIS_ERR_UNSUPPORTED;
     clis::CertWorkspace ws;
     clis::cert_workspace_layout(BH, a.nck, a.ncq, a.d, workspace, &ws);
@@ -112,8 +115,8 @@ clis_status_t clis_certify(const clis_shape_t *shape, const void *q, const void 
 }
 
 clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, const void *k, const void *v, void *o,
-                            float *lse2, const float *kbar, const clis_head_cert_t *certs, float scale_log2,
-                            int causal, clis_variant_t variant, clis_stream_t stream)
+                            float *lse2, const float *kbar, const clis_head_cert_t *certs, const float *mu,
+                            float scale_log2, int causal, clis_variant_t variant, clis_stream_t stream)
 {
     clis_status_t st = check_shape(shape, true);
     if (st != CLIS_OK) return st;
@@ -129,7 +132,7 @@ clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, const void
     if (causal && shape->Nq != shape->Nk) return CLIS_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return CLIS_ERR_MISALIGNED;
     if ((kbar && !aligned16(kbar)) || (certs && !aligned16(certs)) ||
-        (lse2 && (reinterpret_cast<uintptr_t>(lse2) & 3u)))
+        (lse2 && (reinterpret_cast<uintptr_t>(lse2) & 3u)) || (mu && (reinterpret_cast<uintptr_t>(mu) & 3u)))
         return CLIS_ERR_MISALIGNED;
 
     clis::AttnArgs a;
@@ -140,6 +143,7 @@ clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, const void
     a.lse2 = lse2;
     a.kbar = kbar;
     a.certs = certs;
+    a.mu = mu;
     a.q_sb = shape->q_sb;
     a.q_sh = shape->q_sh;
     a.q_sn = shape->q_sn;
@@ -167,7 +171,7 @@ clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, const void
 
 clis_status_t clis_certify_noalloc(const clis_shape_t *shape, const void *q, const void *k, const void *v,
                                    float scale_log2, clis_fmt_t exp_fmt, clis_fmt_t acc_fmt, float *kbar,
-                                   clis_head_cert_t *certs, clis_stream_t stream)
+                                   clis_head_cert_t *certs, float *mu, clis_stream_t stream)
 {
     size_t need = 0;
     const clis_status_t st = clis_certify_workspace_size(shape, &need);
@@ -175,14 +179,14 @@ clis_status_t clis_certify_noalloc(const clis_shape_t *shape, const void *q, con
     if (need > CLIS_NOALLOC_SCRATCH_BYTES) return CLIS_ERR_WORKSPACE;
     void *scratch = clis::certify_static_scratch();
     if (!scratch) return CLIS_ERR_CUDA;
-    return clis_certify(shape, q, k, v, scale_log2, exp_fmt, acc_fmt, kbar, certs, scratch,
+    return clis_certify(shape, q, k, v, scale_log2, exp_fmt, acc_fmt, kbar, certs, mu, scratch,
                         CLIS_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void *q, const void *k, const void *v,
                                   float *o_acc, float *l_acc, float *m_acc, const float *kbar,
-                                  const clis_head_cert_t *certs, float scale_log2, int first, clis_variant_t variant,
-                                  clis_stream_t stream)
+                                  const clis_head_cert_t *certs, const float *mu, float scale_log2, int first,
+                                  clis_variant_t variant, clis_stream_t stream)
 {
     clis_status_t st = check_shape(shape, false);
     if (st != CLIS_OK) return st;
@@ -197,7 +201,8 @@ clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void *q, cons
     if (variant == CLIS_AUTO && !certs) return CLIS_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_acc)) return CLIS_ERR_MISALIGNED;
     if ((kbar && !aligned16(kbar)) || (certs && !aligned16(certs)) ||
-        (reinterpret_cast<uintptr_t>(l_acc) & 3u) || (reinterpret_cast<uintptr_t>(m_acc) & 3u))
+        (reinterpret_cast<uintptr_t>(l_acc) & 3u) || (reinterpret_cast<uintptr_t>(m_acc) & 3u) ||
+        (mu && (reinterpret_cast<uintptr_t>(mu) & 3u)))
         return CLIS_ERR_MISALIGNED;
     const int64_t tiles = shape->B * shape->H * div_up(shape->Nq, 256);
     if (tiles > kMaxN) return CLIS_ERR_UNSUPPORTED;
@@ -210,6 +215,7 @@ clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void *q, cons
     a.lse2 = nullptr;
     a.kbar = kbar;
     a.certs = certs;
+    a.mu = mu;
     a.q_sb = shape->q_sb;
     a.q_sh = shape->q_sh;
     a.q_sn = shape->q_sn;

@@ -34,6 +34,7 @@ struct CertArgs {
     int emax_exp, emax_acc;  // floor(U) of the exp2-output and accumulator formats
     float *kbar;
     clis_head_cert_t *certs;
+    float *mu;  // optional per-row stabilisers [B*H*Nq]
 };
 
 // Carves the workspace for the given sizes; returns the bytes needed.
@@ -54,6 +55,7 @@ struct AttnArgs {
     float *lse2;
     const float *kbar;
     const clis_head_cert_t *certs;
+    const float *mu = nullptr;  // optional per-row stabilisers from clis_certify
     int64_t q_sb, q_sh, q_sn, k_sb, k_sh, k_sn, v_sb, v_sh, v_sn, o_sb, o_sh, o_sn;
     int B, H, Nq, Nk, d;
     float scale_log2;

@@ -124,13 +124,18 @@ CLIS_API clis_status_t clis_certify_workspace_size(const clis_shape_t *shape, si
  *   acc_fmt     accumulator format (U_acc); the kernel accumulates in FP32
  *   kbar        device fp32 out [B*H, d]: step 1 key mean, round-to-nearest
  *   certs       device out [B*H]
+ *   mu          optional device fp32 out [B*H*Nq] (index (b*H + h)*Nq + i):
+ *               the per-row stabilisers mu_i = scale_log2 * (q_i . kbar) that
+ *               the certified path fixes before the KV loop (Figure 5(a));
+ *               pass it to clis_attn_fwd so the kernel need not recompute
+ *               them.  NULL = skip.
  *   workspace   device scratch of at least clis_certify_workspace_size()
  *               bytes, 256-byte aligned; contents need no initialisation
  * Launches four kernels on `stream`.  Nk must be >= 1; Nq may be 0. */
 CLIS_API clis_status_t clis_certify(const clis_shape_t *shape, const void *q, const void *k,
                            const void *v, float scale_log2, clis_fmt_t exp_fmt,
                            clis_fmt_t acc_fmt, float *kbar, clis_head_cert_t *certs,
-                           void *workspace, size_t ws_bytes, clis_stream_t stream);
+                           float *mu, void *workspace, size_t ws_bytes, clis_stream_t stream);
 
 /* Size in bytes of the scratch buffer that clis_certify_noalloc uses instead
  * of a caller workspace (a fixed array inside the library). */
@@ -165,7 +170,7 @@ CLIS_API clis_status_t clis_certify(const clis_shape_t *shape, const void *q, co
 CLIS_API clis_status_t clis_certify_noalloc(const clis_shape_t *shape, const void *q, const void *k,
                                    const void *v, float scale_log2, clis_fmt_t exp_fmt,
                                    clis_fmt_t acc_fmt, float *kbar, clis_head_cert_t *certs,
-                                   clis_stream_t stream);
+                                   float *mu, clis_stream_t stream);
 
 /* Fused attention forward O = softmax(scale * Q K^T) V (paper: abstract and
  * Figure 5(a), "a loop-invariant stabilizer mu_i removes the reduction and
@@ -180,12 +185,14 @@ CLIS_API clis_status_t clis_certify_noalloc(const clis_shape_t *shape, const voi
  *           (b*H + h)*Nq + i): log2 sum_j exp2(scale_log2 * s_ij); NULL = skip
  *   kbar, certs  outputs of clis_certify (may be NULL for CLIS_ONLINE and
  *           CLIS_ONLINE_LAZY)
+ *   mu      optional per-row stabilisers from clis_certify (NULL: the kernel
+ *           computes mu_i from q_i and kbar itself)
  *   causal  0 or 1; 1 requires Nq == Nk (key j visible to query i iff j <= i)
  * Nq == 0 or B*H == 0 launches nothing and returns CLIS_OK. */
 CLIS_API clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, const void *k,
                             const void *v, void *o, float *lse2, const float *kbar,
-                            const clis_head_cert_t *certs, float scale_log2, int causal,
-                            clis_variant_t variant, clis_stream_t stream);
+                            const clis_head_cert_t *certs, const float *mu, float scale_log2,
+                            int causal, clis_variant_t variant, clis_stream_t stream);
 
 /* One KV chunk of a ring / context-parallel attention step (paper: Table 7,
  * the ring and 2D-ring columns, and Figure 6, one ring attention step).  The
@@ -199,15 +206,15 @@ CLIS_API clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, c
  * first = 1 overwrites the accumulators (first chunk), 0 merges.  A certified
  * head's shift is its fixed stabiliser mu_i in every chunk, so its partials
  * add with no exponentials and no rescaling; other heads merge by rescaling
- * to the larger maximum.  kbar and certs must come from clis_certify over the
- * whole key sequence (for a ring: the k-bar partials and norm maxima of all
+ * to the larger maximum.  kbar, certs (and mu, optional) must come from
+ * clis_certify over the whole key sequence (for a ring: the k-bar partials and norm maxima of all
  * chunks reduced before the first step).  Non-causal only; shape->o_* ignored.
  * Errors as clis_attn_fwd. */
 CLIS_API clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void *q, const void *k,
                                   const void *v, float *o_acc, float *l_acc, float *m_acc,
                                   const float *kbar, const clis_head_cert_t *certs,
-                                  float scale_log2, int first, clis_variant_t variant,
-                                  clis_stream_t stream);
+                                  const float *mu, float scale_log2, int first,
+                                  clis_variant_t variant, clis_stream_t stream);
 
 /* After the last chunk: o = o_acc / l_acc (bf16, strides shape->o_*) and, if
  * lse2 is not NULL, lse2 = m_acc + log2(l_acc). */

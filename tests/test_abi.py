@@ -67,7 +67,7 @@ def _certify(clis, shape, q=FAKE, k=FAKE, v=FAKE, scale=0.1, ef=1, af=2, kbar=FA
     lib = clis.load_library()
     vp = ctypes.c_void_p
     return lib.clis_certify(ctypes.byref(shape) if shape is not None else None, vp(q), vp(k), vp(v), scale,
-                            ef, af, vp(kbar), vp(certs), vp(ws), ws_bytes, None)
+                            ef, af, vp(kbar), vp(certs), None, vp(ws), ws_bytes, None)
 
 
 def _attn(clis, shape, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse2=None, kbar=FAKE, certs=FAKE, scale=0.1,
@@ -75,7 +75,7 @@ def _attn(clis, shape, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse2=None, kbar=FAKE, cer
     lib = clis.load_library()
     vp = ctypes.c_void_p
     return lib.clis_attn_fwd(ctypes.byref(shape) if shape is not None else None, vp(q), vp(k), vp(v), vp(o),
-                             vp(lse2), vp(kbar), vp(certs), scale, causal, variant, None)
+                             vp(lse2), vp(kbar), vp(certs), None, scale, causal, variant, None)
 
 
 def test_workspace_size_is_host_only_and_grows(clis):
@@ -117,6 +117,11 @@ def test_attn_rejects_bad_arguments(clis):
     assert _attn(clis, _shape(clis, d=256)) == UNSUP
     assert _attn(clis, _shape(clis), o=FAKE + 2) == MIS
     assert _attn(clis, _shape(clis), lse2=FAKE + 2) == MIS
+    lib = clis.load_library()
+    vp = ctypes.c_void_p
+    s = _shape(clis)
+    assert lib.clis_attn_fwd(ctypes.byref(s), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE), vp(FAKE),
+                             vp(FAKE + 2), 0.1, 0, 0, None) == MIS          # mu misaligned
     s = _shape(clis)
     s.o_sn = 129
     assert _attn(clis, s) == INV or _attn(clis, s) == MIS
@@ -131,7 +136,7 @@ def test_chunk_entry_points_reject_bad_arguments(clis):
     s = _shape(clis)
     call = lambda **kw: lib.clis_attn_fwd_chunk(ctypes.byref(s), vp(kw.get("q", FAKE)), vp(FAKE), vp(FAKE),
                                                 vp(kw.get("oa", FAKE)), vp(kw.get("la", FAKE)), vp(FAKE), vp(FAKE),
-                                                vp(FAKE), kw.get("scale", 0.1), kw.get("first", 0),
+                                                vp(FAKE), None, kw.get("scale", 0.1), kw.get("first", 0),
                                                 kw.get("variant", 0), None)
     assert call(oa=0) == 1
     assert call(first=3) == 1

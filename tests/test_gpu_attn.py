@@ -191,6 +191,22 @@ def test_lazy_rescale_with_growing_maxima():
             np.testing.assert_allclose(l2.cpu().numpy().reshape(rlse.shape), rlse, atol=2e-3, rtol=0)
 
 
+def test_stabilisers_from_certification_match_in_kernel_ones():
+    """clis_attn_fwd with mu from clis_certify vs the kernel computing mu itself."""
+    dev = need_gpu()
+    w = WORKLOADS["causal"]
+    q, k, v = make_inputs(w, device=dev, N=2000, H=4)
+    sl2 = clis.scale_log2_for(w.d)
+    mu = torch.empty(q.shape[0] * q.shape[1] * q.shape[2], device=dev)
+    kbar, certs = clis.clis_certify(q, k, v, sl2, mu=mu)
+    a = clis.clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=True, mu=mu)
+    b = clis.clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=True)
+    torch.cuda.synchronize()
+    assert_paths_agree(flat(a), flat(b), "mu from certify")
+    ref, _ = _oracle(q, k, v, True)
+    assert_close_to_oracle(flat(a).float().cpu().numpy(), ref, "mu from certify vs oracle")
+
+
 def test_outputs_are_deterministic():
     dev = need_gpu()
     w = WORKLOADS["mixed"]

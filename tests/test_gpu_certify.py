@@ -188,3 +188,23 @@ def test_deterministic():
     b = clis.clis_certify(q, k, v, sl2)
     torch.cuda.synchronize()
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixed"])
+def test_per_row_stabilisers(name):
+    """mu_i = scale_log2 * (q_i . kbar) from the certification pass, against the
+    same formula in fp64 with the oracle's kbar (|error| well below one exp2
+    unit: mu is a shift, any fixed value is exact in real arithmetic)."""
+    dev = need_gpu()
+    w = WORKLOADS[name]
+    q, k, v = make_inputs(w, device=dev, N=3000 if name == "mixed" else None)
+    sl2 = clis.scale_log2_for(w.d)
+    mu = torch.full((q.shape[0] * q.shape[1] * q.shape[2],), float("nan"), device=dev)
+    clis.clis_certify(q, k, v, sl2, mu=mu)
+    torch.cuda.synchronize()
+    okbar, _ = oracle.certify(q, k, v, sl2)
+    qf = oracle.bf16_bits_to_f64(oracle.as_bf16_bits(q)).reshape(okbar.shape[0], -1, w.d)
+    ref = sl2 * np.einsum("hnd,hd->hn", qf, okbar)
+    got = mu.cpu().double().numpy().reshape(ref.shape)
+    scale = sl2 * np.linalg.norm(qf, axis=2) * np.linalg.norm(okbar, axis=1)[:, None]
+    assert np.all(np.abs(got - ref) <= 1e-5 * scale + 1e-6)
