@@ -19,7 +19,8 @@
 //
 //   warps 0-3   softmax for query tile 0 (rows 0-127 of the work tile)
 //   warps 4-7   softmax for query tile 1 (rows 128-255)
-//   warps 8-11  correction: rescales O in TMEM (online tiles only)
+//   warps 8-11  correction: rescales O in TMEM (online tiles) and writes the
+//               output of every finished tile (so softmax moves on at once)
 //   warp 12     TMA producer: Q tiles once per work tile, K and V tiles
 //               through an NSTAGE-deep shared-memory ring
 //   warp 13     MMA issuer: S = Q K^T (SMEM x SMEM -> TMEM) and
@@ -62,7 +63,7 @@ constexpr unsigned kErrDrain = 1u << 4;
 
 template <int D>
 struct Cfg {
-    static constexpr int NSTAGE = (D == 128) ? 5 : 8;
+    static constexpr int NSTAGE = (D == 128) ? 4 : 8;
     static constexpr int NBOX = D / 64;                 // 64-column (128-byte) TMA boxes per tile
     static constexpr int BOX_BYTES = 128 * 128;         // 128 rows x 128 bytes
     static constexpr int TILE_BYTES = NBOX * BOX_BYTES; // one Q, K or V tile
@@ -100,8 +101,10 @@ struct __align__(8) Ctl {
     uint64_t kv_full[kNStageMax], kv_empty[kNStageMax];
     uint64_t s_full[2], p_full[2], pv_done[2];
     uint64_t alpha_full[2], o_ready[2], o_free[2];
+    uint64_t epi_full[2];  // softmax -> correction: row sums and shifts of a finished tile
     uint64_t drain;
     float alpha[2][BM];
+    float epi_l[2][BM], epi_shift[2][BM];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -194,6 +197,17 @@ __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, 
             __syncwarp();
         }
         q_issued = w;
+        // Warm L2 with the next work tile's Q while this tile runs: its load
+        // then does not stall the start of that tile (matters for short causal tiles).
+        if (leader && tile + static_cast<int>(gridDim.x) < p.num_tiles) {
+            const Tile N = decode_tile<CAUSAL>(p, tile + gridDim.x);
+#pragma unroll
+            for (int t = 0; t < 2; t++)
+#pragma unroll
+                for (int bx = 0; bx < C::NBOX; bx++)
+                    tma_prefetch_l2_4d(tm_q, bx * 64, N.qb * 2 * BM + t * BM, N.h, N.b);
+        }
+        __syncwarp();
         for (int j = 0; j < T.n_kv; j++) {
 #pragma unroll
             for (int kv = 0; kv < 2; kv++) {
@@ -500,85 +514,100 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
             ++g;
         }
 
-        // Epilogue: O / l -> bf16, written straight from registers.
-        if (!mbar_wait(smem_u32(&c.pv_done[t]), (g - 1) & 1, ab, err, kErrSoftmax)) goto abort;
-        tc_fence_after();
-        if (p.chunk_mode) {
-            // KV-chunk merge.  The accumulator of row i holds sum_j 2^(x_ij - m_i) v_j and
-            // sum_j 2^(x_ij - m_i) over the chunks merged so far, x = scale_log2 * s.  A
-            // certified head uses the same shift mu_i in every chunk, so its partials add
-            // with no exponentials; an online head rescales to the larger maximum.
-            const float m_c = T.cert ? mu : ((m_run == -INFINITY) ? 0.f : m_run);
-            const int64_t ridx = static_cast<int64_t>(T.bh) * p.Nq + row;
-            float a_old = 0.f, a_new = 1.f;
-            if (row_ok && p.chunk_mode == 1) {
-                const float m_old = p.m_acc[ridx];
-                if (m_old == m_c) {
-                    a_old = 1.f;
-                } else {
-                    const float m_new = fmaxf(m_old, m_c);
-                    a_old = ex2_approx(m_old - m_new);
-                    a_new = ex2_approx(m_c - m_new);
-                    p.m_acc[ridx] = m_new;
-                }
-            } else if (row_ok) {
-                p.m_acc[ridx] = m_c;
-            }
-            float4 *oa = reinterpret_cast<float4 *>(p.o_acc + ridx * D);
-#pragma unroll 1
-            for (int c32 = 0; c32 < D / 32; c32++) {
-                uint32_t r[32];
-                tmem_ld32(tO + c32 * 32, r);
-                tmem_wait_ld();
-                if (row_ok) {
-#pragma unroll
-                    for (int e = 0; e < 8; e++) {
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (p.chunk_mode == 1) acc = oa[c32 * 8 + e];
-                        acc.x = fmaf(a_new, __uint_as_float(r[4 * e + 0]), a_old * acc.x);
-                        acc.y = fmaf(a_new, __uint_as_float(r[4 * e + 1]), a_old * acc.y);
-                        acc.z = fmaf(a_new, __uint_as_float(r[4 * e + 2]), a_old * acc.z);
-                        acc.w = fmaf(a_new, __uint_as_float(r[4 * e + 3]), a_old * acc.w);
-                        oa[c32 * 8 + e] = acc;
-                    }
-                }
-            }
-            if (row_ok) {
-                const float l_old = (p.chunk_mode == 1) ? p.l_acc[ridx] : 0.f;
-                p.l_acc[ridx] = fmaf(a_new, l_run, a_old * l_old);
-            }
-        } else {
-            const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-            uint16_t *orow = p.o + T.b * p.o_sb + T.h * p.o_sh + static_cast<int64_t>(row) * p.o_sn;
-#pragma unroll
-            for (int c32 = 0; c32 < D / 32; c32++) {
-                uint32_t r[32];
-                tmem_ld32(tO + c32 * 32, r);
-                tmem_wait_ld();
-                if (row_ok) {
-                    uint32_t pk[16];
-                    const float2 inv2 = make_float2(inv, inv);
-#pragma unroll
-                    for (int e = 0; e < 16; e++) {
-                        const float2 o2 =
-                            fmul2(make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), inv2);
-                        pk[e] = pack_bf16x2(o2.x, o2.y);
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c32 * 32);
-#pragma unroll
-                    for (int e = 0; e < 4; e++) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-                }
-            }
-            if (p.lse2 && row_ok) {
-                const float base = T.cert ? mu : ((m_run == -INFINITY) ? 0.f : m_run);
-                p.lse2[static_cast<int64_t>(T.bh) * p.Nq + row] = base + log2f(l_run);
-            }
-        }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&c.o_free[t]));
+        // Hand the row's sum and shift to the correction warpgroup, which writes
+        // the output (the next work tile starts here without waiting for it).
+        // The previous tile's output must be written first: with a single KV
+        // step a tile never waits on o_free, so without this the group could
+        // publish two tiles ahead of the correction warpgroup.
+        if (w > 0 && !mbar_wait(smem_u32(&c.o_free[t]), (w - 1) & 1, ab, err, kErrSoftmax)) goto abort;
+        c.epi_l[t][rl] = l_run;
+        c.epi_shift[t][rl] = T.cert ? mu : ((m_run == -INFINITY) ? 0.f : m_run);
+        mbar_arrive(smem_u32(&c.epi_full[t]));
     }
 abort:
     return;
+}
+
+// ------------------------------------------------------------------ epilogue
+//
+// Output of one row of a finished work tile, run by the correction warpgroup
+// (thread = TMEM lane = row): O / l -> bf16 (or, in KV-chunk mode, the merge
+// into the fp32 accumulators) and lse2.  `shift` is the row's stabiliser:
+// mu_i on the certified path, the (possibly stale) row maximum online.
+template <int D>
+__device__ __forceinline__ void write_row(const Params &p, const Tile &T, uint32_t tO, int row, bool row_ok,
+                                          float l_run, float shift)
+{
+    if (p.chunk_mode) {
+        // KV-chunk merge.  The accumulator of row i holds sum_j 2^(x_ij - m_i) v_j and
+        // sum_j 2^(x_ij - m_i) over the chunks merged so far, x = scale_log2 * s.  A
+        // certified head uses the same shift mu_i in every chunk, so its partials add
+        // with no exponentials; an online head rescales to the larger maximum.
+        const float m_c = shift;
+        const int64_t ridx = static_cast<int64_t>(T.bh) * p.Nq + row;
+        float a_old = 0.f, a_new = 1.f;
+        if (row_ok && p.chunk_mode == 1) {
+            const float m_old = p.m_acc[ridx];
+            if (m_old == m_c) {
+                a_old = 1.f;
+            } else {
+                const float m_new = fmaxf(m_old, m_c);
+                a_old = ex2_approx(m_old - m_new);
+                a_new = ex2_approx(m_c - m_new);
+                p.m_acc[ridx] = m_new;
+            }
+        } else if (row_ok) {
+            p.m_acc[ridx] = m_c;
+        }
+        float4 *oa = reinterpret_cast<float4 *>(p.o_acc + ridx * D);
+#pragma unroll 1
+        for (int c32 = 0; c32 < D / 32; c32++) {
+            uint32_t r[32];
+            tmem_ld32(tO + c32 * 32, r);
+            tmem_wait_ld();
+            if (row_ok) {
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (p.chunk_mode == 1) acc = oa[c32 * 8 + e];
+                    acc.x = fmaf(a_new, __uint_as_float(r[4 * e + 0]), a_old * acc.x);
+                    acc.y = fmaf(a_new, __uint_as_float(r[4 * e + 1]), a_old * acc.y);
+                    acc.z = fmaf(a_new, __uint_as_float(r[4 * e + 2]), a_old * acc.z);
+                    acc.w = fmaf(a_new, __uint_as_float(r[4 * e + 3]), a_old * acc.w);
+                    oa[c32 * 8 + e] = acc;
+                }
+            }
+        }
+        if (row_ok) {
+            const float l_old = (p.chunk_mode == 1) ? p.l_acc[ridx] : 0.f;
+            p.l_acc[ridx] = fmaf(a_new, l_run, a_old * l_old);
+        }
+    } else {
+        const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+        uint16_t *orow = p.o + T.b * p.o_sb + T.h * p.o_sh + static_cast<int64_t>(row) * p.o_sn;
+#pragma unroll
+        for (int c32 = 0; c32 < D / 32; c32++) {
+            uint32_t r[32];
+            tmem_ld32(tO + c32 * 32, r);
+            tmem_wait_ld();
+            if (row_ok) {
+                uint32_t pk[16];
+                const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    const float2 o2 =
+                        fmul2(make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), inv2);
+                    pk[e] = pack_bf16x2(o2.x, o2.y);
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + c32 * 32);
+#pragma unroll
+                for (int e = 0; e < 4; e++) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            }
+        }
+        if (p.lse2 && row_ok) {
+            p.lse2[static_cast<int64_t>(T.bh) * p.Nq + row] = shift + log2f(l_run);
+        }
+    }
 }
 
 // ---------------------------------------------------------------- correction
@@ -593,12 +622,12 @@ __device__ void correction_role(const Params &p, Ctl &c, uint32_t tmem, int warp
     const int rl = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t g = 0, ncorr = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    int w = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
         const Tile T = decode_tile<CAUSAL>(p, tile);
         if (T.cert || T.lazy) {
             g += T.n_kv;
-            continue;
-        }
+        } else {
         for (int j = 0; j < T.n_kv; j++) {
             if (j > 0) {
                 for (int t = 0; t < 2; t++) {
@@ -629,6 +658,18 @@ __device__ void correction_role(const Params &p, Ctl &c, uint32_t tmem, int warp
             }
             ++g;
         }
+        }
+        // Epilogue of both query tiles, once their last O += P V has completed.
+        for (int t = 0; t < 2; t++) {
+            if (!mbar_wait(smem_u32(&c.epi_full[t]), w & 1, ab, err, kErrCorrection)) return;
+            if (!mbar_wait(smem_u32(&c.pv_done[t]), (g - 1) & 1, ab, err, kErrCorrection)) return;
+            tc_fence_after();
+            const int row = T.qb * 2 * BM + t * BM + rl;
+            write_row<D>(p, T, tmem + (t ? C::TM_O1 : C::TM_O0) + lane_off, row, row < p.Nq, c.epi_l[t][rl],
+                         c.epi_shift[t][rl]);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&c.o_free[t]));
+        }
     }
 }
 
@@ -658,6 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&ctl.alpha_full[t]), BM);
             mbar_init(smem_u32(&ctl.o_ready[t]), BM);
             mbar_init(smem_u32(&ctl.o_free[t]), BM);
+            mbar_init(smem_u32(&ctl.epi_full[t]), BM);
         }
         for (int s = 0; s < C::NSTAGE; s++) {
             mbar_init(smem_u32(&ctl.kv_full[s]), 1);

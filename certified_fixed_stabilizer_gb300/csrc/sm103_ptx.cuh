@@ -132,6 +132,15 @@ __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// Bring a 4-D tile into L2 ahead of its use (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const void *tmap, int c0, int c1, int c2, int c3)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_last()
 {
     uint64_t p;

@@ -25,7 +25,15 @@ def _setup():
     oracle.set_num_threads(os.cpu_count() or 1)
     clis.clis_clear_device_error()
     yield
-    assert clis.clis_get_device_error() == 0
+
+
+@pytest.fixture(autouse=True)
+def _device_error_word_stays_clear():
+    """Every test must leave the kernels' error word at 0 (no wait ran out)."""
+    yield
+    code = clis.clis_get_device_error()
+    clis.clis_clear_device_error()
+    assert code == 0, f"device error word {code:#x}"
 
 
 def _run(q, k, v, causal, variant, lse2=False, softmax_scale=None):
@@ -97,6 +105,8 @@ CASES = [
     (1, 3, 513, 513, 64, False),
     (1, 1, 2000, 2000, 128, True),
     (3, 1, 300, 4097, 64, False),
+    (1, 4, 20000, 100, 128, False),   # one KV step per work tile, several tiles per CTA
+    (2, 3, 9000, 1, 64, False),       # a single key
 ]
 
 

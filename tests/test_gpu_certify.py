@@ -26,7 +26,15 @@ def _setup():
     oracle.set_num_threads(os.cpu_count() or 1)
     clis.clis_clear_device_error()
     yield
-    assert clis.clis_get_device_error() == 0
+
+
+@pytest.fixture(autouse=True)
+def _device_error_word_stays_clear():
+    """Every test must leave the kernels' error word at 0 (no wait ran out)."""
+    yield
+    code = clis.clis_get_device_error()
+    clis.clis_clear_device_error()
+    assert code == 0, f"device error word {code:#x}"
 
 
 def _compare(q, k, v, sl2, exp_fmt="bf16", acc_fmt="fp32", expect_no_band=True):
