@@ -113,6 +113,7 @@ struct Tile {
     int bh, b, h, qb, n_kv;
     bool cert;  // fixed stabiliser, no rescale
     bool lazy;  // online, rescale only when the row maximum grows by more than kLazyTau
+    bool rev;   // sweep the KV tiles last to first
 };
 
 // Work-tile order.  Non-causal: head-major, query blocks ascending (every
@@ -144,6 +145,10 @@ __device__ __forceinline__ Tile decode_tile(const Params &p, int tile)
     }
     t.b = t.bh / p.H;
     t.h = t.bh % p.H;
+    // Odd rounds of the persistent grid sweep K/V backwards: they start with
+    // the keys the previous round touched last, which are still in L2
+    // (softmax does not depend on the key order).
+    t.rev = ((tile / static_cast<int>(gridDim.x)) & 1) != 0;
     t.lazy = p.variant == CLIS_ONLINE_LAZY;
     if (p.variant == CLIS_ONLINE || p.variant == CLIS_ONLINE_LAZY) t.cert = false;
     else if (p.variant == CLIS_CERTIFIED_FORCED) t.cert = true;
@@ -197,17 +202,6 @@ __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, 
             __syncwarp();
         }
         q_issued = w;
-        // Warm L2 with the next work tile's Q while this tile runs: its load
-        // then does not stall the start of that tile (matters for short causal tiles).
-        if (leader && tile + static_cast<int>(gridDim.x) < p.num_tiles) {
-            const Tile N = decode_tile<CAUSAL>(p, tile + gridDim.x);
-#pragma unroll
-            for (int t = 0; t < 2; t++)
-#pragma unroll
-                for (int bx = 0; bx < C::NBOX; bx++)
-                    tma_prefetch_l2_4d(tm_q, bx * 64, N.qb * 2 * BM + t * BM, N.h, N.b);
-        }
-        __syncwarp();
         for (int j = 0; j < T.n_kv; j++) {
 #pragma unroll
             for (int kv = 0; kv < 2; kv++) {
@@ -221,7 +215,7 @@ __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, 
 #pragma unroll
                     for (int bx = 0; bx < C::NBOX; bx++)
                         tma_load_4d_hint(sKV + stage * C::TILE_BYTES + bx * C::BOX_BYTES, tm, bar, bx * 64,
-                                         j * BN, T.h, T.b, pol_kv);
+                                         (T.rev ? T.n_kv - 1 - j : j) * BN, T.h, T.b, pol_kv);
                 }
                 __syncwarp();
                 ++it;
@@ -418,7 +412,7 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
             tmem_wait_ld();
 
             // Mask keys past Nk (ragged last tile) and, if causal, keys after the row.
-            const int key0 = j * BN;
+            const int key0 = (T.rev ? T.n_kv - 1 - j : j) * BN;
             const int lim = CAUSAL ? min(p.Nk, row + 1) : p.Nk;  // keys [0, lim) are visible
             if (key0 + BN > lim) {
 #pragma unroll
