@@ -78,9 +78,9 @@ def _load():
             return _lib
         lib = ctypes.CDLL(build())
         i64, i32, dbl, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
-        lib.oracle_certify.argtypes = [i64, i64, i64, i64, vp, vp, vp, dbl, i32, i32, vp, vp]
+        lib.oracle_certify.argtypes = [i64, i64, i64, i64, vp, vp, vp, i32, dbl, i32, i32, vp, vp]
         lib.oracle_certify.restype = i32
-        for name in ("oracle_attn_bf16", "oracle_attn_f64"):
+        for name in ("oracle_attn_bf16", "oracle_attn_fp16", "oracle_attn_f64"):
             f = getattr(lib, name)
             f.argtypes = [i64, i64, i64, i64, vp, vp, vp, dbl, i32, i64, vp, vp, vp]
             f.restype = i32
@@ -92,6 +92,8 @@ def _load():
         lib.oracle_v_exponent.restype = ctypes.c_int32
         lib.oracle_exponent_budget.argtypes = [i32, i32, ctypes.c_int32]
         lib.oracle_exponent_budget.restype = ctypes.c_int32
+        lib.oracle_decode.argtypes = [ctypes.c_uint16, i32]
+        lib.oracle_decode.restype = dbl
         lib.oracle_num_threads.restype = i32
         lib.oracle_set_num_threads.argtypes = [i32]
         _lib = lib
@@ -102,16 +104,36 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
+IN_FMT = {"bf16": 0, "fp16": 1}
+
+
+def as_bits(x):
+    """bf16 / fp16 torch tensor (any device), numpy float16 array or uint16 bf16
+    bit array -> (contiguous uint16 numpy bits, input format name)."""
+    if isinstance(x, np.ndarray):
+        if x.dtype == np.float16:
+            return np.ascontiguousarray(x).view(np.uint16), "fp16"
+        if x.dtype != np.uint16:
+            raise TypeError("expected bf16 bit patterns as uint16 or a float16 array")
+        return np.ascontiguousarray(x), "bf16"
+    import torch
+    if x.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("expected a bfloat16 or float16 tensor")
+    fmt = "bf16" if x.dtype == torch.bfloat16 else "fp16"
+    return x.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16), fmt
+
+
 def as_bf16_bits(x) -> np.ndarray:
     """bf16 torch tensor (any device) or uint16 array -> contiguous uint16 numpy bits."""
-    if isinstance(x, np.ndarray):
-        if x.dtype != np.uint16:
-            raise TypeError("expected bf16 bit patterns as uint16")
-        return np.ascontiguousarray(x)
-    import torch
-    if x.dtype != torch.bfloat16:
-        raise TypeError("expected a bfloat16 tensor")
-    return x.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
+    bits, fmt = as_bits(x)
+    if fmt != "bf16":
+        raise TypeError("expected bf16 data")
+    return bits
+
+
+def decode(bits: int, fmt: str) -> float:
+    """One bf16 / fp16 bit pattern -> its exact value (as the oracle reads it)."""
+    return _load().oracle_decode(int(bits), IN_FMT[fmt])
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
@@ -150,17 +172,19 @@ def exponent_budget(exp_fmt: str, acc_fmt: str, A: int) -> int:
 def certify(q, k, v, scale_log2: float, exp_fmt: str = "bf16", acc_fmt: str = "fp32"):
     """Algorithm 1 for every head.
 
-    q: [BH, Nq, d], k, v: [BH, Nk, d] (bf16 tensors or uint16 bit arrays; a
-    leading [B, H] pair is flattened).  Returns (kbar [BH, d] float64,
+    q: [BH, Nq, d], k, v: [BH, Nk, d] (bf16 or fp16 tensors, or uint16 bf16 bit
+    arrays; a leading [B, H] pair is flattened).  Returns (kbar [BH, d] float64,
     list of dicts with certified, G, A, C, reason, band, B_h, kappa, qmax, vmax).
     """
-    qb, kb, vb = (as_bf16_bits(t) for t in (q, k, v))
+    (qb, fq), (kb, fk), (vb, fv) = (as_bits(t) for t in (q, k, v))
+    if not fq == fk == fv:
+        raise TypeError("q, k, v must share one format")
     qb, kb, vb = (_heads_first(a) for a in (qb, kb, vb))
     d = qb.shape[-1]
     BH, Nq, Nk = qb.shape[0], qb.shape[1], kb.shape[1]
     kbar = np.zeros((BH, d), dtype=np.float64)
     certs = (OracleCert * max(BH, 1))()
-    rc = _load().oracle_certify(BH, Nq, Nk, d, _ptr(qb), _ptr(kb), _ptr(vb),
+    rc = _load().oracle_certify(BH, Nq, Nk, d, _ptr(qb), _ptr(kb), _ptr(vb), IN_FMT[fq],
                                 float(scale_log2), FMT[exp_fmt], FMT[acc_fmt],
                                 _ptr(kbar), ctypes.cast(certs, ctypes.c_void_p))
     if rc != 0:
@@ -176,8 +200,8 @@ def attention(q, k, v, scale: float, causal: bool = False, rows=None,
               with_lse2: bool = False):
     """fp64 softmax attention (two passes per row).
 
-    q: [BH, Nq, d], k, v: [BH, Nk, d] as bf16 tensors / uint16 bits, or
-    float64 arrays (then the inputs are used as given).  ``scale`` multiplies
+    q: [BH, Nq, d], k, v: [BH, Nk, d] as bf16 / fp16 tensors, uint16 bf16 bits,
+    or float64 arrays (then the inputs are used as given).  ``scale`` multiplies
     q.k inside exp (natural base).  ``rows``: query indices to evaluate (the
     same for every head) or None for all.  Returns out [BH, n_rows, d] and,
     if requested, lse2 [BH, n_rows] = log2 sum_j exp(scale q_i.k_j).
@@ -187,8 +211,10 @@ def attention(q, k, v, scale: float, causal: bool = False, rows=None,
         qa, ka, va = (np.ascontiguousarray(t, dtype=np.float64) for t in (q, k, v))
         fn = _load().oracle_attn_f64
     else:
-        qa, ka, va = (as_bf16_bits(t) for t in (q, k, v))
-        fn = _load().oracle_attn_bf16
+        (qa, fq), (ka, fk), (va, fv) = (as_bits(t) for t in (q, k, v))
+        if not fq == fk == fv:
+            raise TypeError("q, k, v must share one format")
+        fn = _load().oracle_attn_fp16 if fq == "fp16" else _load().oracle_attn_bf16
     qa, ka, va = (_heads_first(a) for a in (qa, ka, va))
     d = qa.shape[-1]
     BH, Nq, Nk = qa.shape[0], qa.shape[1], ka.shape[1]

@@ -9,8 +9,9 @@
  * Stabilization" (Tsai et al., 2026), Algorithm 1, and from the plain
  * definition of softmax attention.
  *
- * Precision: everything is fp64.  Inputs are bf16 bit patterns (uint16) or,
- * for the identity tests, fp64 arrays.  Layout is contiguous [BH][N][d].
+ * Precision: everything is fp64.  Inputs are bf16 or IEEE binary16 (fp16) bit
+ * patterns (uint16) or, for the identity tests, fp64 arrays.  Layout is
+ * contiguous [BH][N][d].
  *
  * Two routines:
  *
@@ -73,6 +74,29 @@ static double bf16_bits_to_double(uint16_t b)
     return (double)f;
 }
 
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double fp16_bits_to_double(uint16_t b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 10) & 0x1F;
+    int f = b & 0x3FF;
+    double v;
+    if (e == 0) v = ldexp((double)f, -24);                  /* zero and subnormals: f * 2^-24 */
+    else if (e == 31) v = f ? NAN : INFINITY;
+    else v = ldexp(1.0 + (double)f / 1024.0, e - 15);
+    return sign ? -v : v;
+}
+
+/* Input element formats of this file. */
+enum { ORC_IN_BF16 = 0, ORC_IN_FP16 = 1 };
+
+static double bits_to_double(uint16_t b, int in_fmt)
+{
+    return in_fmt == ORC_IN_FP16 ? fp16_bits_to_double(b) : bf16_bits_to_double(b);
+}
+
+double oracle_decode(uint16_t bits, int in_fmt) { return bits_to_double(bits, in_fmt); }
+
 /* Largest finite value of a binary floating-point format with p significand
  * bits (implicit bit included) and maximum exponent emax: (2 - 2^(1-p)) 2^emax. */
 static double format_max_finite(int fmt)
@@ -118,12 +142,14 @@ int32_t oracle_exponent_budget(int exp_fmt, int acc_fmt, int32_t A)
 }
 
 /* Algorithm 1, steps 1-7, plus the decision, for BH heads.
- * q: [BH][Nq][d], k, v: [BH][Nk][d] bf16 bits.  kbar_out: [BH][d] (may be NULL). */
+ * q: [BH][Nq][d], k, v: [BH][Nk][d] bit patterns in format in_fmt.
+ * kbar_out: [BH][d] (may be NULL). */
 int oracle_certify(int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
-                   const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                   const uint16_t *q, const uint16_t *k, const uint16_t *v, int in_fmt,
                    double scale_log2, int exp_fmt, int acc_fmt,
                    double *kbar_out, oracle_cert_t *out)
 {
+    if (in_fmt != ORC_IN_BF16 && in_fmt != ORC_IN_FP16) return 1;
     if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || !out) return 1;
     if (!isfinite(format_max_finite(exp_fmt)) || !isfinite(format_max_finite(acc_fmt))) return 1;
 
@@ -139,7 +165,7 @@ int oracle_certify(int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
         for (int64_t c = 0; c < d; c++) kbar[c] = 0.0;
         for (int64_t r = 0; r < Nk; r++)
             for (int64_t c = 0; c < d; c++) {
-                double x = bf16_bits_to_double(kh[r * d + c]);
+                double x = bits_to_double(kh[r * d + c], in_fmt);
                 if (!isfinite(x)) finite = 0;
                 kbar[c] += x;
             }
@@ -150,7 +176,7 @@ int oracle_certify(int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
         for (int64_t r = 0; r < Nk; r++) {
             double ss = 0.0;
             for (int64_t c = 0; c < d; c++) {
-                double t = bf16_bits_to_double(kh[r * d + c]) - kbar[c];
+                double t = bits_to_double(kh[r * d + c], in_fmt) - kbar[c];
                 ss += t * t;
             }
             double nrm = sqrt(ss);
@@ -162,7 +188,7 @@ int oracle_certify(int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
         for (int64_t r = 0; r < Nq; r++) {
             double ss = 0.0;
             for (int64_t c = 0; c < d; c++) {
-                double x = bf16_bits_to_double(qh[r * d + c]);
+                double x = bits_to_double(qh[r * d + c], in_fmt);
                 if (!isfinite(x)) finite = 0;
                 ss += x * x;
             }
@@ -175,7 +201,7 @@ int oracle_certify(int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
         double m = 0.0;
         for (int64_t r = 0; r < Nk; r++)
             for (int64_t c = 0; c < d; c++) {
-                double x = bf16_bits_to_double(vh[r * d + c]);
+                double x = bits_to_double(vh[r * d + c], in_fmt);
                 if (!isfinite(x)) finite = 0;
                 else if (fabs(x) > m) m = fabs(x);
             }
@@ -236,7 +262,8 @@ static void attn_row(const double *qi, const double *kh, const double *vh,
     if (lse2) *lse2 = (m + log(l)) / log(2.0);
 }
 
-/* Shared driver: el = 0 -> inputs are bf16 bits, el = 1 -> inputs are fp64.
+/* Shared driver: el = 0 -> inputs are bf16 bits, el = 1 -> inputs are fp64,
+ * el = 2 -> inputs are fp16 bits.
  * rows: n_rows query indices (same for every head), or NULL for all rows.
  * out: [BH][n_rows][d]; lse2 (may be NULL): [BH][n_rows] = log2 sum_j exp(s_ij). */
 static int attn_driver(int el, int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
@@ -256,9 +283,10 @@ static int attn_driver(int el, int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
 
     for (int64_t h = 0; h < BH; h++) {
         for (int64_t e = 0; e < Nk * d; e++) {
-            if (el == 0) {
-                kh[e] = bf16_bits_to_double(((const uint16_t *)k)[h * Nk * d + e]);
-                vh[e] = bf16_bits_to_double(((const uint16_t *)v)[h * Nk * d + e]);
+            if (el != 1) {
+                const int f = el == 2 ? ORC_IN_FP16 : ORC_IN_BF16;
+                kh[e] = bits_to_double(((const uint16_t *)k)[h * Nk * d + e], f);
+                vh[e] = bits_to_double(((const uint16_t *)v)[h * Nk * d + e], f);
             } else {
                 kh[e] = ((const double *)k)[h * Nk * d + e];
                 vh[e] = ((const double *)v)[h * Nk * d + e];
@@ -273,8 +301,9 @@ static int attn_driver(int el, int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
                 int64_t i = rows ? rows[t] : t;
                 for (int64_t c = 0; c < d; c++) {
                     int64_t e = (h * Nq + i) * d + c;
-                    qi[c] = (el == 0) ? bf16_bits_to_double(((const uint16_t *)q)[e])
-                                      : ((const double *)q)[e];
+                    qi[c] = (el == 1) ? ((const double *)q)[e]
+                                      : bits_to_double(((const uint16_t *)q)[e],
+                                                       el == 2 ? ORC_IN_FP16 : ORC_IN_BF16);
                 }
                 int64_t jmax = causal ? i : Nk - 1;
                 attn_row(qi, kh, vh, jmax, d, scale, s, out + (h * n_rows + t) * d,
@@ -295,6 +324,14 @@ int oracle_attn_bf16(int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
                      double *out, double *lse2)
 {
     return attn_driver(0, BH, Nq, Nk, d, q, k, v, scale, causal, n_rows, rows, out, lse2);
+}
+
+int oracle_attn_fp16(int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
+                     const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     double scale, int causal, int64_t n_rows, const int64_t *rows,
+                     double *out, double *lse2)
+{
+    return attn_driver(2, BH, Nq, Nk, d, q, k, v, scale, causal, n_rows, rows, out, lse2);
 }
 
 int oracle_attn_f64(int64_t BH, int64_t Nq, int64_t Nk, int64_t d,

@@ -356,3 +356,46 @@ def test_rejects_bad_arguments(oracle_mod):
         oracle_mod.attention(q, k, k, 1.0, causal=True)     # causal needs Nq == Nk
     with pytest.raises(ValueError):
         oracle_mod.attention(q, k, k, 1.0, rows=[3])        # row out of range
+
+
+# ---------------------------------------------------------- input formats ----
+
+def test_decode_every_fp16_and_bf16_pattern(oracle_mod):
+    """The oracle's reading of all 65,536 bit patterns of each input format
+    equals numpy's float16 and torch's bfloat16 conversions (NaN patterns
+    decode to NaN)."""
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    ref16 = bits.view(np.float16).astype(np.float64)
+    refb = torch.from_numpy(bits.astype(np.int16)).view(torch.bfloat16).double().numpy()
+    got16 = np.array([oracle_mod.decode(int(b), "fp16") for b in bits])
+    gotb = np.array([oracle_mod.decode(int(b), "bf16") for b in bits])
+    for got, ref in ((got16, ref16), (gotb, refb)):
+        nan = np.isnan(ref)
+        assert np.array_equal(np.isnan(got), nan)
+        assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_fp16_inputs_match_brute_force_and_certify(oracle_mod):
+    rng = np.random.default_rng(12)
+    q = rng.normal(size=(2, 5, 6)).astype(np.float16)
+    k = (rng.normal(size=(2, 7, 6)) * 3 + 1).astype(np.float16)
+    v = rng.normal(size=(2, 7, 6)).astype(np.float16)
+    out = oracle_mod.attention(q, k, v, 0.6)
+    ref, _ = _brute(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64), 0.6, False)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    # FP16 exp2 outputs: C = min(15, 127 - A); a head with B_h between 15 and 125 fails
+    d = 8
+    keys = _pm_keys(d, 1.0)
+    q0 = np.zeros((1, d), dtype=np.float32)
+    q0[0, 0] = 20.0
+    kb, certs = oracle_mod.certify(q0[None].astype(np.float16), keys[None].astype(np.float16),
+                                   np.zeros((1, 4, d), dtype=np.float16), 1.0, exp_fmt="fp16")
+    assert certs[0]["B_h"] == 20.0 and certs[0]["C"] == 15 and certs[0]["certified"] == 0
+    _, certs = oracle_mod.certify(q0[None].astype(np.float16), keys[None].astype(np.float16),
+                                  np.zeros((1, 4, d), dtype=np.float16), 1.0, exp_fmt="bf16")
+    assert certs[0]["C"] == 125 and certs[0]["certified"] == 1
+    # an fp16 infinity is non-finite input
+    vbad = np.zeros((1, 4, d), dtype=np.float16)
+    vbad[0, 2, 3] = np.float16(np.inf)
+    _, certs = oracle_mod.certify(q0[None].astype(np.float16), keys[None].astype(np.float16), vbad, 1.0)
+    assert certs[0]["reason"] == 2
