@@ -19,6 +19,7 @@ LOG2E = 1.4426950408889634
 
 FMT = {"fp16": 0, "bf16": 1, "fp32": 2}
 VARIANT = {"auto": 0, "online": 1, "certified": 2, "online_lazy": 3}
+DTYPE = {torch.bfloat16: 0, torch.float16: 1}
 STATUS = {0: "CLIS_OK", 1: "CLIS_ERR_INVALID_ARG", 2: "CLIS_ERR_UNSUPPORTED", 3: "CLIS_ERR_MISALIGNED",
           4: "CLIS_ERR_WORKSPACE", 5: "CLIS_ERR_CUDA", 6: "CLIS_ERR_TIMEOUT"}
 
@@ -33,7 +34,7 @@ class Shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "B", "H", "Nq", "Nk", "d",
         "q_sb", "q_sh", "q_sn", "k_sb", "k_sh", "k_sn",
-        "v_sb", "v_sh", "v_sn", "o_sb", "o_sh", "o_sn")]
+        "v_sb", "v_sh", "v_sn", "o_sb", "o_sh", "o_sn", "dtype")]
 
 
 class Cert(ctypes.Structure):
@@ -99,12 +100,14 @@ def make_shape(q, k, v, o=None) -> Shape:
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
         if t is None:
             continue
-        if t.dim() != 4 or t.dtype != torch.bfloat16:
-            raise ValueError(f"{name} must be a 4-D bfloat16 tensor [B, H, N, d]")
+        if t.dim() != 4 or t.dtype not in DTYPE:
+            raise ValueError(f"{name} must be a 4-D bfloat16 or float16 tensor [B, H, N, d]")
+        if t.dtype != q.dtype:
+            raise ValueError("q, k, v and o must share one dtype")
         if t.stride(-1) != 1:
             raise ValueError(f"{name} must have a contiguous last dimension")
     B, H, Nq, d = q.shape
-    s = Shape(B=B, H=H, Nq=Nq, Nk=k.shape[2], d=d,
+    s = Shape(B=B, H=H, Nq=Nq, Nk=k.shape[2], d=d, dtype=DTYPE[q.dtype],
               q_sb=q.stride(0), q_sh=q.stride(1), q_sn=q.stride(2),
               k_sb=k.stride(0), k_sh=k.stride(1), k_sn=k.stride(2),
               v_sb=v.stride(0), v_sh=v.stride(1), v_sn=v.stride(2))
@@ -250,7 +253,8 @@ def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
     kbar = certs = mu = None
     if variant in ("auto", "certified"):
         mu = torch.empty(q.shape[0] * q.shape[1] * q.shape[2], dtype=torch.float32, device=q.device)
-        kbar, certs = clis_certify(q, k, v, sl2, mu=mu)
+        exp_fmt = "fp16" if q.dtype == torch.float16 else "bf16"
+        kbar, certs = clis_certify(q, k, v, sl2, mu=mu, exp_fmt=exp_fmt)
     out = clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=causal, variant=variant, mu=mu)
     if on_host:
         out = out.to("cpu")

@@ -70,8 +70,6 @@ struct Cfg {
     static constexpr int SMEM_BYTES = 2 * TILE_BYTES + NSTAGE * TILE_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
-    static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false);  // Q K^T, both K-major
-    static constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, true);    // P V, V is MN-major
 };
 
 struct Params {
@@ -123,7 +121,7 @@ struct Tile {
 // groups and shortest first on odd groups; with static round-robin assignment
 // this keeps the per-CTA work within about 1% while the K/V of one group of
 // heads stays in L2.
-template <bool CAUSAL>
+template <bool CAUSAL, int DT>
 __device__ __forceinline__ Tile decode_tile(const Params &p, int tile)
 {
     Tile t;
@@ -150,9 +148,20 @@ __device__ __forceinline__ Tile decode_tile(const Params &p, int tile)
     // (softmax does not depend on the key order).
     t.rev = ((tile / static_cast<int>(gridDim.x)) & 1) != 0;
     t.lazy = p.variant == CLIS_ONLINE_LAZY;
-    if (p.variant == CLIS_ONLINE || p.variant == CLIS_ONLINE_LAZY) t.cert = false;
-    else if (p.variant == CLIS_CERTIFIED_FORCED) t.cert = true;
-    else t.cert = __ldg(&p.certs[t.bh].certified) != 0;
+    if (p.variant == CLIS_ONLINE || p.variant == CLIS_ONLINE_LAZY) {
+        t.cert = false;
+    } else if (p.variant == CLIS_CERTIFIED_FORCED) {
+        t.cert = true;
+    } else {
+        t.cert = __ldg(&p.certs[t.bh].certified) != 0;
+        // FP16 P holds exp2 outputs only up to 2^15 (Figure 3): a head certified
+        // with a BF16 budget takes the fixed stabiliser only if B_h <= min(15, C).
+        if (DT && t.cert) {
+            const float bh = __ldg(&p.certs[t.bh].B_h);
+            const int cc = __ldg(&p.certs[t.bh].C);
+            t.cert = bh <= static_cast<float>(cc < 15 ? cc : 15);
+        }
+    }
     return t;
 }
 
@@ -173,7 +182,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
 // Runs on all 32 lanes of its warp (warp-uniform control flow); one elected
 // lane issues the copies.
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int DT>
 __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                               const CUtensorMap *tm_v, uint32_t sQ0, uint32_t sKV)
 {
@@ -187,7 +196,7 @@ __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, 
     int w = 0;
     int q_issued = -1;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
-        const Tile T = decode_tile<CAUSAL>(p, tile);
+        const Tile T = decode_tile<CAUSAL, DT>(p, tile);
         for (int t = 0; t < 2; t++) {
             if (!mbar_wait_warp(smem_u32(&c.q_empty[t]), (w & 1) ^ 1, ab, err, kErrProducer)) goto abort;
             if (leader) {
@@ -239,29 +248,32 @@ abort:
 // is advanced by adding (byte offset >> 4); every address stays below
 // 256 KB, so the field never carries into the next one.
 
-template <int D>
+template <int D, int DT>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qd, uint64_t kd)
 {
     using C = Cfg<D>;
+    // Q K^T: M = 128 rows, N = 128 keys, both operands K-major; A/B format 1 = bf16, 0 = f16.
+    constexpr uint32_t IDESC_S = idesc_f16kind_f32(BM, BN, false, DT ? 0u : 1u);
 #pragma unroll
     for (int kk = 0; kk < D / 16; kk++) {
         // 16 elements = 32 bytes inside a 128-byte swizzle row; 4 steps per 64-column box.
         const uint32_t off = ((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4;
-        umma_ss(d_tmem, qd + off, kd + off, C::IDESC_S, kk > 0 ? 1u : 0u);
+        umma_ss(d_tmem, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
     }
 }
 
-template <int D>
+template <int D, int DT>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t vd, uint32_t accumulate)
 {
-    using C = Cfg<D>;
+    // P V: M = 128 rows, N = D, P from TMEM, V MN-major in shared memory.
+    constexpr uint32_t IDESC_O = idesc_f16kind_f32(BM, D, true, DT ? 0u : 1u);
     // V tile: keys x D, D contiguous (MN-major B operand); 16 keys = 2048 bytes.
 #pragma unroll
     for (int kk = 0; kk < BN / 16; kk++)
-        umma_ts(o_tmem, p_tmem + kk * 8, vd + ((kk * 2048) >> 4), C::IDESC_O, (accumulate | kk) ? 1u : 0u);
+        umma_ts(o_tmem, p_tmem + kk * 8, vd + ((kk * 2048) >> 4), IDESC_O, (accumulate | kk) ? 1u : 0u);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int DT>
 __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, uint32_t sKV)
 {
     using C = Cfg<D>;
@@ -278,7 +290,7 @@ __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, u
     const uint64_t kvd_v = sdesc_sw128(sKV, C::BOX_BYTES, 1024);
     auto stage_off = [](uint32_t s) -> uint64_t { return (s * C::TILE_BYTES) >> 4; };
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
-        const Tile T = decode_tile<CAUSAL>(p, tile);
+        const Tile T = decode_tile<CAUSAL, DT>(p, tile);
         for (int t = 0; t < 2; t++)
             if (!mbar_wait_warp(smem_u32(&c.q_full[t]), w & 1, ab, err, kErrMma)) goto abort;
         {
@@ -287,9 +299,9 @@ __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, u
             tc_fence_after();
             const uint64_t kd = kvd_k + stage_off(ks);
             if (leader) {
-                issue_qk<D>(tmem + C::TM_S0, qd0, kd);
+                issue_qk<D, DT>(tmem + C::TM_S0, qd0, kd);
                 umma_commit(smem_u32(&c.s_full[0]));
-                issue_qk<D>(tmem + C::TM_S1, qd1, kd);
+                issue_qk<D, DT>(tmem + C::TM_S1, qd1, kd);
                 umma_commit(smem_u32(&c.s_full[1]));
                 umma_commit(smem_u32(&c.kv_empty[ks]));
                 if (T.n_kv == 1) {
@@ -317,7 +329,7 @@ __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, u
                     if (!mbar_wait_warp(smem_u32(&c.o_free[t]), (w & 1) ^ 1, ab, err, kErrMma)) goto abort;
                 tc_fence_after();
                 if (leader) {
-                    issue_pv<D>(tmem + (t ? C::TM_O1 : C::TM_O0), tmem + (t ? C::TM_S1 : C::TM_S0), vd,
+                    issue_pv<D, DT>(tmem + (t ? C::TM_O1 : C::TM_O0), tmem + (t ? C::TM_S1 : C::TM_S0), vd,
                                 j > 0 ? 1u : 0u);
                     umma_commit(smem_u32(&c.pv_done[t]));
                     if (t == 1) umma_commit(smem_u32(&c.kv_empty[vs]));
@@ -330,7 +342,7 @@ __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, u
                         tc_fence_after();
                     }
                     if (leader) {
-                        issue_qk<D>(tmem + (t ? C::TM_S1 : C::TM_S0), t ? qd1 : qd0, kd);
+                        issue_qk<D, DT>(tmem + (t ? C::TM_S1 : C::TM_S0), t ? qd1 : qd0, kd);
                         umma_commit(smem_u32(&c.s_full[t]));
                         if (t == 1) umma_commit(smem_u32(&c.kv_empty[kns]));
                         if (j + 1 == T.n_kv - 1) umma_commit(smem_u32(&c.q_empty[t]));
@@ -352,7 +364,7 @@ abort:
 
 // ------------------------------------------------------------------- softmax
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int DT>
 __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, int lane)
 {
     using C = Cfg<D>;
@@ -369,7 +381,7 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
     int w = 0;
 
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
-        const Tile T = decode_tile<CAUSAL>(p, tile);
+        const Tile T = decode_tile<CAUSAL, DT>(p, tile);
         const int row = T.qb * 2 * BM + t * BM + rl;  // query index within the head
         const bool row_ok = row < p.Nq;
 
@@ -386,14 +398,14 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
                 const uint4 u = *reinterpret_cast<const uint4 *>(qr + c8 * 8);
                 const float4 k0 = __ldg(reinterpret_cast<const float4 *>(kb + c8 * 8));
                 const float4 k1 = __ldg(reinterpret_cast<const float4 *>(kb + c8 * 8 + 4));
-                acc0 = fmaf(__uint_as_float(u.x << 16), k0.x, acc0);
-                acc1 = fmaf(__uint_as_float(u.x & 0xFFFF0000u), k0.y, acc1);
-                acc0 = fmaf(__uint_as_float(u.y << 16), k0.z, acc0);
-                acc1 = fmaf(__uint_as_float(u.y & 0xFFFF0000u), k0.w, acc1);
-                acc0 = fmaf(__uint_as_float(u.z << 16), k1.x, acc0);
-                acc1 = fmaf(__uint_as_float(u.z & 0xFFFF0000u), k1.y, acc1);
-                acc0 = fmaf(__uint_as_float(u.w << 16), k1.z, acc0);
-                acc1 = fmaf(__uint_as_float(u.w & 0xFFFF0000u), k1.w, acc1);
+                acc0 = fmaf(elem_lo<DT>(u.x), k0.x, acc0);
+                acc1 = fmaf(elem_hi<DT>(u.x), k0.y, acc1);
+                acc0 = fmaf(elem_lo<DT>(u.y), k0.z, acc0);
+                acc1 = fmaf(elem_hi<DT>(u.y), k0.w, acc1);
+                acc0 = fmaf(elem_lo<DT>(u.z), k1.x, acc0);
+                acc1 = fmaf(elem_hi<DT>(u.z), k1.y, acc1);
+                acc0 = fmaf(elem_lo<DT>(u.w), k1.z, acc0);
+                acc1 = fmaf(elem_hi<DT>(u.w), k1.w, acc1);
             }
             mu = sl2 * (acc0 + acc1);
         }
@@ -474,7 +486,7 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
                     const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                     if (e & 1) lb = fadd2(lb, pp);
                     else la = fadd2(la, pp);
-                    pk[e] = pack_bf16x2(pp.x, pp.y);
+                    pk[e] = pack2<DT>(pp.x, pp.y);
                 }
                 tmem_st16(tS + c32 * 16, pk);
             }
@@ -528,7 +540,7 @@ abort:
 // (thread = TMEM lane = row): O / l -> bf16 (or, in KV-chunk mode, the merge
 // into the fp32 accumulators) and lse2.  `shift` is the row's stabiliser:
 // mu_i on the certified path, the (possibly stale) row maximum online.
-template <int D>
+template <int D, int DT>
 __device__ __forceinline__ void write_row(const Params &p, const Tile &T, uint32_t tO, int row, bool row_ok,
                                           float l_run, float shift)
 {
@@ -591,7 +603,7 @@ __device__ __forceinline__ void write_row(const Params &p, const Tile &T, uint32
                 for (int e = 0; e < 16; e++) {
                     const float2 o2 =
                         fmul2(make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), inv2);
-                    pk[e] = pack_bf16x2(o2.x, o2.y);
+                    pk[e] = pack2<DT>(o2.x, o2.y);
                 }
                 uint4 *dst = reinterpret_cast<uint4 *>(orow + c32 * 32);
 #pragma unroll
@@ -606,7 +618,7 @@ __device__ __forceinline__ void write_row(const Params &p, const Tile &T, uint32
 
 // ---------------------------------------------------------------- correction
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int DT>
 __device__ void correction_role(const Params &p, Ctl &c, uint32_t tmem, int warp, int lane)
 {
     using C = Cfg<D>;
@@ -618,7 +630,7 @@ __device__ void correction_role(const Params &p, Ctl &c, uint32_t tmem, int warp
     uint32_t g = 0, ncorr = 0;
     int w = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
-        const Tile T = decode_tile<CAUSAL>(p, tile);
+        const Tile T = decode_tile<CAUSAL, DT>(p, tile);
         if (T.cert || T.lazy) {
             g += T.n_kv;
         } else {
@@ -659,7 +671,7 @@ __device__ void correction_role(const Params &p, Ctl &c, uint32_t tmem, int warp
             if (!mbar_wait(smem_u32(&c.pv_done[t]), (g - 1) & 1, ab, err, kErrCorrection)) return;
             tc_fence_after();
             const int row = T.qb * 2 * BM + t * BM + rl;
-            write_row<D>(p, T, tmem + (t ? C::TM_O1 : C::TM_O0) + lane_off, row, row < p.Nq, c.epi_l[t][rl],
+            write_row<D, DT>(p, T, tmem + (t ? C::TM_O1 : C::TM_O0) + lane_off, row, row < p.Nq, c.epi_l[t][rl],
                          c.epi_shift[t][rl]);
             tc_fence_before();
             mbar_arrive(smem_u32(&c.o_free[t]));
@@ -669,7 +681,7 @@ __device__ void correction_role(const Params &p, Ctl &c, uint32_t tmem, int warp
 
 // -------------------------------------------------------------------- kernel
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params p)
@@ -721,14 +733,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // correction 128 x 80, producer/MMA group 128 x 80 -> 45056 + 10240 + 10240 = 65536.
     if (warp < 8) {
         setmaxnreg_inc<176>();
-        softmax_role<D, CAUSAL>(p, ctl, tmem, warp, lane);
+        softmax_role<D, CAUSAL, DT>(p, ctl, tmem, warp, lane);
     } else if (warp < 12) {
         setmaxnreg_dec<80>();
-        correction_role<D, CAUSAL>(p, ctl, tmem, warp, lane);
+        correction_role<D, CAUSAL, DT>(p, ctl, tmem, warp, lane);
     } else {
         setmaxnreg_dec<80>();
-        if (warp == 12) producer_role<D, CAUSAL>(p, ctl, &tm_q, &tm_k, &tm_v, sQ0, sKV);
-        if (warp == 13) mma_role<D, CAUSAL>(p, ctl, tmem, sQ0, sKV);
+        if (warp == 12) producer_role<D, CAUSAL, DT>(p, ctl, &tm_q, &tm_k, &tm_v, sQ0, sKV);
+        if (warp == 13) mma_role<D, CAUSAL, DT>(p, ctl, tmem, sQ0, sKV);
     }
 
     tc_fence_before();
@@ -756,8 +768,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
 }
 
 // 4-D map over [B, H, N, d] (innermost first: d, N, H, B), 64 x 128 boxes, 128-byte swizzle.
-bool make_map(CUtensorMap *map, const void *base, int64_t B, int64_t H, int64_t N, int64_t d, int64_t sb,
-              int64_t sh, int64_t sn)
+bool make_map(CUtensorMap *map, const void *base, int dtype, int64_t B, int64_t H, int64_t N, int64_t d,
+              int64_t sb, int64_t sh, int64_t sn)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
     if (!enc) return false;
@@ -770,13 +782,14 @@ bool make_map(CUtensorMap *map, const void *base, int64_t B, int64_t H, int64_t 
                              static_cast<cuuint64_t>(sb * 2)};
     cuuint32_t box[4] = {64, 128, 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+    CUresult r = enc(map, dtype == CLIS_DT_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                     const_cast<void *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int DT>
 clis_status_t launch_impl(const AttnArgs &a, cudaStream_t stream)
 {
     using C = Cfg<D>;
@@ -784,14 +797,14 @@ clis_status_t launch_impl(const AttnArgs &a, cudaStream_t stream)
     if (cudaGetDevice(&dev) != cudaSuccess) return CLIS_ERR_CUDA;
     int nsm = 0;
     if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return CLIS_ERR_CUDA;
-    if (cudaFuncSetAttribute(attn_fwd_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_fwd_kernel<D, CAUSAL, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
         return CLIS_ERR_CUDA;
 
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, a.q, a.B, a.H, a.Nq, D, a.q_sb, a.q_sh, a.q_sn)) return CLIS_ERR_CUDA;
-    if (!make_map(&mk, a.k, a.B, a.H, a.Nk, D, a.k_sb, a.k_sh, a.k_sn)) return CLIS_ERR_CUDA;
-    if (!make_map(&mv, a.v, a.B, a.H, a.Nk, D, a.v_sb, a.v_sh, a.v_sn)) return CLIS_ERR_CUDA;
+    if (!make_map(&mq, a.q, DT, a.B, a.H, a.Nq, D, a.q_sb, a.q_sh, a.q_sn)) return CLIS_ERR_CUDA;
+    if (!make_map(&mk, a.k, DT, a.B, a.H, a.Nk, D, a.k_sb, a.k_sh, a.k_sn)) return CLIS_ERR_CUDA;
+    if (!make_map(&mv, a.v, DT, a.B, a.H, a.Nk, D, a.v_sb, a.v_sh, a.v_sn)) return CLIS_ERR_CUDA;
 
     Params p;
     p.q = a.q;
@@ -826,7 +839,7 @@ clis_status_t launch_impl(const AttnArgs &a, cudaStream_t stream)
     p.m_acc = a.m_acc;
     if (p.num_tiles == 0) return CLIS_OK;
     const int grid = p.num_tiles < nsm ? p.num_tiles : nsm;
-    attn_fwd_kernel<D, CAUSAL><<<grid, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+    attn_fwd_kernel<D, CAUSAL, DT><<<grid, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? CLIS_OK : CLIS_ERR_CUDA;
 }
 
@@ -863,10 +876,17 @@ __global__ void chunk_finalize_kernel(ChunkFinalizeArgs a)
     const float4 *src = reinterpret_cast<const float4 *>(a.o_acc + ridx * a.d + c8 * 8);
     const float4 x0 = src[0], x1 = src[1];
     uint4 out;
-    out.x = pack_bf16x2(x0.x * inv, x0.y * inv);
-    out.y = pack_bf16x2(x0.z * inv, x0.w * inv);
-    out.z = pack_bf16x2(x1.x * inv, x1.y * inv);
-    out.w = pack_bf16x2(x1.z * inv, x1.w * inv);
+    if (a.dtype == CLIS_DT_FP16) {
+        out.x = pack_f16x2(x0.x * inv, x0.y * inv);
+        out.y = pack_f16x2(x0.z * inv, x0.w * inv);
+        out.z = pack_f16x2(x1.x * inv, x1.y * inv);
+        out.w = pack_f16x2(x1.z * inv, x1.w * inv);
+    } else {
+        out.x = pack_bf16x2(x0.x * inv, x0.y * inv);
+        out.y = pack_bf16x2(x0.z * inv, x0.w * inv);
+        out.z = pack_bf16x2(x1.x * inv, x1.y * inv);
+        out.w = pack_bf16x2(x1.z * inv, x1.w * inv);
+    }
     *reinterpret_cast<uint4 *>(a.o + b * a.o_sb + h * a.o_sh + static_cast<int64_t>(row) * a.o_sn + c8 * 8) = out;
     if (a.lse2 && c8 == 0) a.lse2[ridx] = a.m_acc[ridx] + log2f(l);
 }
@@ -890,8 +910,13 @@ clis_status_t launch_wait_selftest(uint32_t limit_us, cudaStream_t stream)
 
 clis_status_t launch_attn_fwd(const AttnArgs &a, cudaStream_t stream)
 {
-    if (a.d == 128) return a.causal ? launch_impl<128, true>(a, stream) : launch_impl<128, false>(a, stream);
-    return a.causal ? launch_impl<64, true>(a, stream) : launch_impl<64, false>(a, stream);
+    if (a.dtype == CLIS_DT_FP16) {
+        if (a.d == 128)
+            return a.causal ? launch_impl<128, true, 1>(a, stream) : launch_impl<128, false, 1>(a, stream);
+        return a.causal ? launch_impl<64, true, 1>(a, stream) : launch_impl<64, false, 1>(a, stream);
+    }
+    if (a.d == 128) return a.causal ? launch_impl<128, true, 0>(a, stream) : launch_impl<128, false, 0>(a, stream);
+    return a.causal ? launch_impl<64, true, 0>(a, stream) : launch_impl<64, false, 0>(a, stream);
 }
 
 clis_status_t read_device_error(uint32_t *code)

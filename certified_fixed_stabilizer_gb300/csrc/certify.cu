@@ -27,6 +27,7 @@
 #include <mutex>
 
 #include "clis_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace clis {
 
@@ -37,9 +38,6 @@ namespace clis {
 static __device__ __align__(256) unsigned char g_certify_scratch[CLIS_NOALLOC_SCRATCH_BYTES];
 
 namespace {
-
-__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
 __device__ __forceinline__ uint32_t abs_bits_max(uint32_t u, uint32_t m)
 {
@@ -74,7 +72,8 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red)
 }
 
 // Step 1 (partial): column sums of one chunk of K, plus max |k| bits.
-template <int D>
+// DT: element type (0 bf16, 1 fp16); |x| bit patterns are x & 0x7FFF in both.
+template <int D, int DT>
 __global__ void __launch_bounds__(kCertThreads) certify_ksum_kernel(CertArgs a, CertWorkspace ws)
 {
     constexpr int VPR = D / 8;             // 16-byte vectors per row
@@ -100,8 +99,8 @@ __global__ void __launch_bounds__(kCertThreads) certify_ksum_kernel(CertArgs a, 
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int e = 0; e < 4; e++) {
-            acc[2 * e] += bf16_lo(w[e]);
-            acc[2 * e + 1] += bf16_hi(w[e]);
+            acc[2 * e] += elem_lo<DT>(w[e]);
+            acc[2 * e + 1] += elem_hi<DT>(w[e]);
             amax = abs_bits_max(w[e], amax);
         }
     }
@@ -129,7 +128,7 @@ __global__ void certify_kbar_kernel(CertArgs a, CertWorkspace ws)
 }
 
 // Steps 2-5 (partial): one chunk of K (centred norms), Q (norms) or V (|v|).
-template <int D>
+template <int D, int DT>
 __global__ void __launch_bounds__(kCertThreads) certify_norms_kernel(CertArgs a, CertWorkspace ws)
 {
     constexpr int VPR = D / 8;
@@ -174,7 +173,7 @@ __global__ void __launch_bounds__(kCertThreads) certify_norms_kernel(CertArgs a,
                 const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                 for (int e = 0; e < 4; e++) {
-                    const float x0 = bf16_lo(w[e]), x1 = bf16_hi(w[e]);
+                    const float x0 = elem_lo<DT>(w[e]), x1 = elem_hi<DT>(w[e]);
                     const float d0 = (x0 >= kb[2 * e]) ? __fsub_ru(x0, kb[2 * e]) : __fsub_ru(kb[2 * e], x0);
                     const float d1 = (x1 >= kb[2 * e + 1]) ? __fsub_ru(x1, kb[2 * e + 1])
                                                            : __fsub_ru(kb[2 * e + 1], x1);
@@ -206,7 +205,7 @@ __global__ void __launch_bounds__(kCertThreads) certify_norms_kernel(CertArgs a,
                 const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                 for (int e = 0; e < 4; e++) {
-                    const float x0 = bf16_lo(w[e]), x1 = bf16_hi(w[e]);
+                    const float x0 = elem_lo<DT>(w[e]), x1 = elem_hi<DT>(w[e]);
                     ss = __fmaf_ru(x0, x0, ss);
                     ss = __fmaf_ru(x1, x1, ss);
                     dot = fmaf(x0, kb[2 * e], dot);
@@ -250,14 +249,17 @@ __device__ __forceinline__ int ceil_log2_i64(int64_t n)
     return (n <= 1) ? 0 : 64 - __clzll(static_cast<unsigned long long>(n - 1));
 }
 
-// G = ceil(log2 max(1, m)) for the bf16 magnitude with bit pattern `bits`
-// (sign cleared, finite): m = (1 + f/128) 2^(e-127) for a normal number.
-__device__ __forceinline__ int v_exponent_from_bf16_bits(uint32_t bits)
+// G = ceil(log2 max(1, m)) for the magnitude m with bit pattern `bits` (sign
+// cleared, finite).  bf16: m = (1 + f/2^7) 2^(e-127); fp16: m = (1 + f/2^10)
+// 2^(e-15) for a normal number; m <= 1 (zero, subnormals, 1.0) gives 0.
+__device__ __forceinline__ int v_exponent_from_bits(uint32_t bits, int dtype)
 {
-    if (bits <= 0x3F80u) return 0;  // m <= 1 (includes zero and subnormals)
-    const int e = static_cast<int>(bits >> 7);
-    const uint32_t f = bits & 0x7Fu;
-    return (e - 127) + (f != 0u ? 1 : 0);
+    if (dtype == CLIS_DT_FP16) {
+        if (bits <= 0x3C00u) return 0;
+        return (static_cast<int>(bits >> 10) - 15) + ((bits & 0x3FFu) != 0u ? 1 : 0);
+    }
+    if (bits <= 0x3F80u) return 0;
+    return (static_cast<int>(bits >> 7) - 127) + ((bits & 0x7Fu) != 0u ? 1 : 0);
 }
 
 // Steps 3-7 and the decision: one warp per head.
@@ -285,7 +287,8 @@ __global__ void certify_finalize_kernel(CertArgs a, CertWorkspace ws, int BH)
     if (lane != 0) return;
 
     clis_head_cert_t c;
-    const bool finite = ka < 0x7F80u && va < 0x7F80u && qa < 0x7F80u;
+    const uint32_t inf_bits = (a.dtype == CLIS_DT_FP16) ? 0x7C00u : 0x7F80u;  // |x| of +infinity
+    const bool finite = ka < inf_bits && va < inf_bits && qa < inf_bits;
     c.kappa = __fsqrt_ru(__uint_as_float(kn));   // step 3
     c.qmax = __fsqrt_ru(__uint_as_float(qn));
     if (!finite) {
@@ -295,7 +298,7 @@ __global__ void certify_finalize_kernel(CertArgs a, CertWorkspace ws, int BH)
         c.B_h = __int_as_float(0x7F800000);
     } else {
         c.B_h = __fmul_ru(__fmul_ru(a.scale_log2, c.qmax), c.kappa);  // step 4
-        c.G = v_exponent_from_bf16_bits(va);                           // step 5
+        c.G = v_exponent_from_bits(va, a.dtype);                       // step 5
         c.A = ceil_log2_i64(a.Nk) + c.G;                               // step 6
         // step 7: floor(U_exp) = emax_exp and ceil(U_acc - A) - 1 = emax_acc - A,
         // because log2 of a format's largest finite value lies in (emax, emax + 1).
@@ -358,16 +361,21 @@ cudaError_t launch_certify(const CertArgs &a, const CertWorkspace &ws, cudaStrea
     if (BH == 0) return cudaSuccess;
     const unsigned g1 = static_cast<unsigned>(BH) * static_cast<unsigned>(a.nck);
     const unsigned g3 = static_cast<unsigned>(BH) * static_cast<unsigned>(2 * a.nck + a.ncq);
+    const bool f16 = a.dtype == CLIS_DT_FP16;
     if (a.d == 128) {
-        certify_ksum_kernel<128><<<g1, kCertThreads, 0, stream>>>(a, ws);
+        if (f16) certify_ksum_kernel<128, 1><<<g1, kCertThreads, 0, stream>>>(a, ws);
+        else certify_ksum_kernel<128, 0><<<g1, kCertThreads, 0, stream>>>(a, ws);
     } else {
-        certify_ksum_kernel<64><<<g1, kCertThreads, 0, stream>>>(a, ws);
+        if (f16) certify_ksum_kernel<64, 1><<<g1, kCertThreads, 0, stream>>>(a, ws);
+        else certify_ksum_kernel<64, 0><<<g1, kCertThreads, 0, stream>>>(a, ws);
     }
     certify_kbar_kernel<<<BH, 128, 0, stream>>>(a, ws);
     if (a.d == 128) {
-        certify_norms_kernel<128><<<g3, kCertThreads, 0, stream>>>(a, ws);
+        if (f16) certify_norms_kernel<128, 1><<<g3, kCertThreads, 0, stream>>>(a, ws);
+        else certify_norms_kernel<128, 0><<<g3, kCertThreads, 0, stream>>>(a, ws);
     } else {
-        certify_norms_kernel<64><<<g3, kCertThreads, 0, stream>>>(a, ws);
+        if (f16) certify_norms_kernel<64, 1><<<g3, kCertThreads, 0, stream>>>(a, ws);
+        else certify_norms_kernel<64, 0><<<g3, kCertThreads, 0, stream>>>(a, ws);
     }
     certify_finalize_kernel<<<(BH + 3) / 4, 128, 0, stream>>>(a, ws, BH);
     return cudaGetLastError();

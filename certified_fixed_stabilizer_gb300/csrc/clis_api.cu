@@ -27,6 +27,7 @@ clis_status_t check_shape(const clis_shape_t *s, bool with_o)
     if (!s) return CLIS_ERR_INVALID_ARG;
     if (s->B < 0 || s->H < 0 || s->Nq < 0 || s->Nk < 1 || s->d < 1) return CLIS_ERR_INVALID_ARG;
     if (s->d != 64 && s->d != 128) return CLIS_ERR_UNSUPPORTED;
+    if (s->dtype != CLIS_DT_BF16 && s->dtype != CLIS_DT_FP16) return CLIS_ERR_INVALID_ARG;
     if (s->Nq > kMaxN || s->Nk > kMaxN || s->B * s->H > kMaxN || s->B > kMaxN || s->H > kMaxN)
         return CLIS_ERR_UNSUPPORTED;
     clis_status_t st;
@@ -99,6 +100,7 @@ clis_status_t clis_certify(const clis_shape_t *shape, const void *q, const void 
     a.Nq = static_cast<int>(shape->Nq);
     a.Nk = static_cast<int>(shape->Nk);
     a.d = static_cast<int>(shape->d);
+    a.dtype = static_cast<int>(shape->dtype);
     a.nck = static_cast<int>(div_up(shape->Nk, clis::kCertChunkRows));
     a.ncq = static_cast<int>(div_up(shape->Nq, clis::kCertChunkRows));
     a.scale_log2 = scale_log2;
@@ -161,6 +163,7 @@ clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, const void
     a.Nq = static_cast<int>(shape->Nq);
     a.Nk = static_cast<int>(shape->Nk);
     a.d = static_cast<int>(shape->d);
+    a.dtype = static_cast<int>(shape->dtype);
     a.scale_log2 = scale_log2;
     a.causal = causal;
     a.variant = variant;
@@ -231,6 +234,7 @@ clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void *q, cons
     a.Nq = static_cast<int>(shape->Nq);
     a.Nk = static_cast<int>(shape->Nk);
     a.d = static_cast<int>(shape->d);
+    a.dtype = static_cast<int>(shape->dtype);
     a.scale_log2 = scale_log2;
     a.causal = 0;
     a.variant = variant;
@@ -247,6 +251,7 @@ clis_status_t clis_attn_chunk_finalize(const clis_shape_t *shape, const float *o
     if (!shape) return CLIS_ERR_INVALID_ARG;
     if (shape->B < 0 || shape->H < 0 || shape->Nq < 0) return CLIS_ERR_INVALID_ARG;
     if (shape->d != 64 && shape->d != 128) return CLIS_ERR_UNSUPPORTED;
+    if (shape->dtype != CLIS_DT_BF16 && shape->dtype != CLIS_DT_FP16) return CLIS_ERR_INVALID_ARG;
     if (shape->Nq > kMaxN || shape->B * shape->H > kMaxN) return CLIS_ERR_UNSUPPORTED;
     if (shape->B * shape->H == 0 || shape->Nq == 0) return CLIS_OK;
     if (!o_acc || !l_acc || !m_acc || !o) return CLIS_ERR_INVALID_ARG;
@@ -268,6 +273,7 @@ clis_status_t clis_attn_chunk_finalize(const clis_shape_t *shape, const float *o
     a.H = static_cast<int>(shape->H);
     a.Nq = static_cast<int>(shape->Nq);
     a.d = static_cast<int>(shape->d);
+    a.dtype = static_cast<int>(shape->dtype);
     return clis::launch_chunk_finalize(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -29,6 +29,7 @@ struct CertArgs {
     const uint16_t *q, *k, *v;  // bf16 bits
     int64_t q_sb, q_sh, q_sn, k_sb, k_sh, k_sn, v_sb, v_sh, v_sn;
     int B, H, Nq, Nk, d;
+    int dtype;  // clis_dtype_t
     int nck, ncq;
     float scale_log2;
     int emax_exp, emax_acc;  // floor(U) of the exp2-output and accumulator formats
@@ -58,6 +59,7 @@ struct AttnArgs {
     const float *mu = nullptr;  // optional per-row stabilisers from clis_certify
     int64_t q_sb, q_sh, q_sn, k_sb, k_sh, k_sn, v_sb, v_sh, v_sn, o_sb, o_sh, o_sn;
     int B, H, Nq, Nk, d;
+    int dtype = CLIS_DT_BF16;
     float scale_log2;
     int causal;
     int variant;
@@ -71,6 +73,7 @@ struct ChunkFinalizeArgs {
     float *lse2;
     int64_t o_sb, o_sh, o_sn;
     int B, H, Nq, d;
+    int dtype;
 };
 
 clis_status_t launch_chunk_finalize(const ChunkFinalizeArgs &a, cudaStream_t stream);

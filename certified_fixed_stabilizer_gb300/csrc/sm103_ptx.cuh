@@ -3,6 +3,8 @@
 // loads, tcgen05 TMEM allocation, MMA, commit, loads and stores.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include <cstdint>
 
 namespace clis {
@@ -196,12 +198,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and an fp32 accumulator.
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
+// Instruction descriptor, kind::f16 with an fp32 accumulator; A and B both
+// bf16 (ab_fmt = 1) or both f16 (ab_fmt = 0).
+//   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format,
 //   bit 15 A major (0 = K), bit 16 B major (1 = MN), 17-22 N >> 3, 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major)
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(int M, int N, bool b_mn_major, uint32_t ab_fmt)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) |
+    return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | (b_mn_major ? (1u << 16) : 0u) |
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
@@ -334,6 +337,33 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
+}
+
+// Pack two fp32 into f16x2 (round to nearest even): lo -> bits 0-15, hi -> 16-31.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Element type of Q, K, V, O and P: DT = 0 bf16, 1 fp16 (the clis_dtype_t values).
+template <int DT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    return DT ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+
+template <int DT>
+__device__ __forceinline__ float elem_lo(uint32_t u)
+{
+    return DT ? __half2float(__ushort_as_half(static_cast<unsigned short>(u & 0xFFFFu))) : __uint_as_float(u << 16);
+}
+
+template <int DT>
+__device__ __forceinline__ float elem_hi(uint32_t u)
+{
+    return DT ? __half2float(__ushort_as_half(static_cast<unsigned short>(u >> 16))) : __uint_as_float(u & 0xFFFF0000u);
 }
 
 template <uint32_t N>

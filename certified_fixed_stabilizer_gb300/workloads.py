@@ -11,7 +11,7 @@ so these tensors stand in for them with the paper's shapes (H=40, S=75,600,
 D=128 at 720p x 81 frames, Table 7; 32,760 tokens at 480p x 81 frames,
 Table 8) and simple Gaussian value distributions.
 
-Layout of every tensor: [B, H, N, d], bf16, d contiguous.
+Layout of every tensor: [B, H, N, d], bf16 (or fp16 on request), d contiguous.
 """
 from __future__ import annotations
 
@@ -95,13 +95,14 @@ def injected_heads(w: Workload) -> list[int]:
 
 
 def make_inputs(w: Workload, device="cpu", seed: int | None = None, N: int | None = None,
-                H: int | None = None):
-    """Generate (q, k, v) bf16 tensors of shape [B, H, N, d] for workload ``w``.
+                H: int | None = None, dtype=torch.bfloat16):
+    """Generate (q, k, v) tensors of shape [B, H, N, d] for workload ``w``.
 
     Values are drawn in fp32 with a seeded torch.Generator on ``device`` and
-    rounded to bf16 (nearest even).  ``N`` / ``H`` override the sequence
-    length / head count (reduced-size copies of a workload for tests and
-    profiling; injected heads are then chosen among the heads that exist).
+    rounded to ``dtype`` (bf16 by default, or fp16; nearest even).  ``N`` /
+    ``H`` override the sequence length / head count (reduced-size copies of a
+    workload for tests and profiling; injected heads are then chosen among the
+    heads that exist).
     """
     seed = w.seed if seed is None else seed
     N = w.N if N is None else N
@@ -109,16 +110,16 @@ def make_inputs(w: Workload, device="cpu", seed: int | None = None, N: int | Non
     dev = torch.device(device)
     g = _gen(dev, seed)
     shape = (w.B, H, N, w.d)
-    q = torch.empty(shape, dtype=torch.bfloat16, device=dev)
-    k = torch.empty(shape, dtype=torch.bfloat16, device=dev)
-    v = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    q = torch.empty(shape, dtype=dtype, device=dev)
+    k = torch.empty(shape, dtype=dtype, device=dev)
+    v = torch.empty(shape, dtype=dtype, device=dev)
     # One head at a time keeps the fp32 temporaries small at 720p.
     for b in range(w.B):
         for h in range(H):
             bias = torch.randn(w.d, generator=g, device=dev) * w.bias_sigma
-            q[b, h] = (torch.randn(N, w.d, generator=g, device=dev) * w.q_sigma).to(torch.bfloat16)
-            k[b, h] = (torch.randn(N, w.d, generator=g, device=dev) * w.k_sigma + bias).to(torch.bfloat16)
-            v[b, h] = (torch.randn(N, w.d, generator=g, device=dev) * w.v_sigma).to(torch.bfloat16)
+            q[b, h] = (torch.randn(N, w.d, generator=g, device=dev) * w.q_sigma).to(dtype)
+            k[b, h] = (torch.randn(N, w.d, generator=g, device=dev) * w.k_sigma + bias).to(dtype)
+            v[b, h] = (torch.randn(N, w.d, generator=g, device=dev) * w.v_sigma).to(dtype)
     if w.inject_frac > 0:
         _inject(w, q, k, v, seed)
     return q, k, v
@@ -136,7 +137,7 @@ def _inject(w: Workload, q, k, v, seed: int) -> None:
         if h >= H:
             continue
         rows = torch.randperm(N, generator=g)[:n_out].to(k.device)
-        k[b, h, rows] = (k[b, h, rows].float() * w.outlier_scale).to(torch.bfloat16)
+        k[b, h, rows] = (k[b, h, rows].float() * w.outlier_scale).to(k.dtype)
         n_v = 8
         vr = torch.randint(0, N, (n_v,), generator=g)
         vc = torch.randint(0, w.d, (n_v,), generator=g)

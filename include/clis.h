@@ -9,8 +9,8 @@
  * fail certification run standard online softmax instead (abstract).
  *
  * Conventions shared by every entry point:
- *  - Tensors are bf16 in layout [B, H, N, d] with element strides given in
- *    clis_shape_t; the d dimension is contiguous (stride 1).
+ *  - Tensors are bf16 (or fp16, shape->dtype) in layout [B, H, N, d] with
+ *    element strides given in clis_shape_t; the d dimension is contiguous.
  *  - Device pointers must be 16-byte aligned and every stride (n, h, b) a
  *    multiple of 8 elements (16 bytes); otherwise CLIS_ERR_MISALIGNED.
  *  - d must be 64 or 128 (CLIS_ERR_UNSUPPORTED otherwise).
@@ -46,7 +46,7 @@ typedef struct CUstream_st *clis_stream_t;
 
 typedef enum {
     CLIS_OK = 0,
-    CLIS_ERR_INVALID_ARG = 1,  /* null pointer, negative/zero size, bad enum, non-finite or <= 0 scale */
+    CLIS_ERR_INVALID_ARG = 1,  /* null pointer, negative/zero size, bad enum or dtype, non-finite or <= 0 scale */
     CLIS_ERR_UNSUPPORTED = 2,  /* head dim not in {64, 128}, causal with Nq != Nk, sizes beyond int32 */
     CLIS_ERR_MISALIGNED = 3,   /* pointer not 16-byte aligned or stride not a multiple of 8 elements */
     CLIS_ERR_WORKSPACE = 4,    /* workspace null or smaller than clis_certify_workspace_size() */
@@ -80,14 +80,24 @@ typedef enum {
     CLIS_ONLINE_LAZY = 3
 } clis_variant_t;
 
+/* Element type of Q, K, V and O (all four share it).  The attention kernel
+ * feeds P to the tensor cores in the same type, so with FP16 data the exp2
+ * outputs are FP16 (Figure 3: U_exp = 15.9993): certify FP16 data with
+ * exp_fmt = CLIS_FMT_FP16.  As a safeguard, in CLIS_AUTO an FP16 head takes the
+ * fixed-stabiliser path only if its certificate also satisfies
+ * B_h <= min(15, C); otherwise it runs online softmax. */
+typedef enum { CLIS_DT_BF16 = 0, CLIS_DT_FP16 = 1 } clis_dtype_t;
+
 /* Problem shape and element strides (elements, not bytes).  K and V share
- * Nk; Q and O share Nq.  O strides are ignored by clis_certify. */
+ * Nk; Q and O share Nq.  O strides are ignored by clis_certify.  dtype is a
+ * clis_dtype_t (0 = BF16, the zero-initialised default). */
 typedef struct {
     int64_t B, H, Nq, Nk, d;
     int64_t q_sb, q_sh, q_sn;
     int64_t k_sb, k_sh, k_sn;
     int64_t v_sb, v_sh, v_sn;
     int64_t o_sb, o_sh, o_sn;
+    int64_t dtype;
 } clis_shape_t;
 
 /* Per-head certificate, Algorithm 1 (one per (b, h) pair, index b*H + h).

@@ -115,6 +115,10 @@ def test_attn_rejects_bad_arguments(clis):
     assert _attn(clis, _shape(clis), causal=2) == INV
     assert _attn(clis, _shape(clis, Nq=300, Nk=400), causal=1) == UNSUP
     assert _attn(clis, _shape(clis, d=256)) == UNSUP
+    bad = _shape(clis)
+    bad.dtype = 7
+    assert _attn(clis, bad) == INV
+    assert _certify(clis, bad) == INV
     assert _attn(clis, _shape(clis), o=FAKE + 2) == MIS
     assert _attn(clis, _shape(clis), lse2=FAKE + 2) == MIS
     lib = clis.load_library()

@@ -36,9 +36,11 @@ def _device_error_word_stays_clear():
     assert code == 0, f"device error word {code:#x}"
 
 
-def _run(q, k, v, causal, variant, lse2=False, softmax_scale=None):
+def _run(q, k, v, causal, variant, lse2=False, softmax_scale=None, exp_fmt=None):
     sl2 = clis.scale_log2_for(q.shape[-1], softmax_scale)
-    kbar, certs = clis.clis_certify(q, k, v, sl2)
+    if exp_fmt is None:
+        exp_fmt = "fp16" if q.dtype == torch.float16 else "bf16"
+    kbar, certs = clis.clis_certify(q, k, v, sl2, exp_fmt=exp_fmt)
     l2 = None
     if lse2:
         l2 = torch.full((q.shape[0] * q.shape[1] * q.shape[2],), float("nan"), device=q.device)
@@ -303,3 +305,65 @@ def test_kv_chunk_single_chunk_equals_fused():
     fused = clis.clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs)
     out, _, _, _ = _chunked(q, k, v, [0, 3000], "auto", kbar, certs, lse2=False)
     assert_paths_agree(flat(out), flat(fused), "single chunk")
+
+
+
+@pytest.mark.parametrize("variant", ["auto", "online", "certified", "online_lazy"])
+def test_fp16_full_parity(variant):
+    """FP16 data with the 480p distributions (B_h ~ 5.5, within the FP16 budget
+    C = 15), all rows checked.  (The tiny workload's B_h ~ 20 exceeds it: with
+    fp16 data those heads do not certify.)"""
+    dev = need_gpu()
+    w = WORKLOADS["480p"]
+    q, k, v = make_inputs(w, device=dev, N=777, H=2, dtype=torch.float16)
+    out, l2, certs = _run(q, k, v, False, variant, lse2=True)
+    assert out.dtype == torch.float16
+    ref, rlse = _oracle(q, k, v, False)
+    assert_close_to_oracle(out.float().cpu().numpy(), ref, f"fp16/{variant}")
+    np.testing.assert_allclose(l2.cpu().numpy().reshape(rlse.shape), rlse, atol=1e-3, rtol=0)
+    c = clis.decode_certs(certs)
+    assert all(x["certified"] and x["C"] == 15 for x in c)
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal", [(1, 2, 1, 1, 64, False), (2, 3, 129, 129, 64, True),
+                                                (1, 2, 1000, 257, 128, False), (2, 2, 700, 700, 128, True),
+                                                (1, 4, 20000, 100, 128, False)])
+@pytest.mark.parametrize("variant", ["auto", "online", "online_lazy"])
+def test_fp16_ragged_shapes(B, H, Nq, Nk, d, causal, variant):
+    dev = need_gpu()
+    g = torch.Generator(device=dev)
+    g.manual_seed(B * 7919 + H * 131 + Nq + Nk * 3 + d)
+    q = torch.randn(B, H, Nq, d, generator=g, device=dev).half()
+    k = (torch.randn(B, H, Nk, d, generator=g, device=dev) * 0.5 + 0.7).half()
+    v = torch.randn(B, H, Nk, d, generator=g, device=dev).half()
+    out, l2, _ = _run(q, k, v, causal, variant, lse2=True)
+    ref, rlse = _oracle(q, k, v, causal)
+    assert_close_to_oracle(out.float().cpu().numpy(), ref, f"fp16 {(B, H, Nq, Nk, d, causal)}/{variant}")
+    np.testing.assert_allclose(l2.cpu().numpy().reshape(rlse.shape), rlse, atol=2e-3, rtol=0)
+
+
+def test_fp16_auto_guard_with_bf16_budget():
+    """Heads certified with the BF16 budget (B_h ~ 23 <= 127 - A) but not the FP16
+    one: in AUTO with fp16 data they must run online softmax (fixed-stabiliser
+    p would reach 2^23 and overflow FP16)."""
+    dev = need_gpu()
+    w = WORKLOADS["causal"]
+    q, k, v = make_inputs(w, device=dev, N=1500, H=2, dtype=torch.float16)
+    out, _, certs = _run(q, k, v, False, "auto", exp_fmt="bf16")
+    c = clis.decode_certs(certs)
+    assert all(x["certified"] for x in c) and all(x["B_h"] > 15 for x in c)
+    assert torch.isfinite(out).all()
+    ref, _ = _oracle(q, k, v, False)
+    assert_close_to_oracle(out.float().cpu().numpy(), ref, "fp16 guard")
+
+
+def test_fp16_kv_chunks():
+    dev = need_gpu()
+    w = WORKLOADS["480p"]
+    q, k, v = make_inputs(w, device=dev, N=3000, H=3, dtype=torch.float16)
+    sl2 = clis.scale_log2_for(w.d)
+    kbar, certs = clis.clis_certify(q, k, v, sl2, exp_fmt="fp16")
+    out, l2, _, _ = _chunked(q, k, v, [0, 1000, 1001, 3000], "auto", kbar, certs)
+    assert out.dtype == torch.float16
+    ref, rlse = _oracle(q, k, v, False)
+    assert_close_to_oracle(flat(out).float().cpu().numpy(), ref, "fp16 chunked")

@@ -216,3 +216,41 @@ def test_per_row_stabilisers(name):
     got = mu.cpu().double().numpy().reshape(ref.shape)
     scale = sl2 * np.linalg.norm(qf, axis=2) * np.linalg.norm(okbar, axis=1)[:, None]
     assert np.all(np.abs(got - ref) <= 1e-5 * scale + 1e-6)
+
+
+@pytest.mark.parametrize("name,N,H", [("tiny", None, None), ("480p", 5000, 4), ("mixed", 3000, 8), ("causal", 2000, 4)])
+def test_fp16_certificates_match_oracle(name, N, H):
+    """FP16 data certified with the FP16 exp2 budget (U_exp = 15.9993, Figure 3):
+    flags, G, A, C bit-exact vs the oracle."""
+    dev = need_gpu()
+    w = WORKLOADS[name]
+    q, k, v = make_inputs(w, device=dev, N=N, H=H, dtype=torch.float16)
+    g, oc = _compare(q, k, v, clis.scale_log2_for(w.d), exp_fmt="fp16")
+    assert all(c["C"] <= 15 for c in g if c["reason"] != 2)
+    if name == "causal":   # B_h ~ 23 > 15: every head fails the FP16 budget
+        assert not any(c["certified"] for c in g)
+
+
+@pytest.mark.parametrize("vm,G", [(4096.0, 12), (4100.0, 13), (1.0, 0), (0.5, 0), (3.0, 2), (65504.0, 16)])
+def test_fp16_v_exponent_bit_exact(vm, G):
+    dev = need_gpu()
+    d = 64
+    keys = np.stack([np.eye(1, d, 0)[0], -np.eye(1, d, 0)[0]] * 2).astype(np.float32)
+    vals = np.zeros((4, d), dtype=np.float32)
+    vals[1, 3] = -vm
+    q = torch.tensor(np.ones((1, d), np.float32)).to(torch.float16).reshape(1, 1, 1, d).to(dev)
+    k = torch.tensor(keys).to(torch.float16).reshape(1, 1, 4, d).to(dev)
+    v = torch.tensor(vals).to(torch.float16).reshape(1, 1, 4, d).to(dev)
+    g, _ = _compare(q, k, v, 1.0, expect_no_band=False)
+    assert g[0]["G"] == G and g[0]["A"] == 2 + G
+
+
+@pytest.mark.parametrize("where", ["q", "k", "v"])
+def test_fp16_nonfinite_inputs_fail_certification(where):
+    dev = need_gpu()
+    w = WORKLOADS["480p"]   # B_h ~ 5.5: clean heads certify under the FP16 budget
+    q, k, v = make_inputs(w, device=dev, N=700, H=2, dtype=torch.float16)
+    t = {"q": q, "k": k, "v": v}[where]
+    t[0, 1, 300, 9] = float("inf")
+    g, oc = _compare(q, k, v, clis.scale_log2_for(w.d), exp_fmt="fp16")
+    assert g[1]["reason"] == 2 and g[0]["certified"] == 1
