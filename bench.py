@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling runs)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--variant", default="auto", choices=["auto", "online", "certified", "online_lazy"])
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"],
+                    help="element type of Q, K, V, P and O (fp16 certifies with the FP16 exp2 budget)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the online-variant, e2e and CPU-baseline legs (profiling runs)")
     return ap.parse_args()
@@ -231,7 +233,9 @@ def main():
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
 
-    q, k, v = make_inputs(w, device=dev, H=H)
+    dt = torch.float16 if args.dtype == "fp16" else torch.bfloat16
+    exp_fmt = args.dtype
+    q, k, v = make_inputs(w, device=dev, H=H, dtype=dt)
     heads = w.B * H
     flops = w.flops() * H / w.H
     sl2 = clis.scale_log2_for(w.d)
@@ -247,7 +251,7 @@ def main():
 
     def step(variant):
         if variant in ("auto", "certified"):
-            clis.clis_certify(q, k, v, sl2, kbar=kbar, certs=certs, workspace=wsp, mu=mu)
+            clis.clis_certify(q, k, v, sl2, kbar=kbar, certs=certs, workspace=wsp, mu=mu, exp_fmt=exp_fmt)
         clis.clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=w.causal, variant=variant, out=out,
                            mu=mu)
 
@@ -264,7 +268,7 @@ def main():
                 flush_buf.zero_()
             e0.record(stream)
             if variant in ("auto", "certified"):
-                clis.clis_certify(q, k, v, sl2, kbar=kbar, certs=certs, workspace=wsp, mu=mu)
+                clis.clis_certify(q, k, v, sl2, kbar=kbar, certs=certs, workspace=wsp, mu=mu, exp_fmt=exp_fmt)
             e1.record(stream)
             clis.clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=w.causal, variant=variant,
                                out=out, mu=mu)
@@ -303,7 +307,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
+        "dtype": args.dtype, "data": "synthetic",
         "config": config_dict(w, H, args.variant),
         "gpu_launches": args.steps * (5 if args.variant in ("auto", "certified") else 1),
         "certified_heads": f"{n_cert}/{heads}",
@@ -373,7 +377,7 @@ def main():
             dq.copy_(qh, non_blocking=True)
             dk.copy_(kh, non_blocking=True)
             dv.copy_(vh, non_blocking=True)
-            clis.clis_certify(dq, dk, dv, sl2, kbar=kbar, certs=certs, workspace=wsp, mu=mu)
+            clis.clis_certify(dq, dk, dv, sl2, kbar=kbar, certs=certs, workspace=wsp, mu=mu, exp_fmt=exp_fmt)
             clis.clis_attn_fwd(dq, dk, dv, sl2, kbar=kbar, certs=certs, causal=w.causal, variant=args.variant,
                                out=out, mu=mu)
             oh.copy_(out, non_blocking=True)
