@@ -237,27 +237,93 @@ def certify(q, k, v, softmax_scale: float | None = None, **kw):
     return clis_certify(q, k, v, scale_log2_for(q.shape[-1], softmax_scale), **kw)
 
 
+def _exp_fmt(q) -> str:
+    return "fp16" if q.dtype == torch.float16 else "bf16"
+
+
 def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
-              variant: str = "auto", return_certs: bool = False, device=None):
+              variant: str = "auto", return_certs: bool = False, device=None, out=None,
+              groups: int = 8, non_blocking: bool = False):
     """CLiS attention forward: certification pre-pass, then the fused kernel.
 
-    q, k, v: bf16 [B, H, N, d].  Host tensors (pinned or not) are copied to
-    ``device`` (default cuda:0) and the result is copied back to the host;
-    device tensors stay where they are.
+    q, k, v: bf16 or fp16 [B, H, N, d].  Device tensors are processed in place
+    on the current stream.  Host tensors (pinned for overlap) are copied to
+    ``device`` (default cuda:0) and the result is written to ``out`` (a host
+    tensor, allocated if None): heads are processed in ``groups`` groups on
+    three streams so that the copies of one group overlap the compute of
+    another (heads are independent).  The call returns once ``out`` is filled,
+    unless ``non_blocking``: then the current stream is ordered after the work
+    and the caller synchronises it before reading ``out``.
     """
-    on_host = q.device.type == "cpu"
-    if on_host:
-        dev = torch.device(device or "cuda:0")
-        q, k, v = (t.to(dev, non_blocking=True) for t in (q, k, v))
+    if q.device.type == "cpu":
+        return _attention_host(q, k, v, softmax_scale, causal, variant, return_certs,
+                               torch.device(device or "cuda:0"), out, groups, non_blocking)
     sl2 = scale_log2_for(q.shape[-1], softmax_scale)
     kbar = certs = mu = None
     if variant in ("auto", "certified"):
         mu = torch.empty(q.shape[0] * q.shape[1] * q.shape[2], dtype=torch.float32, device=q.device)
-        exp_fmt = "fp16" if q.dtype == torch.float16 else "bf16"
-        kbar, certs = clis_certify(q, k, v, sl2, mu=mu, exp_fmt=exp_fmt)
-    out = clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=causal, variant=variant, mu=mu)
-    if on_host:
-        out = out.to("cpu")
+        kbar, certs = clis_certify(q, k, v, sl2, mu=mu, exp_fmt=_exp_fmt(q))
+    res = clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=causal, variant=variant, mu=mu,
+                        out=out)
+    if return_certs:
+        return res, kbar, certs
+    return res
+
+
+def _attention_host(q, k, v, softmax_scale, causal, variant, return_certs, dev, out, groups, non_blocking):
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned())
+    qd = torch.empty(q.shape, dtype=q.dtype, device=dev)
+    kd = torch.empty(k.shape, dtype=k.dtype, device=dev)
+    vd = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    od = torch.empty(q.shape, dtype=q.dtype, device=dev)
+    sl2 = scale_log2_for(d, softmax_scale)
+    certified = variant in ("auto", "certified")
+    kbar = torch.empty((B * H, d), dtype=torch.float32, device=dev) if certified else None
+    certs = torch.empty((B * H, CERT_WORDS), dtype=torch.int32, device=dev) if certified else None
+    mu = torch.empty(B * H * Nq, dtype=torch.float32, device=dev) if certified else None
+    # head groups: contiguous (b, h0:h1) slices, about `groups` of them in total
+    per = max(1, -(-B * H // max(1, groups)))
+    spans = []
+    for b in range(B):
+        for h0 in range(0, H, per):
+            spans.append((b, h0, min(H, h0 + per)))
+    cur = torch.cuda.current_stream(dev)
+    s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    for s in (s_in, s_run, s_out):
+        s.wait_stream(cur)
+    for b, h0, h1 in spans:
+        sl = (slice(b, b + 1), slice(h0, h1))
+        ev_in = torch.cuda.Event()
+        with torch.cuda.stream(s_in):
+            qd[sl].copy_(q[sl], non_blocking=True)
+            kd[sl].copy_(k[sl], non_blocking=True)
+            vd[sl].copy_(v[sl], non_blocking=True)
+            ev_in.record(s_in)
+        s_run.wait_event(ev_in)
+        f0, f1 = b * H + h0, b * H + h1
+        ev_run = torch.cuda.Event()
+        with torch.cuda.stream(s_run):
+            kb = cs = m = None
+            if certified:
+                kb, cs, m = kbar[f0:f1], certs[f0:f1], mu[f0 * Nq:f1 * Nq]
+                clis_certify(qd[sl], kd[sl], vd[sl], sl2, kbar=kb, certs=cs, mu=m, exp_fmt=_exp_fmt(q),
+                             stream=s_run)
+            clis_attn_fwd(qd[sl], kd[sl], vd[sl], sl2, kbar=kb, certs=cs, causal=causal, variant=variant,
+                          mu=m, out=od[sl], stream=s_run)
+            ev_run.record(s_run)
+        s_out.wait_event(ev_run)
+        with torch.cuda.stream(s_out):
+            out[sl].copy_(od[sl], non_blocking=True)
+    cur.wait_stream(s_out)
+    for t in (qd, kd, vd, od):
+        t.record_stream(s_in)
+        t.record_stream(s_run)
+        t.record_stream(s_out)
+    if not non_blocking:
+        s_out.synchronize()
     if return_certs:
         return out, kbar, certs
     return out

@@ -219,6 +219,26 @@ def test_stabilisers_from_certification_match_in_kernel_ones():
     assert_close_to_oracle(flat(a).float().cpu().numpy(), ref, "mu from certify vs oracle")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_host_path_pipelined_over_head_groups(causal):
+    """attention() with pinned host tensors splits the heads into groups that
+    cross the batch boundary; the result matches the device path and the oracle."""
+    dev = need_gpu()
+    g = torch.Generator(device="cpu")
+    g.manual_seed(17)
+    B, H, N, d = 2, 3, 900, 128
+    q = torch.randn(B, H, N, d, generator=g).to(torch.bfloat16).pin_memory()
+    k = (torch.randn(B, H, N, d, generator=g) * 0.5 + 0.3).to(torch.bfloat16).pin_memory()
+    v = torch.randn(B, H, N, d, generator=g).to(torch.bfloat16).pin_memory()
+    host = clis.attention(q, k, v, causal=causal, groups=4)
+    assert host.device.type == "cpu" and host.shape == q.shape
+    dev_out = clis.attention(q.to(dev), k.to(dev), v.to(dev), causal=causal)
+    torch.cuda.synchronize()
+    assert_paths_agree(flat(host.to(dev)), flat(dev_out), "host vs device")
+    ref, _ = _oracle(q, k, v, causal)
+    assert_close_to_oracle(host.float().numpy().reshape(ref.shape), ref, "host pipelined")
+
+
 def test_outputs_are_deterministic():
     dev = need_gpu()
     w = WORKLOADS["mixed"]
