@@ -16,6 +16,9 @@ What it computes (each routine cites the passage it follows):
   q_i.k_j) v_j, computed in fp64 with two passes per row.  A fixed stabiliser
   cancels exactly in real arithmetic, so this definition is the result both
   CLiS kernels must reproduce.
+* :func:`attention_bwd` -- gradients dQ, dK, dV of sum_i dO_i . O_i for the
+  same attention, by the plain chain rule through softmax (the pages give no
+  backward algorithm; their causal LLM training results, Table 3, need one).
 
 The arithmetic lives in ``clis_oracle.c``; this module only builds it with
 gcc and marshals numpy arrays.  Every function here is pinned by the
@@ -83,6 +86,10 @@ def _load():
         for name in ("oracle_attn_bf16", "oracle_attn_fp16", "oracle_attn_f64"):
             f = getattr(lib, name)
             f.argtypes = [i64, i64, i64, i64, vp, vp, vp, dbl, i32, i64, vp, vp, vp]
+            f.restype = i32
+        for name in ("oracle_attn_bwd_bf16", "oracle_attn_bwd_fp16", "oracle_attn_bwd_f64"):
+            f = getattr(lib, name)
+            f.argtypes = [i64, i64, i64, i64, vp, vp, vp, vp, dbl, i32, vp, vp, vp]
             f.restype = i32
         lib.oracle_format_log2_max.argtypes = [i32]
         lib.oracle_format_log2_max.restype = dbl
@@ -231,6 +238,36 @@ def attention(q, k, v, scale: float, causal: bool = False, rows=None,
     if rc != 0:
         raise ValueError(f"oracle attention rejected its arguments (rc={rc})")
     return (out, lse2) if with_lse2 else out
+
+
+def attention_bwd(q, k, v, do, scale: float, causal: bool = False):
+    """fp64 gradients (dq, dk, dv) of L = sum(O * do) for O = attention(q, k, v).
+
+    Inputs as for :func:`attention` (``do`` has q's shape and format).  Returns
+    three float64 arrays, heads first: dq [BH, Nq, d], dk and dv [BH, Nk, d].
+    """
+    f64 = isinstance(q, np.ndarray) and q.dtype == np.float64
+    if f64:
+        qa, ka, va, ga = (np.ascontiguousarray(t, dtype=np.float64) for t in (q, k, v, do))
+        fn = _load().oracle_attn_bwd_f64
+    else:
+        (qa, fq), (ka, fk), (va, fv), (ga, fg) = (as_bits(t) for t in (q, k, v, do))
+        if not fq == fk == fv == fg:
+            raise TypeError("q, k, v, do must share one format")
+        fn = _load().oracle_attn_bwd_fp16 if fq == "fp16" else _load().oracle_attn_bwd_bf16
+    qa, ka, va, ga = (_heads_first(a) for a in (qa, ka, va, ga))
+    if ga.shape != qa.shape:
+        raise ValueError("do must have q's shape")
+    BH, Nq, d = qa.shape
+    Nk = ka.shape[1]
+    dq = np.zeros((BH, Nq, d), dtype=np.float64)
+    dk = np.zeros((BH, Nk, d), dtype=np.float64)
+    dv = np.zeros((BH, Nk, d), dtype=np.float64)
+    rc = fn(BH, Nq, Nk, d, _ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), float(scale), int(bool(causal)),
+            _ptr(dq), _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise ValueError(f"oracle attention_bwd rejected its arguments (rc={rc})")
+    return dq, dk, dv
 
 
 def num_threads() -> int:

@@ -26,6 +26,11 @@
  *                   cancels between numerator and denominator, this plain
  *                   definition is the exact result CLiS must reproduce.
  *
+ *  oracle_attn_bwd_*  gradients dQ, dK, dV of L = sum_i dO_i . O_i for the
+ *                   same attention (the backward pass of causal training,
+ *                   Table 3's setting).  The pages give no backward
+ *                   algorithm; this is the plain chain rule through softmax.
+ *
  * Readings of the pages (where they are silent or garbled):
  *  - kappa ("a conservative upper bound on max_r ||k~_r||_2", Alg. 1 step 3):
  *    the oracle computes the exact fp64 maximum of the centred key norms.
@@ -340,6 +345,144 @@ int oracle_attn_f64(int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
                     double *out, double *lse2)
 {
     return attn_driver(1, BH, Nq, Nk, d, q, k, v, scale, causal, n_rows, rows, out, lse2);
+}
+
+/* ---------------------------------------------------------------- backward
+ *
+ * For one head with scores x_ij = scale * q_i . k_j over the visible keys and
+ * P_ij = softmax_j(x_ij) (row i sums to one):
+ *
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = dO_i . v_j
+ *   D_i   = sum_j P_ij dP_ij
+ *   dX_ij = P_ij (dP_ij - D_i)        (softmax Jacobian times dP, row i)
+ *   dQ_i  = scale sum_j dX_ij k_j
+ *   dK_j  = scale sum_i dX_ij q_i
+ *
+ * Pass 1 runs over rows (in parallel): the row's log-sum-exp, D_i and dQ_i.
+ * Pass 2 runs over keys (in parallel): P_ij = exp(x_ij - lse_i) for every row
+ * that sees key j, then dV_j and dK_j.  Inputs are decoded to fp64 first.
+ * el: 0 bf16 bits, 1 fp64, 2 fp16 bits.  Outputs [BH][N][d] fp64.
+ */
+static double load_el(const void *a, int64_t e, int el)
+{
+    if (el == 1) return ((const double *)a)[e];
+    return bits_to_double(((const uint16_t *)a)[e], el == 2 ? ORC_IN_FP16 : ORC_IN_BF16);
+}
+
+static int attn_bwd_driver(int el, int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
+                           const void *q, const void *k, const void *v, const void *dout,
+                           double scale, int causal, double *dq, double *dk, double *dv)
+{
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1) return 1;
+    if (causal && Nq != Nk) return 1;
+    size_t nq = (size_t)(Nq * d), nk = (size_t)(Nk * d);
+    double *qh = (double *)malloc((nq ? nq : 1) * sizeof(double));
+    double *gh = (double *)malloc((nq ? nq : 1) * sizeof(double));
+    double *kh = (double *)malloc(nk * sizeof(double));
+    double *vh = (double *)malloc(nk * sizeof(double));
+    double *lse = (double *)malloc((Nq ? (size_t)Nq : 1) * sizeof(double));
+    double *D = (double *)malloc((Nq ? (size_t)Nq : 1) * sizeof(double));
+    if (!qh || !gh || !kh || !vh || !lse || !D) {
+        free(qh); free(gh); free(kh); free(vh); free(lse); free(D);
+        return 2;
+    }
+    for (int64_t h = 0; h < BH; h++) {
+        for (size_t e = 0; e < nq; e++) {
+            qh[e] = load_el(q, (int64_t)(h * nq + e), el);
+            gh[e] = load_el(dout, (int64_t)(h * nq + e), el);
+        }
+        for (size_t e = 0; e < nk; e++) {
+            kh[e] = load_el(k, (int64_t)(h * nk + e), el);
+            vh[e] = load_el(v, (int64_t)(h * nk + e), el);
+        }
+        double *dqh = dq + h * nq, *dkh = dk + h * nk, *dvh = dv + h * nk;
+
+        /* pass 1: rows */
+#pragma omp parallel
+        {
+            double *x = (double *)malloc((size_t)Nk * sizeof(double));
+            double *dp = (double *)malloc((size_t)Nk * sizeof(double));
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t i = 0; i < Nq; i++) {
+                const double *qi = qh + i * d, *gi = gh + i * d;
+                int64_t jmax = causal ? i : Nk - 1;
+                double m = -INFINITY;
+                for (int64_t j = 0; j <= jmax; j++) {
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < d; c++) acc += qi[c] * kh[j * d + c];
+                    x[j] = scale * acc;
+                    if (x[j] > m) m = x[j];
+                }
+                double l = 0.0;
+                for (int64_t j = 0; j <= jmax; j++) l += exp(x[j] - m);
+                lse[i] = m + log(l);
+                double Di = 0.0;
+                for (int64_t j = 0; j <= jmax; j++) {
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < d; c++) acc += gi[c] * vh[j * d + c];
+                    dp[j] = acc;
+                    Di += exp(x[j] - lse[i]) * acc;
+                }
+                D[i] = Di;
+                double *o = dqh + i * d;
+                for (int64_t c = 0; c < d; c++) o[c] = 0.0;
+                for (int64_t j = 0; j <= jmax; j++) {
+                    double dx = exp(x[j] - lse[i]) * (dp[j] - Di);
+                    for (int64_t c = 0; c < d; c++) o[c] += dx * kh[j * d + c];
+                }
+                for (int64_t c = 0; c < d; c++) o[c] *= scale;
+            }
+            free(x);
+            free(dp);
+        }
+
+        /* pass 2: keys */
+#pragma omp parallel for schedule(dynamic, 4)
+        for (int64_t j = 0; j < Nk; j++) {
+            const double *kj = kh + j * d, *vj = vh + j * d;
+            double *gk = dkh + j * d, *gv = dvh + j * d;
+            for (int64_t c = 0; c < d; c++) { gk[c] = 0.0; gv[c] = 0.0; }
+            for (int64_t i = causal ? j : 0; i < Nq; i++) {
+                const double *qi = qh + i * d, *gi = gh + i * d;
+                double s = 0.0, dpij = 0.0;
+                for (int64_t c = 0; c < d; c++) {
+                    s += qi[c] * kj[c];
+                    dpij += gi[c] * vj[c];
+                }
+                double pij = exp(scale * s - lse[i]);
+                double dx = pij * (dpij - D[i]);
+                for (int64_t c = 0; c < d; c++) {
+                    gv[c] += pij * gi[c];
+                    gk[c] += dx * qi[c];
+                }
+            }
+            for (int64_t c = 0; c < d; c++) gk[c] *= scale;
+        }
+    }
+    free(qh); free(gh); free(kh); free(vh); free(lse); free(D);
+    return 0;
+}
+
+int oracle_attn_bwd_bf16(int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
+                         const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
+                         double scale, int causal, double *dq, double *dk, double *dv)
+{
+    return attn_bwd_driver(0, BH, Nq, Nk, d, q, k, v, dout, scale, causal, dq, dk, dv);
+}
+
+int oracle_attn_bwd_fp16(int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
+                         const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
+                         double scale, int causal, double *dq, double *dk, double *dv)
+{
+    return attn_bwd_driver(2, BH, Nq, Nk, d, q, k, v, dout, scale, causal, dq, dk, dv);
+}
+
+int oracle_attn_bwd_f64(int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
+                        const double *q, const double *k, const double *v, const double *dout,
+                        double scale, int causal, double *dq, double *dk, double *dv)
+{
+    return attn_bwd_driver(1, BH, Nq, Nk, d, q, k, v, dout, scale, causal, dq, dk, dv);
 }
 
 int oracle_num_threads(void)
