@@ -1,4 +1,4 @@
-"""CLiS (Certified Loop-invariant Stabilization) attention forward for GB300.
+"""CLiS (Certified Loop-invariant Stabilization) attention for GB300.
 
 The compute lives in ``libclis.so`` (CUDA for sm_103a, C ABI declared in
 ``include/clis.h``).  :mod:`certified_fixed_stabilizer_gb300.clis` is the thin
@@ -17,6 +17,8 @@ _BINDING_NAMES = {
     "ClisError", "attention", "certify", "Cert", "VARIANT", "FMT", "STATUS",
     "library_path", "load_library", "decode_certs", "make_shape", "scale_log2_for",
     "Shape", "CERT_WORDS", "LOG2E", "clis_debug_wait_selftest", "clis_attn_fwd_chunk", "clis_attn_chunk_finalize",
+    "clis_attn_bwd", "clis_attn_bwd_workspace_size", "attention_bwd", "attention_fwd_lse", "attention_autograd",
+    "AttentionFunction",
 }
 
 

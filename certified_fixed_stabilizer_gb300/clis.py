@@ -81,6 +81,10 @@ def load_library():
     lib.clis_attn_chunk_finalize.restype = i32
     lib.clis_debug_wait_selftest.argtypes = [ctypes.c_uint32, vp]
     lib.clis_debug_wait_selftest.restype = i32
+    lib.clis_attn_bwd_workspace_size.argtypes = [sp, ctypes.POINTER(sz)]
+    lib.clis_attn_bwd_workspace_size.restype = i32
+    lib.clis_attn_bwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, vp, sz, vp]
+    lib.clis_attn_bwd.restype = i32
     _lib = lib
     return lib
 
@@ -192,6 +196,87 @@ def clis_attn_chunk_finalize(q, o_acc, l_acc, m_acc, out=None, lse2=None, stream
     if st != 0:
         raise ClisError("clis_attn_chunk_finalize", st)
     return out
+
+
+def clis_attn_bwd_workspace_size(shape: Shape) -> int:
+    n = ctypes.c_size_t(0)
+    st = load_library().clis_attn_bwd_workspace_size(ctypes.byref(shape), ctypes.byref(n))
+    if st != 0:
+        raise ClisError("clis_attn_bwd_workspace_size", st)
+    return n.value
+
+
+def _like(t):
+    """Empty tensor with t's shape and strides (the backward writes dq, dk, dv
+    with the strides of q, k, v)."""
+    return torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, device=t.device)
+
+
+def clis_attn_bwd(q, k, v, o, dout, lse2, scale_log2: float, causal: bool = False, dq=None, dk=None, dv=None,
+                  workspace=None, stream=None):
+    """Attention backward; returns (dq, dk, dv) with the strides of q, k, v.
+
+    o: the forward output; dout: its gradient, with o's strides; lse2: the
+    forward's fp32 row statistic [B*H*Nq]."""
+    lib = load_library()
+    if dout.stride() != o.stride():
+        dout = torch.empty_strided(o.shape, o.stride(), dtype=o.dtype, device=o.device).copy_(dout)
+    dq = _like(q) if dq is None else dq
+    dk = _like(k) if dk is None else dk
+    dv = _like(v) if dv is None else dv
+    for name, g, t in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if g.stride() != t.stride() or g.shape != t.shape or g.dtype != t.dtype:
+            raise ValueError(f"{name} must have the shape, strides and dtype of {name[1]}")
+    shape = make_shape(q, k, v, o)
+    if workspace is None:
+        workspace = torch.empty(max(1, clis_attn_bwd_workspace_size(shape)), dtype=torch.uint8, device=q.device)
+    st = lib.clis_attn_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse2),
+                           _ptr(dq), _ptr(dk), _ptr(dv), float(scale_log2), int(bool(causal)), _ptr(workspace),
+                           workspace.numel(), _stream(stream))
+    if st != 0:
+        raise ClisError("clis_attn_bwd", st)
+    return dq, dk, dv
+
+
+def attention_fwd_lse(q, k, v, softmax_scale: float | None = None, causal: bool = False, variant: str = "auto"):
+    """Forward that also returns the row statistic the backward needs:
+    (o, lse2), lse2 fp32 [B*H*Nq]."""
+    sl2 = scale_log2_for(q.shape[-1], softmax_scale)
+    lse2 = torch.empty(q.shape[0] * q.shape[1] * q.shape[2], dtype=torch.float32, device=q.device)
+    kbar = certs = mu = None
+    if variant in ("auto", "certified"):
+        mu = torch.empty_like(lse2)
+        kbar, certs = clis_certify(q, k, v, sl2, mu=mu, exp_fmt=_exp_fmt(q))
+    o = clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=causal, variant=variant, mu=mu, lse2=lse2)
+    return o, lse2
+
+
+def attention_bwd(q, k, v, o, dout, lse2, softmax_scale: float | None = None, causal: bool = False):
+    """(dq, dk, dv) for the attention whose forward gave (o, lse2)."""
+    return clis_attn_bwd(q, k, v, o, dout, lse2, scale_log2_for(q.shape[-1], softmax_scale), causal=causal)
+
+
+class AttentionFunction(torch.autograd.Function):
+    """Autograd wrapper: CLiS forward (certify + fused kernel), backward
+    through clis_attn_bwd.  Device tensors only."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, softmax_scale, causal, variant):
+        o, lse2 = attention_fwd_lse(q, k, v, softmax_scale, causal, variant)
+        ctx.save_for_backward(q, k, v, o, lse2)
+        ctx.softmax_scale, ctx.causal = softmax_scale, causal
+        return o
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, o, lse2 = ctx.saved_tensors
+        dq, dk, dv = attention_bwd(q, k, v, o, dout, lse2, ctx.softmax_scale, ctx.causal)
+        return dq, dk, dv, None, None, None
+
+
+def attention_autograd(q, k, v, softmax_scale: float | None = None, causal: bool = False, variant: str = "auto"):
+    """Differentiable CLiS attention (training): o = attention(q, k, v)."""
+    return AttentionFunction.apply(q, k, v, softmax_scale, causal, variant)
 
 
 def clis_get_device_error() -> int:

@@ -291,13 +291,90 @@ const char *clis_status_string(clis_status_t s)
     return "unknown status";
 }
 
+clis_status_t clis_attn_bwd_workspace_size(const clis_shape_t *shape, size_t *bytes)
+{
+    if (!bytes) return CLIS_ERR_INVALID_ARG;
+    clis_status_t st = check_shape(shape, true);
+    if (st != CLIS_OK) return st;
+    const int64_t rows = shape->B * shape->H * shape->Nq;
+    *bytes = static_cast<size_t>(div_up(rows * 4, 256) * 256);
+    return CLIS_OK;
+}
+
+clis_status_t clis_attn_bwd(const clis_shape_t *shape, const void *q, const void *k, const void *v, const void *o,
+                            const void *dout, const float *lse2, void *dq, void *dk, void *dv, float scale_log2,
+                            int causal, void *workspace, size_t ws_bytes, clis_stream_t stream)
+{
+    clis_status_t st = check_shape(shape, true);
+    if (st != CLIS_OK) return st;
+    if (shape->B * shape->H == 0) return CLIS_OK;
+    if (!std::isfinite(scale_log2) || !(scale_log2 > 0.f)) return CLIS_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return CLIS_ERR_INVALID_ARG;
+    if (causal && shape->Nq != shape->Nk) return CLIS_ERR_UNSUPPORTED;
+    if (!k || !v || !dk || !dv) return CLIS_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv)) return CLIS_ERR_MISALIGNED;
+    if (shape->Nq > 0) {
+        if (!q || !o || !dout || !lse2 || !dq) return CLIS_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+            (reinterpret_cast<uintptr_t>(lse2) & 3u))
+            return CLIS_ERR_MISALIGNED;
+        size_t need = 0;
+        clis_attn_bwd_workspace_size(shape, &need);
+        if (!workspace || ws_bytes < need || !aligned16(workspace)) return CLIS_ERR_WORKSPACE;
+    }
+    const int64_t tiles = shape->B * shape->H * div_up(shape->Nk > shape->Nq ? shape->Nk : shape->Nq, 128);
+    if (tiles > kMaxN) return CLIS_ERR_UNSUPPORTED;
+
+    clis::AttnBwdArgs a;
+    a.q = static_cast<const uint16_t *>(q);
+    a.k = static_cast<const uint16_t *>(k);
+    a.v = static_cast<const uint16_t *>(v);
+    a.o = static_cast<const uint16_t *>(o);
+    a.dout = static_cast<const uint16_t *>(dout);
+    a.lse2 = lse2;
+    a.dvec = static_cast<float *>(workspace);
+    a.dq = static_cast<uint16_t *>(dq);
+    a.dk = static_cast<uint16_t *>(dk);
+    a.dv = static_cast<uint16_t *>(dv);
+    a.q_sb = shape->q_sb;
+    a.q_sh = shape->q_sh;
+    a.q_sn = shape->q_sn;
+    a.k_sb = shape->k_sb;
+    a.k_sh = shape->k_sh;
+    a.k_sn = shape->k_sn;
+    a.v_sb = shape->v_sb;
+    a.v_sh = shape->v_sh;
+    a.v_sn = shape->v_sn;
+    a.o_sb = shape->o_sb;
+    a.o_sh = shape->o_sh;
+    a.o_sn = shape->o_sn;
+    a.B = static_cast<int>(shape->B);
+    a.H = static_cast<int>(shape->H);
+    a.Nq = static_cast<int>(shape->Nq);
+    a.Nk = static_cast<int>(shape->Nk);
+    a.d = static_cast<int>(shape->d);
+    a.dtype = static_cast<int>(shape->dtype);
+    a.scale_log2 = scale_log2;
+    a.causal = causal;
+    return clis::launch_attn_bwd(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 clis_status_t clis_get_device_error(uint32_t *code)
 {
     if (!code) return CLIS_ERR_INVALID_ARG;
-    return clis::read_device_error(code);
+    uint32_t fwd = 0, bwd = 0;
+    clis_status_t st = clis::read_device_error(&fwd);
+    if (st == CLIS_ERR_CUDA) return st;
+    if (clis::read_bwd_error(&bwd) != CLIS_OK) return CLIS_ERR_CUDA;
+    *code = fwd | bwd;
+    return *code ? CLIS_ERR_TIMEOUT : CLIS_OK;
 }
 
-clis_status_t clis_clear_device_error(void) { return clis::clear_device_error(); }
+clis_status_t clis_clear_device_error(void)
+{
+    clis_status_t st = clis::clear_device_error();
+    return st != CLIS_OK ? st : clis::clear_bwd_error();
+}
 
 clis_status_t clis_debug_wait_selftest(uint32_t limit_us, clis_stream_t stream)
 {

@@ -82,6 +82,27 @@ clis_status_t launch_chunk_finalize(const ChunkFinalizeArgs &a, cudaStream_t str
 // Returns CLIS_OK, CLIS_ERR_CUDA (tensor-map encode or launch failure).
 clis_status_t launch_attn_fwd(const AttnArgs &a, cudaStream_t stream);
 
+// ---------------------------------------------------------------- backward
+
+struct AttnBwdArgs {
+    const uint16_t *q, *k, *v, *o, *dout;
+    const float *lse2;
+    float *dvec;  // workspace: D_i = dO_i . O_i, [B*H*Nq]
+    uint16_t *dq, *dk, *dv;
+    // dq shares q's strides, dk k's, dv v's, dout o's.
+    int64_t q_sb, q_sh, q_sn, k_sb, k_sh, k_sn, v_sb, v_sh, v_sn, o_sb, o_sh, o_sn;
+    int B, H, Nq, Nk, d;
+    int dtype;
+    float scale_log2;
+    int causal;
+};
+
+// Launches the row-dot, dK/dV and dQ kernels (or zero-fills dK and dV when
+// Nq = 0).  Returns CLIS_OK or CLIS_ERR_CUDA.
+clis_status_t launch_attn_bwd(const AttnBwdArgs &a, cudaStream_t stream);
+clis_status_t read_bwd_error(uint32_t *code);
+clis_status_t clear_bwd_error();
+
 clis_status_t launch_wait_selftest(uint32_t limit_us, cudaStream_t stream);
 clis_status_t read_device_error(uint32_t *code);
 clis_status_t clear_device_error();

@@ -125,6 +125,13 @@ def make_inputs(w: Workload, device="cpu", seed: int | None = None, N: int | Non
     return q, k, v
 
 
+def make_dout(shape, device="cpu", seed: int = 0, dtype=torch.bfloat16, sigma: float = 1.0):
+    """Upstream gradient dO ~ sigma * N(0, 1) of the given [B, H, N, d] shape
+    (the backward's input; a training loss would supply it)."""
+    g = _gen(torch.device(device), seed + 65537)
+    return (torch.randn(tuple(shape), generator=g, device=device) * sigma).to(dtype)
+
+
 def _inject(w: Workload, q, k, v, seed: int) -> None:
     """Plant outlier keys (x outlier_scale, exact in bf16 for a power of two)
     and large V entries (magnitude uniform in [1, v_inject_max], one entry

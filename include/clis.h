@@ -1,5 +1,5 @@
 /*
- * clis.h -- C ABI of the CLiS attention-forward library (libclis.so), sm_103a.
+ * clis.h -- C ABI of the CLiS attention library (libclis.so), sm_103a.
  *
  * CLiS ("CLiS: Plug-and-Play Attention Acceleration for Video Diffusion on
  * TPUs via Certified Stabilization", Tsai et al., 2026) fixes one softmax
@@ -231,6 +231,38 @@ CLIS_API clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void
 CLIS_API clis_status_t clis_attn_chunk_finalize(const clis_shape_t *shape, const float *o_acc,
                                        const float *l_acc, const float *m_acc, void *o,
                                        float *lse2, clis_stream_t stream);
+
+/* Workspace bytes for clis_attn_bwd: one fp32 per query row (B*H*Nq, the
+ * row dots D_i), rounded up to 256.  CLIS_ERR_INVALID_ARG for a NULL or
+ * invalid shape. */
+CLIS_API clis_status_t clis_attn_bwd_workspace_size(const clis_shape_t *shape, size_t *bytes);
+
+/* Attention backward: dQ, dK, dV of L = sum(dout * O) for O = softmax(scale *
+ * Q K^T) V, scale = scale_log2 * ln 2.  The paper's causal LLM training
+ * results (Table 3) run a backward pass but the paper gives none; this is the
+ * plain chain rule through softmax, driven by the forward's row statistic:
+ *   P_ij = exp2(scale_log2 * s_ij - lse2_i),  D_i = dout_i . o_i,
+ *   dS_ij = P_ij (dout_i . v_j - D_i),
+ *   dV_j = sum_i P_ij dout_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j.
+ * lse2 is fixed per row, whichever forward path produced it, so the
+ * backward has no running maximum and no rescaling.
+ *   q, k, v   the forward's inputs (device, shape->dtype)
+ *   o         the forward's output and dout its gradient, both with strides
+ *             shape->o_*
+ *   lse2      device fp32 [B*H*Nq], from clis_attn_fwd (or
+ *             clis_attn_chunk_finalize) with the same q, k, scale_log2, causal
+ *   dq, dk, dv  device outputs, same dtype; dq has strides shape->q_*, dk
+ *             shape->k_*, dv shape->v_*.  Every element is written once
+ *             (deterministic: no atomics).
+ *   workspace device buffer of at least clis_attn_bwd_workspace_size() bytes,
+ *             16-byte aligned (CLIS_ERR_WORKSPACE otherwise)
+ *   causal    0 or 1; 1 requires Nq == Nk
+ * Nq == 0 writes dK = dV = 0.  Errors as clis_attn_fwd. */
+CLIS_API clis_status_t clis_attn_bwd(const clis_shape_t *shape, const void *q, const void *k,
+                                     const void *v, const void *o, const void *dout,
+                                     const float *lse2, void *dq, void *dk, void *dv,
+                                     float scale_log2, int causal, void *workspace,
+                                     size_t ws_bytes, clis_stream_t stream);
 
 /* Static description of a status code (never NULL). */
 CLIS_API const char *clis_status_string(clis_status_t status);

@@ -27,7 +27,8 @@ def test_header_declares_the_boundary():
     names = _declared_symbols()
     for n in ("clis_certify_workspace_size", "clis_certify", "clis_attn_fwd", "clis_status_string",
               "clis_get_device_error", "clis_clear_device_error", "clis_debug_wait_selftest",
-              "clis_attn_fwd_chunk", "clis_attn_chunk_finalize", "clis_certify_noalloc"):
+              "clis_attn_fwd_chunk", "clis_attn_chunk_finalize", "clis_certify_noalloc",
+              "clis_attn_bwd_workspace_size", "clis_attn_bwd"):
         assert n in names
 
 
@@ -151,6 +152,44 @@ def test_chunk_entry_points_reject_bad_arguments(clis):
     assert lib.clis_attn_chunk_finalize(ctypes.byref(s), vp(FAKE), vp(FAKE), vp(FAKE), vp(0), None, None) == 1
     s2 = _shape(clis, d=80)
     assert lib.clis_attn_chunk_finalize(ctypes.byref(s2), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, None) == 2
+
+
+def _bwd(clis, shape=None, ws_bytes=1 << 20, scale=0.1, causal=0, **ptrs):
+    lib = clis.load_library()
+    vp = ctypes.c_void_p
+    s = shape if shape is not None else _shape(clis)
+    args = [vp(ptrs.get(n, FAKE)) for n in ("q", "k", "v", "o", "do", "lse2", "dq", "dk", "dv")]
+    return lib.clis_attn_bwd(ctypes.byref(s), *args, scale, causal, vp(ptrs.get("ws", FAKE)), ws_bytes, None)
+
+
+def test_bwd_workspace_size(clis):
+    assert clis.clis_attn_bwd_workspace_size(_shape(clis, Nq=300)) == 2560  # 2 heads x 300 rows x 4 B -> 256s
+    assert clis.clis_attn_bwd_workspace_size(_shape(clis, Nq=0)) == 0
+    with pytest.raises(clis.ClisError):
+        clis.clis_attn_bwd_workspace_size(_shape(clis, d=96))
+
+
+def test_bwd_rejects_bad_arguments(clis):
+    INV, UNSUP, MIS, WS = 1, 2, 3, 4
+    for name in ("q", "k", "v", "o", "do", "lse2", "dq", "dk", "dv"):
+        assert _bwd(clis, **{name: 0}) == INV, name
+    assert _bwd(clis, scale=0.0) == INV
+    assert _bwd(clis, scale=float("inf")) == INV
+    assert _bwd(clis, causal=2) == INV
+    assert _bwd(clis, _shape(clis, Nq=300, Nk=200), causal=1) == UNSUP
+    assert _bwd(clis, _shape(clis, d=256)) == UNSUP
+    bad = _shape(clis)
+    bad.dtype = 3
+    assert _bwd(clis, bad) == INV
+    assert _bwd(clis, dq=FAKE + 8) == MIS
+    assert _bwd(clis, do=FAKE + 2) == MIS
+    assert _bwd(clis, lse2=FAKE + 2) == MIS
+    assert _bwd(clis, ws=0) == WS
+    assert _bwd(clis, ws_bytes=2559) == WS
+    assert _bwd(clis, ws=FAKE + 8) == WS
+    s = _shape(clis)
+    s.o_sn = 132
+    assert _bwd(clis, s) == MIS
 
 
 def test_binding_has_no_cpu_fallback(clis):

@@ -1,0 +1,55 @@
+"""Where the backward parity tolerance comes from (no GPU needed).
+
+The backward kernels compute in fp32 except at three points: P and dS are
+rounded to the input format (bf16) before they enter the matmuls, O enters
+D_i = dO_i . O_i as the forward's bf16 output, and dQ, dK, dV are rounded to
+bf16 once at the end.  This test applies exactly those roundings to an fp64
+computation and measures the error against the oracle on the workload
+distributions: it must stay within half of the GPU tests' bounds
+(gpu_util.GRAD_TOL), leaving the other half for fp32 summation order and the
+hardware exp2.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import GRAD_TOL, grad_errors
+
+
+def _bf(x):
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("causal,N,qs,ks,bs", [
+    (True, 512, 1.0, 1.0, math.sqrt(2.0)),   # causal LLM distributions
+    (False, 1024, 0.5, 0.5, 2.0),           # 480p / 720p DiT distributions
+    (False, 384, 1.0, 1.0, 2.0),
+])
+def test_rounding_alone_uses_at_most_half_the_bound(oracle_mod, causal, N, qs, ks, bs, seed):
+    rng = np.random.default_rng(1000 * seed + N + int(causal))
+    d = 128
+    scale = 1.0 / math.sqrt(d)
+    bias = rng.standard_normal(d) * bs
+    q = _bf(rng.standard_normal((N, d)) * qs)
+    k = _bf(rng.standard_normal((N, d)) * ks + bias)
+    v = _bf(rng.standard_normal((N, d)))
+    g = _bf(rng.standard_normal((N, d)))
+    ref = oracle_mod.attention_bwd(q[None], k[None], v[None], g[None], scale, causal=causal)
+
+    s = scale * (q @ k.T)
+    if causal:
+        s = np.where(np.tril(np.ones((N, N))) > 0, s, -np.inf)
+    P = np.exp(s - s.max(axis=1, keepdims=True))
+    P /= P.sum(axis=1, keepdims=True)
+    O = _bf(P @ v)                                   # forward output, bf16
+    dV = _bf(_bf(P).T @ g)                           # P rounded for the matmul
+    dS = _bf(P * (g @ v.T - (g * O).sum(axis=1, keepdims=True)))
+    dQ = _bf(scale * (dS @ k))
+    dK = _bf(scale * (dS.T @ q))
+    for got, r, name in ((dQ, ref[0], "dq"), (dK, ref[1], "dk"), (dV, ref[2], "dv")):
+        mx, mn = grad_errors(got[None], r)
+        assert mx.max() <= GRAD_TOL[name][0] / 2, (name, mx.max())
+        assert mn.max() <= GRAD_TOL[name][1] / 2, (name, mn.max())
