@@ -31,7 +31,7 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from certified_fixed_stabilizer_gb300.workloads import WORKLOADS, make_inputs, sample_rows  # noqa: E402
+from certified_fixed_stabilizer_gb300.workloads import WORKLOADS, make_dout, make_inputs, sample_rows  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "attention fwd TFLOP/s (BF16, 1xGB300); CLiS step = certification + fused attention (AUTO)"
@@ -56,8 +56,10 @@ def parse():
     ap.add_argument("--variant", default="auto", choices=["auto", "online", "certified", "online_lazy"])
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"],
                     help="element type of Q, K, V, P and O (fp16 certifies with the FP16 exp2 budget)")
-    ap.add_argument("--no-extras", action="store_true",
-                    help="skip the online-variant, e2e and CPU-baseline legs (profiling runs)")
+    ap.add_argument("--extras", default="all", choices=["all", "none", "backward"],
+                    help="legs after the headline step: all (online variants, ring-step chunks, backward, e2e, "
+                         "CPU baseline), none, or only the backward (profiling runs)")
+    ap.add_argument("--no-extras", action="store_true", help="same as --extras none")
     return ap.parse_args()
 
 
@@ -323,7 +325,8 @@ def main():
         "clocks": clocks,
     }
 
-    if not args.no_extras:
+    extras = "none" if args.no_extras else args.extras
+    if extras == "all":
         # Online-softmax baseline (same kernel skeleton, every head on the online path).
         on_total, _, on_attn = timed_loop("online", args.steps, args.warmup)
         line["online"] = {"value": flops / (statistics.mean(on_attn) * 1e-3) / 1e12, "unit": "TFLOP/s",
@@ -368,6 +371,41 @@ def main():
             chunked["certified_speedup_vs_online"] = chunked["online"]["ms"] / chunked["certified"]["ms"]
             line["chunked"] = chunked
             del o_acc, l_acc, m_acc
+    if extras in ("all", "backward"):
+        # Backward (clis_attn_bwd: row dots, dK/dV kernel, dQ kernel) on the same
+        # inputs, from a forward that also wrote lse2, for a seeded dO.  FLOPs
+        # are the backward's five matmuls: 2.5 x the forward's count.
+        lse2 = torch.empty(heads * w.N, dtype=torch.float32, device=dev)
+        clis.clis_certify(q, k, v, sl2, kbar=kbar, certs=certs, workspace=wsp, mu=mu, exp_fmt=exp_fmt)
+        clis.clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=w.causal, variant=args.variant, out=out,
+                           mu=mu, lse2=lse2)
+        dout = make_dout(q.shape, device=dev, dtype=dt)
+        dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
+        bws = torch.empty(max(256, clis.clis_attn_bwd_workspace_size(clis.make_shape(q, k, v, out))),
+                          dtype=torch.uint8, device=dev)
+
+        def bwd_step():
+            clis.clis_attn_bwd(q, k, v, out, dout, lse2, sl2, causal=w.causal, dq=dq, dk=dk, dv=dv, workspace=bws)
+
+        for _ in range(args.warmup):
+            bwd_step()
+        torch.cuda.synchronize()
+        bev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for e0, e1 in bev:
+            if flush_buf is not None:
+                flush_buf.zero_()
+            e0.record(stream)
+            bwd_step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        bwd_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in bev)
+        bwd_tf = 2.5 * flops / (bwd_ms * 1e-3) / 1e12
+        line["backward"] = {"value": bwd_tf, "unit": "TFLOP/s", "ms": bwd_ms, "frac_of_peak": bwd_tf / peak_tf,
+                            "launches_per_step": 3, "flops": "five matmuls (2.5x the forward's count)",
+                            "fwd_plus_bwd_ms": attn_avg_ms + cert_avg_ms + bwd_ms}
+        del dout, dq, dk, dv, bws, lse2
+    if extras == "all":
         # End to end through the public call (clis.attention) with pinned host
         # buffers: every step copies Q, K, V in, computes and copies O out; the
         # call pipelines head groups over three streams.
