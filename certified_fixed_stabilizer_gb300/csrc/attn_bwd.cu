@@ -64,11 +64,14 @@ struct BCfg {
     // dK/dV: K and V resident, (Q, dO) pairs through QSTAGE stages.
     static constexpr int QSTAGE = (D == 128) ? 2 : 4;
     static constexpr int KV_SMEM = 2 * TILE_BYTES + QSTAGE * 2 * TILE_BYTES + 1024;
-    // dQ: Q and dO resident, K and V tiles through a KSLOT ring.  Five slots at
-    // D = 128: the slot of K_{j+1} is that of V_{j-2}, long free, and V_{j+1}
-    // lands in K_{j-1}'s slot, freed by dQ_{j-1} three matmuls before use.
-    static constexpr int KSLOT = (D == 128) ? 5 : 8;
-    static constexpr int Q_SMEM = 2 * TILE_BYTES + KSLOT * TILE_BYTES + 1024;
+    // dQ: Q and dO resident; K and V tiles through two rings sized by how long
+    // each lives.  K_j is read by S_j and again by dQ_j, issued in the next
+    // step, so K_{j+1} takes the slot of K_{j-2} (KRING = 3, freed one and a half
+    // steps before it is needed); V_j is read only by dP_j, so V_{j+1} takes the
+    // slot of V_{j-1} (VRING = 2, freed two steps before).
+    static constexpr int KRING = (D == 128) ? 3 : 4;
+    static constexpr int VRING = (D == 128) ? 2 : 4;
+    static constexpr int Q_SMEM = 2 * TILE_BYTES + (KRING + VRING) * TILE_BYTES + 1024;
     // TMEM columns (512 allocated).
     static constexpr uint32_t TM_ST = 0, TM_DPT = 128, TM_DV = 256, TM_DK = 256 + D;  // dK/dV kernel
     static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_DP = 256, TM_DQ = 384;       // dQ kernel
@@ -307,39 +310,78 @@ __device__ void kv_mma(const BParams &p, KCtl<D> &c, uint32_t tmem, uint32_t sK,
     const uint64_t qd_mn = sdesc_sw128(sQS, C::BOX_BYTES, 1024);              // Q as MN-major B
     const uint64_t dod_k = sdesc_sw128(sQS + C::TILE_BYTES, 16, 1024);        // dO as K-major B
     const uint64_t dod_mn = sdesc_sw128(sQS + C::TILE_BYTES, C::BOX_BYTES, 1024);
+    auto stage_off = [](uint32_t m) -> uint64_t {
+        return (static_cast<uint64_t>(m % C::QSTAGE) * 2 * C::TILE_BYTES) >> 4;
+    };
     uint32_t n = 0;
     int w = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
         const KTile T = decode_ktile<CAUSAL>(p, tile);
         if (!mbar_wait_warp(smem_u32(&c.kv_full), w & 1, ab, err, kErrMma)) goto abort;
+        // First step of the tile: S^T and dP^T.
+        if (!mbar_wait_warp(smem_u32(&c.qs_full[n % C::QSTAGE]), (n / C::QSTAGE) & 1, ab, err, kErrMma)) goto abort;
+        tc_fence_after();
+        if (leader) {
+            issue_scores<D, DT>(tmem + C::TM_ST, kd, qd_k + stage_off(n));  // S^T = K Q^T
+            umma_commit(smem_u32(&c.s_full));
+            issue_scores<D, DT>(tmem + C::TM_DPT, vd, dod_k + stage_off(n));  // dP^T = V dO^T
+            umma_commit(smem_u32(&c.dp_full));
+            if (T.nq == 1) umma_commit(smem_u32(&c.kv_empty));
+        }
+        __syncwarp();
         for (int i = 0; i < T.nq; i++, n++) {
-            const uint32_t s = n % C::QSTAGE;
-            const uint64_t so = (static_cast<uint64_t>(s) * 2 * C::TILE_BYTES) >> 4;
-            if (!mbar_wait_warp(smem_u32(&c.qs_full[s]), (n / C::QSTAGE) & 1, ab, err, kErrMma)) goto abort;
-            tc_fence_after();
-            if (leader) {
-                issue_scores<D, DT>(tmem + C::TM_ST, kd, qd_k + so);  // S^T = K Q^T
-                umma_commit(smem_u32(&c.s_full));
-                issue_scores<D, DT>(tmem + C::TM_DPT, vd, dod_k + so);  // dP^T = V dO^T
-                umma_commit(smem_u32(&c.dp_full));
-                if (i == T.nq - 1) umma_commit(smem_u32(&c.kv_empty));
-            }
-            __syncwarp();
+            const bool has_next = i + 1 < T.nq;
+            const uint32_t nx = n + 1;
             // The previous tile's epilogue must have read dV and dK before they restart.
             if (i == 0 && w > 0)
                 if (!mbar_wait_warp(smem_u32(&c.acc_free), (w - 1) & 1, ab, err, kErrMma)) goto abort;
             if (!mbar_wait_warp(smem_u32(&c.p_full), n & 1, ab, err, kErrMma)) goto abort;
             tc_fence_after();
-            if (leader) issue_accum<D, DT>(tmem + C::TM_DV, tmem + C::TM_ST, dod_mn + so, i > 0 ? 1u : 0u);
+            if (leader) issue_accum<D, DT>(tmem + C::TM_DV, tmem + C::TM_ST, dod_mn + stage_off(n), i > 0 ? 1u : 0u);
             __syncwarp();
+            // S^T of the next step goes in as soon as its Q tile is there: the S^T
+            // columns hold P^T(n), which dV (issued just above) reads first, and the
+            // softmax warps then overlap its exponentials with dK and the next dP^T.
+            // If the tile has not landed yet, dK goes first (no blocking wait here).
+            bool s_next = false;
+            if (has_next &&
+                __all_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&c.qs_full[nx % C::QSTAGE]), (nx / C::QSTAGE) & 1))) {
+                tc_fence_after();
+                if (leader) {
+                    issue_scores<D, DT>(tmem + C::TM_ST, kd, qd_k + stage_off(nx));
+                    umma_commit(smem_u32(&c.s_full));
+                }
+                __syncwarp();
+                s_next = true;
+            }
             if (!mbar_wait_warp(smem_u32(&c.ds_full), n & 1, ab, err, kErrMma)) goto abort;
             tc_fence_after();
             if (leader) {
-                issue_accum<D, DT>(tmem + C::TM_DK, tmem + C::TM_DPT, qd_mn + so, i > 0 ? 1u : 0u);
-                umma_commit(smem_u32(&c.qs_empty[s]));
-                if (i == T.nq - 1) umma_commit(smem_u32(&c.acc_full));
+                issue_accum<D, DT>(tmem + C::TM_DK, tmem + C::TM_DPT, qd_mn + stage_off(n), i > 0 ? 1u : 0u);
+                umma_commit(smem_u32(&c.qs_empty[n % C::QSTAGE]));
+                if (!has_next) umma_commit(smem_u32(&c.acc_full));
             }
             __syncwarp();
+            if (has_next) {
+                if (!s_next) {
+                    if (!mbar_wait_warp(smem_u32(&c.qs_full[nx % C::QSTAGE]), (nx / C::QSTAGE) & 1, ab, err,
+                                        kErrMma))
+                        goto abort;
+                    tc_fence_after();
+                    if (leader) {
+                        issue_scores<D, DT>(tmem + C::TM_ST, kd, qd_k + stage_off(nx));
+                        umma_commit(smem_u32(&c.s_full));
+                    }
+                    __syncwarp();
+                }
+                // dP^T of the next step after dK, which read dS^T(n) from the same columns.
+                if (leader) {
+                    issue_scores<D, DT>(tmem + C::TM_DPT, vd, dod_k + stage_off(nx));
+                    umma_commit(smem_u32(&c.dp_full));
+                    if (i + 2 == T.nq) umma_commit(smem_u32(&c.kv_empty));
+                }
+                __syncwarp();
+            }
         }
     }
     return;
@@ -513,7 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 struct __align__(16) QCtl {
     uint64_t qo_full, qo_empty;
-    uint64_t kv_full[BCfg<D>::KSLOT], kv_empty[BCfg<D>::KSLOT];
+    uint64_t k_full[BCfg<D>::KRING], k_empty[BCfg<D>::KRING];
+    uint64_t v_full[BCfg<D>::VRING], v_empty[BCfg<D>::VRING];
     uint64_t s_full[2], dp_full, ds_full, acc_full, acc_free, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -521,7 +564,8 @@ struct __align__(16) QCtl {
 
 template <int D, bool CAUSAL, int DT>
 __device__ void q_producer(const BParams &p, QCtl<D> &c, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
-                           const CUtensorMap *tm_v, const CUtensorMap *tm_do, uint32_t sQ, uint32_t sDO, uint32_t sR)
+                           const CUtensorMap *tm_v, const CUtensorMap *tm_do, uint32_t sQ, uint32_t sDO, uint32_t sK,
+                           uint32_t sV)
 {
     using C = BCfg<D>;
     volatile int *ab = &c.abort_flag;
@@ -529,7 +573,7 @@ __device__ void q_producer(const BParams &p, QCtl<D> &c, const CUtensorMap *tm_q
     const bool leader = elect_one();
     const uint64_t pol_keep = policy_evict_last();   // K, V: read by every query block of the head
     const uint64_t pol_once = policy_evict_first();  // Q, dO: read by one work tile
-    uint32_t it = 0;
+    uint32_t nk = 0, nv = 0;  // K and V tiles issued (one of each per step)
     int w = 0, q_issued = -1;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
         const QTile T = decode_qtile<CAUSAL>(p, tile);
@@ -546,33 +590,47 @@ __device__ void q_producer(const BParams &p, QCtl<D> &c, const CUtensorMap *tm_q
         __syncwarp();
         q_issued = w;
         for (int j = 0; j < T.nkv; j++) {
+            const uint32_t ks = nk % C::KRING;
+            if (!mbar_wait_warp(smem_u32(&c.k_empty[ks]), ((nk / C::KRING) & 1) ^ 1, ab, err, kErrProducer))
+                goto abort;
+            if (leader) {
+                const uint32_t bar = smem_u32(&c.k_full[ks]);
+                mbar_arrive_expect_tx(bar, C::TILE_BYTES);
 #pragma unroll
-            for (int kv = 0; kv < 2; kv++) {
-                const uint32_t slot = it % C::KSLOT;
-                if (!mbar_wait_warp(smem_u32(&c.kv_empty[slot]), ((it / C::KSLOT) & 1) ^ 1, ab, err, kErrProducer))
-                    goto abort;
-                if (leader) {
-                    const uint32_t bar = smem_u32(&c.kv_full[slot]);
-                    mbar_arrive_expect_tx(bar, C::TILE_BYTES);
-#pragma unroll
-                    for (int bx = 0; bx < C::NBOX; bx++)
-                        tma_load_4d_hint(sR + slot * C::TILE_BYTES + bx * C::BOX_BYTES, kv ? tm_v : tm_k, bar,
-                                         bx * 64, j * BN, T.h, T.b, pol_keep);
-                }
-                __syncwarp();
-                ++it;
+                for (int bx = 0; bx < C::NBOX; bx++)
+                    tma_load_4d_hint(sK + ks * C::TILE_BYTES + bx * C::BOX_BYTES, tm_k, bar, bx * 64, j * BN, T.h,
+                                     T.b, pol_keep);
             }
+            __syncwarp();
+            ++nk;
+            const uint32_t vs = nv % C::VRING;
+            if (!mbar_wait_warp(smem_u32(&c.v_empty[vs]), ((nv / C::VRING) & 1) ^ 1, ab, err, kErrProducer))
+                goto abort;
+            if (leader) {
+                const uint32_t bar = smem_u32(&c.v_full[vs]);
+                mbar_arrive_expect_tx(bar, C::TILE_BYTES);
+#pragma unroll
+                for (int bx = 0; bx < C::NBOX; bx++)
+                    tma_load_4d_hint(sV + vs * C::TILE_BYTES + bx * C::BOX_BYTES, tm_v, bar, bx * 64, j * BN, T.h,
+                                     T.b, pol_keep);
+            }
+            __syncwarp();
+            ++nv;
         }
     }
     return;
 abort:
-    for (uint32_t k = (it > C::KSLOT ? it - C::KSLOT : 0); k < it; k++)
-        drain_wait(smem_u32(&c.kv_full[k % C::KSLOT]), (k / C::KSLOT) & 1);
+    // Let every copy already issued land before the CTA leaves.
+    for (uint32_t k = (nk > C::KRING ? nk - C::KRING : 0); k < nk; k++)
+        drain_wait(smem_u32(&c.k_full[k % C::KRING]), (k / C::KRING) & 1);
+    for (uint32_t k = (nv > C::VRING ? nv - C::VRING : 0); k < nv; k++)
+        drain_wait(smem_u32(&c.v_full[k % C::VRING]), (k / C::VRING) & 1);
     if (q_issued >= 0) drain_wait(smem_u32(&c.qo_full), q_issued & 1);
 }
 
 template <int D, bool CAUSAL, int DT>
-__device__ void q_mma(const BParams &p, QCtl<D> &c, uint32_t tmem, uint32_t sQ, uint32_t sDO, uint32_t sR)
+__device__ void q_mma(const BParams &p, QCtl<D> &c, uint32_t tmem, uint32_t sQ, uint32_t sDO, uint32_t sK,
+                      uint32_t sV)
 {
     using C = BCfg<D>;
     volatile int *ab = &c.abort_flag;
@@ -580,26 +638,25 @@ __device__ void q_mma(const BParams &p, QCtl<D> &c, uint32_t tmem, uint32_t sQ, 
     const bool leader = elect_one();
     const uint64_t qd = sdesc_sw128(sQ, 16, 1024);
     const uint64_t dod = sdesc_sw128(sDO, 16, 1024);
-    const uint64_t rd_k = sdesc_sw128(sR, 16, 1024);             // ring tile as K-major B (K or V)
-    const uint64_t rd_mn = sdesc_sw128(sR, C::BOX_BYTES, 1024);  // ring tile as MN-major B (K in dQ += dS K)
+    const uint64_t kd_k = sdesc_sw128(sK, 16, 1024);             // K slot as K-major B (S = Q K^T)
+    const uint64_t kd_mn = sdesc_sw128(sK, C::BOX_BYTES, 1024);  // K slot as MN-major B (dQ += dS K)
+    const uint64_t vd_k = sdesc_sw128(sV, 16, 1024);             // V slot as K-major B (dP = dO V^T)
     auto slot_off = [](uint32_t s) -> uint64_t { return (static_cast<uint64_t>(s) * C::TILE_BYTES) >> 4; };
-    uint32_t it = 0, n = 0;
+    uint32_t n = 0;  // global step index; K_n and V_n are the rings' n-th tiles
     int w = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
         const QTile T = decode_qtile<CAUSAL>(p, tile);
         if (!mbar_wait_warp(smem_u32(&c.qo_full), w & 1, ab, err, kErrMma)) goto abort;
-        uint32_t kprev = 0;
         for (int j = 0; j < T.nkv; j++, n++) {
             // S_j = Q K_j^T into S[n & 1].
-            const uint32_t ks = it % C::KSLOT;
-            if (!mbar_wait_warp(smem_u32(&c.kv_full[ks]), (it / C::KSLOT) & 1, ab, err, kErrMma)) goto abort;
+            const uint32_t ks = n % C::KRING;
+            if (!mbar_wait_warp(smem_u32(&c.k_full[ks]), (n / C::KRING) & 1, ab, err, kErrMma)) goto abort;
             tc_fence_after();
             if (leader) {
-                issue_scores<D, DT>(tmem + ((n & 1) ? C::TM_S1 : C::TM_S0), qd, rd_k + slot_off(ks));
+                issue_scores<D, DT>(tmem + ((n & 1) ? C::TM_S1 : C::TM_S0), qd, kd_k + slot_off(ks));
                 umma_commit(smem_u32(&c.s_full[n & 1]));
             }
             __syncwarp();
-            ++it;
             // dQ += dS_{j-1} K_{j-1} once the softmax warps stored dS_{j-1}.
             if (j > 0) {
                 if (j == 1 && w > 0)
@@ -607,32 +664,32 @@ __device__ void q_mma(const BParams &p, QCtl<D> &c, uint32_t tmem, uint32_t sQ, 
                 if (!mbar_wait_warp(smem_u32(&c.ds_full), (n - 1) & 1, ab, err, kErrMma)) goto abort;
                 tc_fence_after();
                 if (leader) {
-                    issue_accum<D, DT>(tmem + C::TM_DQ, tmem + C::TM_DP, rd_mn + slot_off(kprev), j > 1 ? 1u : 0u);
-                    umma_commit(smem_u32(&c.kv_empty[kprev]));
+                    issue_accum<D, DT>(tmem + C::TM_DQ, tmem + C::TM_DP, kd_mn + slot_off((n - 1) % C::KRING),
+                                       j > 1 ? 1u : 0u);
+                    umma_commit(smem_u32(&c.k_empty[(n - 1) % C::KRING]));
                 }
                 __syncwarp();
             }
             // dP_j = dO V_j^T (after dQ has read dS_{j-1} from the same columns).
-            const uint32_t vs = it % C::KSLOT;
-            if (!mbar_wait_warp(smem_u32(&c.kv_full[vs]), (it / C::KSLOT) & 1, ab, err, kErrMma)) goto abort;
+            const uint32_t vs = n % C::VRING;
+            if (!mbar_wait_warp(smem_u32(&c.v_full[vs]), (n / C::VRING) & 1, ab, err, kErrMma)) goto abort;
             tc_fence_after();
             if (leader) {
-                issue_scores<D, DT>(tmem + C::TM_DP, dod, rd_k + slot_off(vs));
+                issue_scores<D, DT>(tmem + C::TM_DP, dod, vd_k + slot_off(vs));
                 umma_commit(smem_u32(&c.dp_full));
-                umma_commit(smem_u32(&c.kv_empty[vs]));
+                umma_commit(smem_u32(&c.v_empty[vs]));
                 if (j == T.nkv - 1) umma_commit(smem_u32(&c.qo_empty));
             }
             __syncwarp();
-            ++it;
-            kprev = ks;
         }
         if (T.nkv == 1 && w > 0)
             if (!mbar_wait_warp(smem_u32(&c.acc_free), (w - 1) & 1, ab, err, kErrMma)) goto abort;
         if (!mbar_wait_warp(smem_u32(&c.ds_full), (n - 1) & 1, ab, err, kErrMma)) goto abort;
         tc_fence_after();
         if (leader) {
-            issue_accum<D, DT>(tmem + C::TM_DQ, tmem + C::TM_DP, rd_mn + slot_off(kprev), T.nkv > 1 ? 1u : 0u);
-            umma_commit(smem_u32(&c.kv_empty[kprev]));
+            issue_accum<D, DT>(tmem + C::TM_DQ, tmem + C::TM_DP, kd_mn + slot_off((n - 1) % C::KRING),
+                               T.nkv > 1 ? 1u : 0u);
+            umma_commit(smem_u32(&c.k_empty[(n - 1) % C::KRING]));
             umma_commit(smem_u32(&c.acc_full));
         }
         __syncwarp();
@@ -731,15 +788,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t dsmem[];
     __shared__ QCtl<D> ctl;
     const uint32_t sbase = (smem_u32(dsmem) + 1023u) & ~1023u;
-    const uint32_t sQ = sbase, sDO = sbase + C::TILE_BYTES, sR = sbase + 2 * C::TILE_BYTES;
+    const uint32_t sQ = sbase, sDO = sbase + C::TILE_BYTES, sK = sbase + 2 * C::TILE_BYTES;
+    const uint32_t sV = sK + C::KRING * C::TILE_BYTES;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&ctl.qo_full), 1);
         mbar_init(smem_u32(&ctl.qo_empty), 1);
-        for (int s = 0; s < C::KSLOT; s++) {
-            mbar_init(smem_u32(&ctl.kv_full[s]), 1);
-            mbar_init(smem_u32(&ctl.kv_empty[s]), 1);
+        for (int s = 0; s < C::KRING; s++) {
+            mbar_init(smem_u32(&ctl.k_full[s]), 1);
+            mbar_init(smem_u32(&ctl.k_empty[s]), 1);
+        }
+        for (int s = 0; s < C::VRING; s++) {
+            mbar_init(smem_u32(&ctl.v_full[s]), 1);
+            mbar_init(smem_u32(&ctl.v_empty[s]), 1);
         }
         mbar_init(smem_u32(&ctl.s_full[0]), 1);
         mbar_init(smem_u32(&ctl.s_full[1]), 1);
@@ -768,9 +830,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 8)
         q_softmax<D, CAUSAL, DT>(p, ctl, tmem, warp, lane);
     else if (warp == 8)
-        q_producer<D, CAUSAL, DT>(p, ctl, &tm_q, &tm_k, &tm_v, &tm_do, sQ, sDO, sR);
+        q_producer<D, CAUSAL, DT>(p, ctl, &tm_q, &tm_k, &tm_v, &tm_do, sQ, sDO, sK, sV);
     else
-        q_mma<D, CAUSAL, DT>(p, ctl, tmem, sQ, sDO, sR);
+        q_mma<D, CAUSAL, DT>(p, ctl, tmem, sQ, sDO, sK, sV);
     tc_fence_before();
     __syncthreads();
     if (warp == 9) {
