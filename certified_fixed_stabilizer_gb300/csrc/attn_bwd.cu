@@ -55,15 +55,22 @@ constexpr unsigned kErrProducer = 1u << 16;
 constexpr unsigned kErrMma = 1u << 17;
 constexpr unsigned kErrSoftmax = 1u << 18;
 constexpr unsigned kErrDrain = 1u << 20;
+constexpr unsigned kErrLayout = 1u << 21;  // shared-memory allocation too small for the aligned layout
 
 template <int D>
 struct BCfg {
     static constexpr int NBOX = D / 64;
     static constexpr int BOX_BYTES = 128 * 128;          // 128 rows x 128 bytes
     static constexpr int TILE_BYTES = NBOX * BOX_BYTES;  // one 128-row tile of Q, K, V or dO
-    // dK/dV: K and V resident, (Q, dO) pairs through QSTAGE stages.
-    static constexpr int QSTAGE = (D == 128) ? 2 : 4;
-    static constexpr int KV_SMEM = 2 * TILE_BYTES + QSTAGE * 2 * TILE_BYTES + 1024;
+    // dK/dV: K and V resident; Q and dO stream through rings of their own.  Q_n
+    // is read by S^T_n and, a step later, by dK_n, so it gets three slots (the
+    // tile of step n+1 is loaded while steps n-1 and n still hold theirs); dO_n
+    // is done after dV_n and gets two.  Shared memory: the tiles, then the
+    // control block (barriers and two slots of -lse2 / -D), 231.6 KB at D = 128.
+    static constexpr int QRING = (D == 128) ? 3 : 4;
+    static constexpr int ORING = (D == 128) ? 2 : 3;
+    static constexpr int LSLOT = 2;
+    static constexpr int KV_TILES = (2 + QRING + ORING) * TILE_BYTES;
     // dQ: Q and dO resident; K and V tiles through two rings sized by how long
     // each lives.  K_j is read by S_j and again by dQ_j, issued in the next
     // step, so K_{j+1} takes the slot of K_{j-2} (KRING = 3, freed one and a half
@@ -88,6 +95,7 @@ struct BParams {
     int num_tiles;
     float scale_log2;
     float scale;     // softmax scale = scale_log2 * ln 2
+    int smem_bytes;  // dynamic shared memory of the launch
 };
 
 // Wait ignoring the abort flag (used only while draining after an abort).
@@ -224,21 +232,23 @@ __device__ __forceinline__ void store_row(uint32_t t_src, float mul, uint16_t *d
 
 template <int D>
 struct __align__(16) KCtl {
-    // Per stage, for the 128 query rows of the block: -lse2_i and -D_i (rows
-    // past Nq: -inf and 0, so P = dS = 0 there).  First in the struct so the
-    // softmax warps' float4 reads are 16-byte aligned.
-    float nlse[BCfg<D>::QSTAGE][BN], nd[BCfg<D>::QSTAGE][BN];
+    // Per slot, for the 128 query rows of a block: -lse2_i and -D_i (rows past
+    // Nq: -inf and 0, so P = dS = 0 there).  Slot n % LSLOT serves step n.
+    float nlse[BCfg<D>::LSLOT][BN], nd[BCfg<D>::LSLOT][BN];
     uint64_t kv_full, kv_empty;
-    uint64_t qs_full[BCfg<D>::QSTAGE], qs_empty[BCfg<D>::QSTAGE];
+    uint64_t q_full[BCfg<D>::QRING], q_empty[BCfg<D>::QRING];
+    uint64_t o_full[BCfg<D>::ORING], o_empty[BCfg<D>::ORING];
+    uint64_t ls_full[BCfg<D>::LSLOT], ls_empty[BCfg<D>::LSLOT];
     uint64_t s_full, dp_full, p_full, ds_full, acc_full, acc_free, drain;
     uint32_t tmem_base;
     int abort_flag;
 };
 
+
 template <int D, bool CAUSAL, int DT>
 __device__ void kv_producer(const BParams &p, KCtl<D> &c, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                             const CUtensorMap *tm_v, const CUtensorMap *tm_do, uint32_t sK, uint32_t sV,
-                            uint32_t sQS, int lane)
+                            uint32_t sQ, uint32_t sO, int lane)
 {
     using C = BCfg<D>;
     volatile int *ab = &c.abort_flag;
@@ -246,7 +256,7 @@ __device__ void kv_producer(const BParams &p, KCtl<D> &c, const CUtensorMap *tm_
     const bool leader = elect_one();
     const uint64_t pol_once = policy_evict_first();  // K, V: read by one work tile
     const uint64_t pol_keep = policy_evict_last();   // Q, dO: read by every key block of the head
-    uint32_t n = 0;
+    uint32_t nq = 0, no = 0;  // Q and dO tiles issued (one of each per step)
     int w = 0, kv_issued = -1;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
         const KTile T = decode_ktile<CAUSAL>(p, tile);
@@ -262,43 +272,65 @@ __device__ void kv_producer(const BParams &p, KCtl<D> &c, const CUtensorMap *tm_
         }
         __syncwarp();
         kv_issued = w;
-        for (int i = 0; i < T.nq; i++, n++) {
-            const uint32_t s = n % C::QSTAGE;
-            if (!mbar_wait_warp(smem_u32(&c.qs_empty[s]), ((n / C::QSTAGE) & 1) ^ 1, ab, err, kErrProducer))
-                goto abort;
+        for (int i = 0; i < T.nq; i++) {
+            const uint32_t n = nq;  // global step index
             const int qb = T.q0 + i;
+            const uint32_t qs = n % C::QRING;
+            if (!mbar_wait_warp(smem_u32(&c.q_empty[qs]), ((n / C::QRING) & 1) ^ 1, ab, err, kErrProducer))
+                goto abort;
+            if (leader) {
+                const uint32_t bar = smem_u32(&c.q_full[qs]);
+                mbar_arrive_expect_tx(bar, C::TILE_BYTES);
+#pragma unroll
+                for (int bx = 0; bx < C::NBOX; bx++)
+                    tma_load_4d_hint(sQ + qs * C::TILE_BYTES + bx * C::BOX_BYTES, tm_q, bar, bx * 64, qb * BN, T.h,
+                                     T.b, pol_keep);
+            }
+            __syncwarp();
+            ++nq;
+            const uint32_t os = n % C::ORING;
+            if (!mbar_wait_warp(smem_u32(&c.o_empty[os]), ((n / C::ORING) & 1) ^ 1, ab, err, kErrProducer))
+                goto abort;
+            if (leader) {
+                const uint32_t bar = smem_u32(&c.o_full[os]);
+                mbar_arrive_expect_tx(bar, C::TILE_BYTES);
+#pragma unroll
+                for (int bx = 0; bx < C::NBOX; bx++)
+                    tma_load_4d_hint(sO + os * C::TILE_BYTES + bx * C::BOX_BYTES, tm_do, bar, bx * 64, qb * BN, T.h,
+                                     T.b, pol_keep);
+            }
+            __syncwarp();
+            ++no;
+            // -lse2 and -D of the block, once the softmax warps have read the slot's
+            // previous step (n - LSLOT).
+            const uint32_t ls = n % C::LSLOT;
+            if (!mbar_wait_warp(smem_u32(&c.ls_empty[ls]), ((n / C::LSLOT) & 1) ^ 1, ab, err, kErrProducer))
+                goto abort;
             const int64_t rbase = static_cast<int64_t>(T.bh) * p.Nq;
 #pragma unroll
             for (int r = lane; r < BN; r += 32) {
                 const int row = qb * BN + r;
                 const bool ok = row < p.Nq;
-                c.nlse[s][r] = ok ? -__ldg(p.lse2 + rbase + row) : -INFINITY;
-                c.nd[s][r] = ok ? -__ldg(p.dvec + rbase + row) : 0.f;
+                c.nlse[ls][r] = ok ? -__ldg(p.lse2 + rbase + row) : -INFINITY;
+                c.nd[ls][r] = ok ? -__ldg(p.dvec + rbase + row) : 0.f;
             }
             __syncwarp();
-            if (leader) {
-                const uint32_t bar = smem_u32(&c.qs_full[s]);
-                mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES);
-                const uint32_t dst = sQS + s * 2 * C::TILE_BYTES;
-#pragma unroll
-                for (int bx = 0; bx < C::NBOX; bx++) {
-                    tma_load_4d_hint(dst + bx * C::BOX_BYTES, tm_q, bar, bx * 64, qb * BN, T.h, T.b, pol_keep);
-                    tma_load_4d_hint(dst + C::TILE_BYTES + bx * C::BOX_BYTES, tm_do, bar, bx * 64, qb * BN, T.h,
-                                     T.b, pol_keep);
-                }
-            }
+            if (leader) mbar_arrive(smem_u32(&c.ls_full[ls]));
             __syncwarp();
         }
     }
     return;
 abort:
-    for (uint32_t k = (n > C::QSTAGE ? n - C::QSTAGE : 0); k < n; k++)
-        drain_wait(smem_u32(&c.qs_full[k % C::QSTAGE]), (k / C::QSTAGE) & 1);
+    for (uint32_t k = (nq > C::QRING ? nq - C::QRING : 0); k < nq; k++)
+        drain_wait(smem_u32(&c.q_full[k % C::QRING]), (k / C::QRING) & 1);
+    for (uint32_t k = (no > C::ORING ? no - C::ORING : 0); k < no; k++)
+        drain_wait(smem_u32(&c.o_full[k % C::ORING]), (k / C::ORING) & 1);
     if (kv_issued >= 0) drain_wait(smem_u32(&c.kv_full), kv_issued & 1);
 }
 
 template <int D, bool CAUSAL, int DT>
-__device__ void kv_mma(const BParams &p, KCtl<D> &c, uint32_t tmem, uint32_t sK, uint32_t sV, uint32_t sQS)
+__device__ void kv_mma(const BParams &p, KCtl<D> &c, uint32_t tmem, uint32_t sK, uint32_t sV, uint32_t sQ,
+                       uint32_t sO)
 {
     using C = BCfg<D>;
     volatile int *ab = &c.abort_flag;
@@ -306,12 +338,19 @@ __device__ void kv_mma(const BParams &p, KCtl<D> &c, uint32_t tmem, uint32_t sK,
     const bool leader = elect_one();
     const uint64_t kd = sdesc_sw128(sK, 16, 1024);
     const uint64_t vd = sdesc_sw128(sV, 16, 1024);
-    const uint64_t qd_k = sdesc_sw128(sQS, 16, 1024);                         // Q as K-major B
-    const uint64_t qd_mn = sdesc_sw128(sQS, C::BOX_BYTES, 1024);              // Q as MN-major B
-    const uint64_t dod_k = sdesc_sw128(sQS + C::TILE_BYTES, 16, 1024);        // dO as K-major B
-    const uint64_t dod_mn = sdesc_sw128(sQS + C::TILE_BYTES, C::BOX_BYTES, 1024);
-    auto stage_off = [](uint32_t m) -> uint64_t {
-        return (static_cast<uint64_t>(m % C::QSTAGE) * 2 * C::TILE_BYTES) >> 4;
+    const uint64_t qd_k = sdesc_sw128(sQ, 16, 1024);            // Q as K-major B
+    const uint64_t qd_mn = sdesc_sw128(sQ, C::BOX_BYTES, 1024); // Q as MN-major B
+    const uint64_t od_k = sdesc_sw128(sO, 16, 1024);            // dO as K-major B
+    const uint64_t od_mn = sdesc_sw128(sO, C::BOX_BYTES, 1024);
+    auto qoff = [](uint32_t m) -> uint64_t { return (static_cast<uint64_t>(m % C::QRING) * C::TILE_BYTES) >> 4; };
+    auto ooff = [](uint32_t m) -> uint64_t { return (static_cast<uint64_t>(m % C::ORING) * C::TILE_BYTES) >> 4; };
+    auto issue_s = [&](uint32_t m) {  // S^T_m = K Q_m^T
+        issue_scores<D, DT>(tmem + C::TM_ST, kd, qd_k + qoff(m));
+        umma_commit(smem_u32(&c.s_full));
+    };
+    auto issue_dp = [&](uint32_t m) {  // dP^T_m = V dO_m^T
+        issue_scores<D, DT>(tmem + C::TM_DPT, vd, od_k + ooff(m));
+        umma_commit(smem_u32(&c.dp_full));
     };
     uint32_t n = 0;
     int w = 0;
@@ -319,13 +358,14 @@ __device__ void kv_mma(const BParams &p, KCtl<D> &c, uint32_t tmem, uint32_t sK,
         const KTile T = decode_ktile<CAUSAL>(p, tile);
         if (!mbar_wait_warp(smem_u32(&c.kv_full), w & 1, ab, err, kErrMma)) goto abort;
         // First step of the tile: S^T and dP^T.
-        if (!mbar_wait_warp(smem_u32(&c.qs_full[n % C::QSTAGE]), (n / C::QSTAGE) & 1, ab, err, kErrMma)) goto abort;
+        if (!mbar_wait_warp(smem_u32(&c.q_full[n % C::QRING]), (n / C::QRING) & 1, ab, err, kErrMma)) goto abort;
+        tc_fence_after();
+        if (leader) issue_s(n);
+        __syncwarp();
+        if (!mbar_wait_warp(smem_u32(&c.o_full[n % C::ORING]), (n / C::ORING) & 1, ab, err, kErrMma)) goto abort;
         tc_fence_after();
         if (leader) {
-            issue_scores<D, DT>(tmem + C::TM_ST, kd, qd_k + stage_off(n));  // S^T = K Q^T
-            umma_commit(smem_u32(&c.s_full));
-            issue_scores<D, DT>(tmem + C::TM_DPT, vd, dod_k + stage_off(n));  // dP^T = V dO^T
-            umma_commit(smem_u32(&c.dp_full));
+            issue_dp(n);
             if (T.nq == 1) umma_commit(smem_u32(&c.kv_empty));
         }
         __syncwarp();
@@ -337,47 +377,45 @@ __device__ void kv_mma(const BParams &p, KCtl<D> &c, uint32_t tmem, uint32_t sK,
                 if (!mbar_wait_warp(smem_u32(&c.acc_free), (w - 1) & 1, ab, err, kErrMma)) goto abort;
             if (!mbar_wait_warp(smem_u32(&c.p_full), n & 1, ab, err, kErrMma)) goto abort;
             tc_fence_after();
-            if (leader) issue_accum<D, DT>(tmem + C::TM_DV, tmem + C::TM_ST, dod_mn + stage_off(n), i > 0 ? 1u : 0u);
+            if (leader) {
+                issue_accum<D, DT>(tmem + C::TM_DV, tmem + C::TM_ST, od_mn + ooff(n), i > 0 ? 1u : 0u);
+                umma_commit(smem_u32(&c.o_empty[n % C::ORING]));  // dO_n is done
+            }
             __syncwarp();
             // S^T of the next step goes in as soon as its Q tile is there: the S^T
             // columns hold P^T(n), which dV (issued just above) reads first, and the
             // softmax warps then overlap its exponentials with dK and the next dP^T.
-            // If the tile has not landed yet, dK goes first (no blocking wait here).
+            // If the tile has not landed yet (test_wait never blocks), dK goes first.
             bool s_next = false;
             if (has_next &&
-                __all_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&c.qs_full[nx % C::QSTAGE]), (nx / C::QSTAGE) & 1))) {
+                __all_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&c.q_full[nx % C::QRING]), (nx / C::QRING) & 1))) {
                 tc_fence_after();
-                if (leader) {
-                    issue_scores<D, DT>(tmem + C::TM_ST, kd, qd_k + stage_off(nx));
-                    umma_commit(smem_u32(&c.s_full));
-                }
+                if (leader) issue_s(nx);
                 __syncwarp();
                 s_next = true;
             }
             if (!mbar_wait_warp(smem_u32(&c.ds_full), n & 1, ab, err, kErrMma)) goto abort;
             tc_fence_after();
             if (leader) {
-                issue_accum<D, DT>(tmem + C::TM_DK, tmem + C::TM_DPT, qd_mn + stage_off(n), i > 0 ? 1u : 0u);
-                umma_commit(smem_u32(&c.qs_empty[n % C::QSTAGE]));
+                issue_accum<D, DT>(tmem + C::TM_DK, tmem + C::TM_DPT, qd_mn + qoff(n), i > 0 ? 1u : 0u);
+                umma_commit(smem_u32(&c.q_empty[n % C::QRING]));  // Q_n is done
                 if (!has_next) umma_commit(smem_u32(&c.acc_full));
             }
             __syncwarp();
             if (has_next) {
                 if (!s_next) {
-                    if (!mbar_wait_warp(smem_u32(&c.qs_full[nx % C::QSTAGE]), (nx / C::QSTAGE) & 1, ab, err,
-                                        kErrMma))
+                    if (!mbar_wait_warp(smem_u32(&c.q_full[nx % C::QRING]), (nx / C::QRING) & 1, ab, err, kErrMma))
                         goto abort;
                     tc_fence_after();
-                    if (leader) {
-                        issue_scores<D, DT>(tmem + C::TM_ST, kd, qd_k + stage_off(nx));
-                        umma_commit(smem_u32(&c.s_full));
-                    }
+                    if (leader) issue_s(nx);
                     __syncwarp();
                 }
                 // dP^T of the next step after dK, which read dS^T(n) from the same columns.
+                if (!mbar_wait_warp(smem_u32(&c.o_full[nx % C::ORING]), (nx / C::ORING) & 1, ab, err, kErrMma))
+                    goto abort;
+                tc_fence_after();
                 if (leader) {
-                    issue_scores<D, DT>(tmem + C::TM_DPT, vd, dod_k + stage_off(nx));
-                    umma_commit(smem_u32(&c.dp_full));
+                    issue_dp(nx);
                     if (i + 2 == T.nq) umma_commit(smem_u32(&c.kv_empty));
                 }
                 __syncwarp();
@@ -411,13 +449,12 @@ __device__ void kv_softmax(const BParams &p, KCtl<D> &c, uint32_t tmem, int warp
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
         const KTile T = decode_ktile<CAUSAL>(p, tile);
         for (int i = 0; i < T.nq; i++, n++) {
-            const uint32_t s = n % C::QSTAGE;
+            const uint32_t s = n % C::LSLOT;
             // The diagonal block: query column c sees this key only if c >= rl.
             const bool diag = CAUSAL && (T.q0 + i == T.kb);
             if (!mbar_wait(smem_u32(&c.s_full), n & 1, ab, err, kErrSoftmax)) return;
-            // Already complete (the MMA waited on it); this acquire orders the
-            // producer's writes of the stage's -lse2 and -D before the reads below.
-            if (!mbar_wait(smem_u32(&c.qs_full[s]), (n / C::QSTAGE) & 1, ab, err, kErrSoftmax)) return;
+            // -lse2 and -D of this step's query block, staged by the producer warp.
+            if (!mbar_wait(smem_u32(&c.ls_full[s]), (n / C::LSLOT) & 1, ab, err, kErrSoftmax)) return;
             tc_fence_after();
             uint32_t r[64];
             tmem_ld32(tS, r);
@@ -470,6 +507,7 @@ __device__ void kv_softmax(const BParams &p, KCtl<D> &c, uint32_t tmem, int warp
                     pk[e >> 1] = pack2<DT>(ds.x, ds.y);
                 }
             }
+            mbar_arrive(smem_u32(&c.ls_empty[s]));  // the slot's -lse2 and -D are read
             tmem_st16(tDP, pk);
             tmem_st16(tDP + 16, pk + 16);
             tmem_wait_st();
@@ -499,18 +537,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const BParams p)
 {
     using C = BCfg<D>;
-    extern __shared__ uint8_t dsmem[];
-    __shared__ KCtl<D> ctl;
-    const uint32_t sbase = (smem_u32(dsmem) + 1023u) & ~1023u;
-    const uint32_t sK = sbase, sV = sbase + C::TILE_BYTES, sQS = sbase + 2 * C::TILE_BYTES;
+    // Dynamic shared memory: [K][V][Q x QRING][dO x ORING] from the first
+    // 1024-byte boundary (128-byte swizzle atoms), then the control block.
+    extern __shared__ __align__(1024) uint8_t dsmem[];
+    const uint32_t dbase = smem_u32(dsmem);
+    const uint32_t sbase = (dbase + 1023u) & ~1023u;
+    const uint32_t ctl_off = sbase - dbase + C::KV_TILES;
+    if (ctl_off + sizeof(KCtl<D>) > static_cast<uint32_t>(p.smem_bytes)) {
+        // The allocation cannot hold the aligned layout: report, touch nothing.
+        if (threadIdx.x == 0) atomicOr(&g_bwd_error_word, kErrLayout);
+        return;
+    }
+    KCtl<D> &ctl = *reinterpret_cast<KCtl<D> *>(dsmem + ctl_off);
+    const uint32_t sK = sbase, sV = sbase + C::TILE_BYTES, sQ = sbase + 2 * C::TILE_BYTES;
+    const uint32_t sO = sQ + C::QRING * C::TILE_BYTES;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&ctl.kv_full), 1);
         mbar_init(smem_u32(&ctl.kv_empty), 1);
-        for (int s = 0; s < C::QSTAGE; s++) {
-            mbar_init(smem_u32(&ctl.qs_full[s]), 1);
-            mbar_init(smem_u32(&ctl.qs_empty[s]), 1);
+        for (int s = 0; s < C::QRING; s++) {
+            mbar_init(smem_u32(&ctl.q_full[s]), 1);
+            mbar_init(smem_u32(&ctl.q_empty[s]), 1);
+        }
+        for (int s = 0; s < C::ORING; s++) {
+            mbar_init(smem_u32(&ctl.o_full[s]), 1);
+            mbar_init(smem_u32(&ctl.o_empty[s]), 1);
+        }
+        for (int s = 0; s < C::LSLOT; s++) {
+            mbar_init(smem_u32(&ctl.ls_full[s]), 1);
+            mbar_init(smem_u32(&ctl.ls_empty[s]), kSoftThreads);
         }
         mbar_init(smem_u32(&ctl.s_full), 1);
         mbar_init(smem_u32(&ctl.dp_full), 1);
@@ -539,9 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 8)
         kv_softmax<D, CAUSAL, DT>(p, ctl, tmem, warp, lane);
     else if (warp == 8)
-        kv_producer<D, CAUSAL, DT>(p, ctl, &tm_q, &tm_k, &tm_v, &tm_do, sK, sV, sQS, lane);
+        kv_producer<D, CAUSAL, DT>(p, ctl, &tm_q, &tm_k, &tm_v, &tm_do, sK, sV, sQ, sO, lane);
     else
-        kv_mma<D, CAUSAL, DT>(p, ctl, tmem, sK, sV, sQS);
+        kv_mma<D, CAUSAL, DT>(p, ctl, tmem, sK, sV, sQ, sO);
     tc_fence_before();
     __syncthreads();
     if (warp == 9) {
@@ -937,8 +993,16 @@ clis_status_t launch_impl(const AttnBwdArgs &a, cudaStream_t stream)
     int dev = 0, nsm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CLIS_ERR_CUDA;
     if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return CLIS_ERR_CUDA;
+    // dK/dV: tiles + control block + alignment slack, capped at the device's
+    // per-block maximum (the kernel checks that its aligned layout fits).
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return CLIS_ERR_CUDA;
+    const int kv_need = C::KV_TILES + static_cast<int>(sizeof(KCtl<D>));
+    if (kv_need > optin) return CLIS_ERR_UNSUPPORTED;
+    const int kv_smem = kv_need + 1023 < optin ? kv_need + 1023 : optin;
     if (cudaFuncSetAttribute(bwd_dkdv_kernel<D, CAUSAL, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::KV_SMEM) != cudaSuccess ||
+                             kv_smem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_dq_kernel<D, CAUSAL, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::Q_SMEM) != cudaSuccess)
         return CLIS_ERR_CUDA;
@@ -989,7 +1053,8 @@ clis_status_t launch_impl(const AttnBwdArgs &a, cudaStream_t stream)
     p.grp = (2 * nsm + p.nkb - 1) / p.nkb;
     p.grp = p.grp > BH ? BH : (p.grp < 1 ? 1 : p.grp);
     int grid = p.num_tiles < nsm ? p.num_tiles : nsm;
-    bwd_dkdv_kernel<D, CAUSAL, DT><<<grid, kThreads, C::KV_SMEM, stream>>>(mq, mk, mv, mdo, p);
+    p.smem_bytes = kv_smem;
+    bwd_dkdv_kernel<D, CAUSAL, DT><<<grid, kThreads, kv_smem, stream>>>(mq, mk, mv, mdo, p);
     if (cudaGetLastError() != cudaSuccess) return CLIS_ERR_CUDA;
 
     // dQ: one work tile per (head, query block).
