@@ -317,7 +317,9 @@ def main():
         "attention_only": {"value": achieved, "unit": "TFLOP/s", "ms": attn_avg_ms},
         "certify": {"ms": cert_avg_ms,
                     "gbs_algorithmic": in_bytes / (cert_avg_ms * 1e-3) / 1e9,
-                    "gbs_moved": (in_bytes * 4 / 3) / (cert_avg_ms * 1e-3) / 1e9},
+                    "gbs_moved": (in_bytes * 4 / 3) / (cert_avg_ms * 1e-3) / 1e9,
+                    "frac_of_hbm_peak_moved": (in_bytes * 4 / 3) / (cert_avg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                    "hbm_peak_gbs": peaks["hbm_gbs"]},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": achieved / peak_tf, "traffic": traffic,
                      "kernel": "attn_fwd_kernel<128,%s>" % ("true" if w.causal else "false"),
