@@ -544,11 +544,31 @@ template <int D, int DT>
 __device__ __forceinline__ void write_row(const Params &p, const Tile &T, uint32_t tO, int row, bool row_ok,
                                           float l_run, float shift)
 {
-    if (p.chunk_mode) {
+    if (p.chunk_mode == 1 && T.cert) {
+        // KV-chunk merge of a certified head: every chunk used the same shift mu_i
+        // (written to m_acc by the first chunk), so the partial adds to the
+        // accumulators as it is -- no exponentials, and no read of the
+        // accumulators: vector reductions that the thread does not wait for.  Each
+        // element receives one add per launch, in launch order (deterministic).
+        const int64_t ridx = static_cast<int64_t>(T.bh) * p.Nq + row;
+        float *oa = p.o_acc + ridx * D;
+#pragma unroll 1
+        for (int c32 = 0; c32 < D / 32; c32++) {
+            uint32_t r[32];
+            tmem_ld32(tO + c32 * 32, r);
+            tmem_wait_ld();
+            if (row_ok) {
+#pragma unroll
+                for (int e = 0; e < 8; e++)
+                    red_add_v4_f32(oa + c32 * 32 + 4 * e, __uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                                   __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+            }
+        }
+        if (row_ok) red_add_f32(p.l_acc + ridx, l_run);
+    } else if (p.chunk_mode) {
         // KV-chunk merge.  The accumulator of row i holds sum_j 2^(x_ij - m_i) v_j and
-        // sum_j 2^(x_ij - m_i) over the chunks merged so far, x = scale_log2 * s.  A
-        // certified head uses the same shift mu_i in every chunk, so its partials add
-        // with no exponentials; an online head rescales to the larger maximum.
+        // sum_j 2^(x_ij - m_i) over the chunks merged so far, x = scale_log2 * s.  An
+        // online head rescales to the larger maximum (a first chunk just stores).
         const float m_c = shift;
         const int64_t ridx = static_cast<int64_t>(T.bh) * p.Nq + row;
         float a_old = 0.f, a_new = 1.f;

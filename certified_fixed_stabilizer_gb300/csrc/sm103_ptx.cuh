@@ -293,6 +293,22 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r)
         : "memory");
 }
 
+// ------------------------------------------------------------ reductions
+
+// Fire-and-forget fp32 adds into global memory (no value returned, so the
+// thread does not wait for the round trip).
+__device__ __forceinline__ void red_add_v4_f32(float *addr, float a, float b, float c, float d)
+{
+    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void red_add_f32(float *addr, float a)
+{
+    asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
+}
+
 // ------------------------------------------------------------------ arithmetic
 
 // exp2 on the MUFU (special function) unit; flushes subnormal results to 0,
