@@ -91,6 +91,8 @@ def _load():
             f = getattr(lib, name)
             f.argtypes = [i64, i64, i64, i64, vp, vp, vp, vp, dbl, i32, vp, vp, vp]
             f.restype = i32
+        lib.oracle_attn_bwd_dq_rows.argtypes = [i32, i64, i64, i64, i64, vp, vp, vp, vp, dbl, i32, i64, vp, vp]
+        lib.oracle_attn_bwd_dq_rows.restype = i32
         lib.oracle_format_log2_max.argtypes = [i32]
         lib.oracle_format_log2_max.restype = dbl
         lib.oracle_ceil_log2_count.argtypes = [i64]
@@ -268,6 +270,34 @@ def attention_bwd(q, k, v, do, scale: float, causal: bool = False):
     if rc != 0:
         raise ValueError(f"oracle attention_bwd rejected its arguments (rc={rc})")
     return dq, dk, dv
+
+
+def attention_bwd_dq_rows(q, k, v, do, scale: float, rows, causal: bool = False):
+    """fp64 dQ of sum(O * do) for the given query rows only: [BH, len(rows), d].
+
+    Each row needs only its own scores, so this reaches sizes where the full
+    backward (dK, dV need every row) does not."""
+    f64 = isinstance(q, np.ndarray) and q.dtype == np.float64
+    if f64:
+        qa, ka, va, ga = (np.ascontiguousarray(t, dtype=np.float64) for t in (q, k, v, do))
+        el = 1
+    else:
+        (qa, fq), (ka, fk), (va, fv), (ga, fg) = (as_bits(t) for t in (q, k, v, do))
+        if not fq == fk == fv == fg:
+            raise TypeError("q, k, v, do must share one format")
+        el = 2 if fq == "fp16" else 0
+    qa, ka, va, ga = (_heads_first(a) for a in (qa, ka, va, ga))
+    if ga.shape != qa.shape:
+        raise ValueError("do must have q's shape")
+    BH, Nq, d = qa.shape
+    rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    dq = np.zeros((BH, rows_arr.shape[0], d), dtype=np.float64)
+    rc = _load().oracle_attn_bwd_dq_rows(el, BH, Nq, ka.shape[1], d, _ptr(qa), _ptr(ka), _ptr(va), _ptr(ga),
+                                         float(scale), int(bool(causal)), rows_arr.shape[0], _ptr(rows_arr),
+                                         _ptr(dq))
+    if rc != 0:
+        raise ValueError(f"oracle attention_bwd_dq_rows rejected its arguments (rc={rc})")
+    return dq
 
 
 def num_threads() -> int:

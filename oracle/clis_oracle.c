@@ -464,6 +464,81 @@ static int attn_bwd_driver(int el, int64_t BH, int64_t Nq, int64_t Nk, int64_t d
     return 0;
 }
 
+/* dQ for selected query rows only (each row's pass 1 needs only its own
+ * scores), for sizes where the key-side pass is out of reach.  rows: n_rows
+ * indices shared by every head; dq: [BH][n_rows][d]. */
+static int attn_bwd_dq_rows_driver(int el, int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
+                                   const void *q, const void *k, const void *v, const void *dout,
+                                   double scale, int causal, int64_t n_rows, const int64_t *rows,
+                                   double *dq)
+{
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || n_rows < 0 || !rows) return 1;
+    if (causal && Nq != Nk) return 1;
+    for (int64_t t = 0; t < n_rows; t++)
+        if (rows[t] < 0 || rows[t] >= Nq) return 1;
+    size_t nk = (size_t)(Nk * d);
+    double *kh = (double *)malloc(nk * sizeof(double));
+    double *vh = (double *)malloc(nk * sizeof(double));
+    if (!kh || !vh) { free(kh); free(vh); return 2; }
+    for (int64_t h = 0; h < BH; h++) {
+        for (size_t e = 0; e < nk; e++) {
+            kh[e] = load_el(k, (int64_t)(h * nk + e), el);
+            vh[e] = load_el(v, (int64_t)(h * nk + e), el);
+        }
+#pragma omp parallel
+        {
+            double *x = (double *)malloc((size_t)Nk * sizeof(double));
+            double *dp = (double *)malloc((size_t)Nk * sizeof(double));
+            double *qi = (double *)malloc((size_t)d * sizeof(double));
+            double *gi = (double *)malloc((size_t)d * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t t = 0; t < n_rows; t++) {
+                int64_t i = rows[t];
+                for (int64_t c = 0; c < d; c++) {
+                    qi[c] = load_el(q, (h * Nq + i) * d + c, el);
+                    gi[c] = load_el(dout, (h * Nq + i) * d + c, el);
+                }
+                int64_t jmax = causal ? i : Nk - 1;
+                double m = -INFINITY;
+                for (int64_t j = 0; j <= jmax; j++) {
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < d; c++) acc += qi[c] * kh[j * d + c];
+                    x[j] = scale * acc;
+                    if (x[j] > m) m = x[j];
+                }
+                double l = 0.0;
+                for (int64_t j = 0; j <= jmax; j++) l += exp(x[j] - m);
+                double lse = m + log(l), Di = 0.0;
+                for (int64_t j = 0; j <= jmax; j++) {
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < d; c++) acc += gi[c] * vh[j * d + c];
+                    dp[j] = acc;
+                    Di += exp(x[j] - lse) * acc;
+                }
+                double *o = dq + (h * n_rows + t) * d;
+                for (int64_t c = 0; c < d; c++) o[c] = 0.0;
+                for (int64_t j = 0; j <= jmax; j++) {
+                    double dx = exp(x[j] - lse) * (dp[j] - Di);
+                    for (int64_t c = 0; c < d; c++) o[c] += dx * kh[j * d + c];
+                }
+                for (int64_t c = 0; c < d; c++) o[c] *= scale;
+            }
+            free(x); free(dp); free(qi); free(gi);
+        }
+    }
+    free(kh);
+    free(vh);
+    return 0;
+}
+
+int oracle_attn_bwd_dq_rows(int el, int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
+                            const void *q, const void *k, const void *v, const void *dout,
+                            double scale, int causal, int64_t n_rows, const int64_t *rows, double *dq)
+{
+    if (el < 0 || el > 2) return 1;
+    return attn_bwd_dq_rows_driver(el, BH, Nq, Nk, d, q, k, v, dout, scale, causal, n_rows, rows, dq);
+}
+
 int oracle_attn_bwd_bf16(int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
                          const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
                          double scale, int causal, double *dq, double *dk, double *dv)

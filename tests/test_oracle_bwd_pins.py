@@ -172,3 +172,20 @@ def test_backward_rejects_bad_arguments(oracle_mod):
         oracle_mod.attention_bwd(q, k[:, :0], k[:, :0], q, 1.0)  # no keys
     with pytest.raises(ValueError):
         oracle_mod.attention_bwd(q, k, k, q[:, :3], 1.0)  # do shape
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dq_rows_equal_full_backward_rows(oracle_mod, causal):
+    """The row-sampled dQ routine (used at sizes the full backward cannot
+    reach) reproduces the pinned full backward's dQ rows exactly."""
+    rng = np.random.default_rng(12)
+    q, g = _rand(rng, 2, 23, 8), _rand(rng, 2, 23, 8)
+    k, v = _rand(rng, 2, 23, 8), _rand(rng, 2, 23, 8)
+    dq, _, _ = oracle_mod.attention_bwd(q, k, v, g, 0.4, causal=causal)
+    rows = [0, 5, 22, 11]
+    got = oracle_mod.attention_bwd_dq_rows(q, k, v, g, 0.4, rows, causal=causal)
+    np.testing.assert_allclose(got, dq[:, rows], rtol=1e-13, atol=1e-15)
+    tq, tk, tv, tg = (torch.from_numpy(t.astype(np.float32)).to(torch.bfloat16) for t in (q, k, v, g))
+    got16 = oracle_mod.attention_bwd_dq_rows(tq, tk, tv, tg, 0.4, rows, causal=causal)
+    ref16, _, _ = oracle_mod.attention_bwd(tq, tk, tv, tg, 0.4, causal=causal)
+    np.testing.assert_allclose(got16, ref16[:, rows], rtol=1e-13, atol=1e-15)
