@@ -399,3 +399,27 @@ def test_fp16_inputs_match_brute_force_and_certify(oracle_mod):
     vbad[0, 2, 3] = np.float16(np.inf)
     _, certs = oracle_mod.certify(q0[None].astype(np.float16), keys[None].astype(np.float16), vbad, 1.0)
     assert certs[0]["reason"] == 2
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_centred_scores_have_nonnegative_row_max_and_stay_within_bound(oracle_mod, seed):
+    """With mu_i = scale_log2 * q_i . kbar, row i's exp2 arguments are
+    scale_log2 * q_i . (k_j - kbar).  kbar is the key mean, so they average to
+    zero over j: the row maximum is >= 0 and the row sum of 2^x is >= 1 (the
+    no-underflow reading for non-causal rows).  And every argument lies in
+    [-B_h, B_h], the certificate's Cauchy-Schwarz bound (Algorithm 1 step 4)."""
+    rng = np.random.default_rng(100 + seed)
+    BH, N, d = 3, 300, 64
+    bias = rng.standard_normal((BH, 1, d)) * 2.0
+    q = _bf16(rng.standard_normal((BH, N, d)) * (0.5 + seed))
+    k = _bf16(rng.standard_normal((BH, N, d)) * 0.7 + bias)
+    v = _bf16(rng.standard_normal((BH, N, d)))
+    sl2 = 0.125 * 1.4426950408889634
+    kbar, certs = oracle_mod.certify(q, k, v, sl2)
+    qf, kf = q.double().numpy(), k.double().numpy()
+    for h in range(BH):
+        x = sl2 * (qf[h] @ (kf[h] - kbar[h]).T)
+        assert x.max(axis=1).min() >= -1e-9
+        assert np.exp2(x).sum(axis=1).min() >= 1.0 - 1e-12
+        assert np.abs(x).max() <= certs[h]["B_h"] * (1 + 1e-12)
+        assert np.abs(x).max() >= 0.25 * certs[h]["B_h"]  # and not vacuous (a few-fold inflated B_h fails)
