@@ -56,9 +56,9 @@ def parse():
     ap.add_argument("--variant", default="auto", choices=["auto", "online", "certified", "online_lazy"])
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"],
                     help="element type of Q, K, V, P and O (fp16 certifies with the FP16 exp2 budget)")
-    ap.add_argument("--extras", default="all", choices=["all", "none", "backward"],
+    ap.add_argument("--extras", default="all", choices=["all", "none", "backward", "chunks"],
                     help="legs after the headline step: all (online variants, ring-step chunks, backward, e2e, "
-                         "CPU baseline), none, or only the backward (profiling runs)")
+                         "CPU baseline), none, or only the backward or the ring-step chunks (profiling runs)")
     ap.add_argument("--no-extras", action="store_true", help="same as --extras none")
     return ap.parse_args()
 
@@ -339,6 +339,7 @@ def main():
         line["online_lazy"] = {"value": flops / (statistics.mean(lz_attn) * 1e-3) / 1e12, "unit": "TFLOP/s",
                                "ms": statistics.mean(lz_attn)}
         line["certified_speedup_vs_online_lazy"] = statistics.mean(lz_attn) / attn_avg_ms
+    if extras in ("all", "chunks"):
         # Ring-step form: K/V in 8 chunks, each merged into fp32 accumulators
         # (clis_attn_fwd_chunk), then clis_attn_chunk_finalize.  Certified heads
         # add their partials with no rescaling; online heads rescale per chunk.
