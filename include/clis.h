@@ -22,8 +22,10 @@
  *    nothing is launched.  Faults found inside a kernel (a pipeline wait
  *    that exceeded its time limit) are recorded in a device-side error word
  *    read by clis_get_device_error().
- *  - All results are deterministic: no floating-point atomics, fixed
- *    reduction orders.
+ *  - All results are deterministic: every floating-point sum has a fixed
+ *    order.  (The one place that adds through memory, the KV-chunk merge of
+ *    certified heads, adds one value per accumulator element per launch, so
+ *    the order is the launch order.)
  */
 #ifndef CLIS_H
 #define CLIS_H
@@ -215,8 +217,10 @@ CLIS_API clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, c
  *   m_acc [B*H*Nq]    the shift m_i (exp2 units), x_ij = scale_log2 * q_i . k_j
  * first = 1 overwrites the accumulators (first chunk), 0 merges.  A certified
  * head's shift is its fixed stabiliser mu_i in every chunk, so its partials
- * add with no exponentials and no rescaling; other heads merge by rescaling
- * to the larger maximum.  kbar, certs (and mu, optional) must come from
+ * add with no exponentials, no rescaling and no read of the accumulators
+ * (in-memory vector adds); other heads read the accumulators and merge by
+ * rescaling to the larger maximum.  Calls on one set of accumulators must
+ * be ordered (one stream, or events between streams).  kbar, certs (and mu, optional) must come from
  * clis_certify over the whole key sequence (for a ring: the k-bar partials and norm maxima of all
  * chunks reduced before the first step).  Non-causal only; shape->o_* ignored.
  * Errors as clis_attn_fwd. */
