@@ -316,6 +316,20 @@ def test_kv_chunk_merge_matches_full_attention(variant):
                 assert torch.equal(m_first[h * rows:(h + 1) * rows], m_acc[h * rows:(h + 1) * rows])
 
 
+def test_kv_chunk_merge_is_deterministic():
+    """Certified heads merge chunks with in-memory vector adds: one add per
+    accumulator element per launch, so two identical passes agree bit for
+    bit (mixed heads: the online ones read-modify-write)."""
+    dev = need_gpu()
+    w = WORKLOADS["mixed"]
+    q, k, v = make_inputs(w, device=dev, N=5000, H=8)
+    kbar, certs = clis.clis_certify(q, k, v, clis.scale_log2_for(w.d))
+    bounds = [0, 700, 2500, 2501, 5000]
+    a = _chunked(q, k, v, bounds, "auto", kbar, certs)
+    b = _chunked(q, k, v, bounds, "auto", kbar, certs)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and torch.equal(a[3], b[3])
+
+
 def test_kv_chunk_single_chunk_equals_fused():
     dev = need_gpu()
     w = WORKLOADS["480p"]
