@@ -101,9 +101,10 @@ def test_backward_after_each_forward_path(variant):
     _check(_gpu_grads(q, k, v, do, True, variant), q, k, v, do, True, f"bwd after {variant}")
 
 
-def test_backward_fp16():
-    q, k, v, do = _inputs(1, 2, 600, 600, 128, True, dtype=torch.float16, seed=7)
-    _check(_gpu_grads(q, k, v, do, True), q, k, v, do, True, "bwd fp16")
+@pytest.mark.parametrize("d,causal", [(128, True), (64, True), (64, False)])
+def test_backward_fp16(d, causal):
+    q, k, v, do = _inputs(1, 2, 600, 600, d, causal, dtype=torch.float16, seed=7)
+    _check(_gpu_grads(q, k, v, do, causal), q, k, v, do, causal, f"bwd fp16 d={d} causal={causal}")
 
 
 def test_backward_strided_layout():
