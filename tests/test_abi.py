@@ -32,6 +32,21 @@ def test_header_declares_the_boundary():
         assert n in names
 
 
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c", "-std=c11"), ("c++", "-std=c++11")])
+def test_header_compiles_standalone(tmp_path, lang, std):
+    """include/clis.h needs no CUDA or C++ headers: plain C99 and C++11 accept it."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("t.c" if lang == "c" else "t.cpp")
+    src.write_text('#include "clis.h"\nint main(void) { clis_shape_t s; (void)s; return (int)CLIS_OK; }\n')
+    r = subprocess.run([cc, std, "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-I" + os.path.dirname(HEADER),
+                        str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_library_exports_every_declared_symbol(clis):
     lib = ctypes.CDLL(clis.library_path())
     for n in _declared_symbols():
