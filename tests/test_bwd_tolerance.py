@@ -1,4 +1,4 @@
-"""Where the backward parity tolerance comes from (no GPU needed).
+"""Where the parity tolerances come from (no GPU needed).
 
 The backward kernels compute in fp32 except at three points: P and dS are
 rounded to the input format (bf16) before they enter the matmuls, O enters
@@ -53,3 +53,40 @@ def test_rounding_alone_uses_at_most_half_the_bound(oracle_mod, causal, N, qs, k
         mx, mn = grad_errors(got[None], r)
         assert mx.max() <= GRAD_TOL[name][0] / 2, (name, mx.max())
         assert mn.max() <= GRAD_TOL[name][1] / 2, (name, mn.max())
+
+
+@pytest.mark.parametrize("nk", [2, 3, 5])
+def test_few_key_heads_forward_rounding(nk):
+    """Forward heads with a handful of keys: the kernel rounds P to bf16 for the
+    P V product (the row sum stays fp32) and the output to bf16.  With nothing
+    to average, one rounded weight scales a whole value row, so a two-key head's
+    mean error from these roundings alone exceeds 1e-3 now and then (a few
+    percent of random heads; errors divided by max(1, max |O|) as in the parity
+    tests), while the mean over a case of 15 heads stays near 0.55e-3, below
+    0.7e-3 (the forward's other errors, fp32 sums and the hardware exp2, are
+    orders of magnitude smaller than these roundings).
+    This is why the random-shape test applies the mean bound per case for heads
+    with fewer than 16 keys."""
+    from gpu_util import MEAN_ABS, head_errors
+    rng = np.random.default_rng(nk)
+    d = 64
+    sl2 = 1.4426950408889634 / math.sqrt(d)
+    got, ref = [], []
+    for _ in range(1500):
+        bias = rng.standard_normal(d) * 2.0
+        q = _bf(rng.standard_normal(d))
+        k = _bf(rng.standard_normal((nk, d)) + bias)
+        v = _bf(rng.standard_normal((nk, d)))
+        x = sl2 * (k @ q)
+        mu = sl2 * (q @ k.mean(axis=0))
+        p = np.exp2(x - mu).astype(np.float32).astype(np.float64)
+        got.append(_bf((_bf(p) @ v) / p.sum()))
+        e = np.exp2(x - x.max())
+        ref.append((e @ v) / e.sum())
+    got, ref = np.array(got)[:, None, :], np.array(ref)[:, None, :]
+    _, per_head = head_errors(got, ref)
+    if nk == 2:
+        assert 0.005 <= (per_head > MEAN_ABS).mean() <= 0.2  # the inherent tail
+    for c in range(0, 1500, 15):
+        _, per_case = head_errors(got[c:c + 15].reshape(1, -1), ref[c:c + 15].reshape(1, -1))
+        assert per_case[0] <= 0.7 * MEAN_ABS

@@ -1,0 +1,125 @@
+"""Seeded random shapes and options against the oracle (forward and backward).
+
+Each case draws batch, heads, query and key lengths (including 1 and
+lengths that leave ragged tiles), head dimension, causal or not, element
+type, forward variant and a strided layout, and checks the GPU forward (and
+for a subset the backward) against the fp64 oracle with the same bounds as
+the dedicated parity tests.  The cases are fixed by their seeds.
+"""
+import dataclasses
+import os
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from certified_fixed_stabilizer_gb300 import clis
+from certified_fixed_stabilizer_gb300.workloads import WORKLOADS, make_dout, make_inputs
+from gpu_util import MAX_ABS, MEAN_ABS, assert_close_to_oracle, assert_grads_close, flat, head_errors, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    need_gpu()
+    oracle.set_num_threads(os.cpu_count() or 1)
+    clis.clis_clear_device_error()
+    yield
+
+
+@pytest.fixture(autouse=True)
+def _device_error_word_stays_clear():
+    yield
+    code = clis.clis_get_device_error()
+    clis.clis_clear_device_error()
+    assert code == 0, f"device error word {code:#x}"
+
+
+def _case(seed):
+    r = random.Random(seed)
+    causal = r.random() < 0.4
+    d = r.choice([64, 128])
+    B, H = r.choice([1, 2, 3]), r.choice([1, 2, 5])
+    Nq = r.choice([1, 7, 128, 129, 255, 300, 513, 1000, 1409])
+    Nk = Nq if causal else r.choice([1, 2, 128, 200, 257, 700, 1290])
+    dtype = r.choice([torch.bfloat16, torch.bfloat16, torch.float16])
+    variant = r.choice(["auto", "auto", "online", "online_lazy", "certified"])
+    strided = r.random() < 0.5
+    return causal, d, B, H, Nq, Nk, dtype, variant, strided
+
+
+def _inputs(seed, causal, d, B, H, Nq, Nk, dtype, strided):
+    dev = need_gpu()
+    w = WORKLOADS["causal" if causal else ("480p" if d == 128 else "tiny")]
+    w = dataclasses.replace(w, B=B, d=d)
+    q, k, v = make_inputs(w, device=dev, seed=seed, N=max(Nq, Nk), H=H, dtype=dtype)
+    q, k, v = q[:, :, :Nq], k[:, :, :Nk], v[:, :, :Nk]
+    if strided:  # [B, N, H, d] storage viewed as [B, H, N, d]
+        q, k, v = (t.transpose(1, 2).contiguous().transpose(1, 2) for t in (q, k, v))
+    else:
+        q, k, v = (t.contiguous() for t in (q, k, v))
+    return w, q, k, v
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_forward_matches_oracle(seed):
+    causal, d, B, H, Nq, Nk, dtype, variant, strided = _case(seed)
+    w, q, k, v = _inputs(seed, causal, d, B, H, Nq, Nk, dtype, strided)
+    sl2 = clis.scale_log2_for(d)
+    exp_fmt = "fp16" if dtype == torch.float16 else "bf16"
+    kbar, certs = clis.clis_certify(q, k, v, sl2, exp_fmt=exp_fmt)
+    lse2 = torch.empty(B * H * Nq, dtype=torch.float32, device=q.device)
+    o = clis.clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=causal, variant=variant, lse2=lse2)
+    torch.cuda.synchronize()
+    ref, rlse = oracle.attention(flat(q.contiguous()).cpu(), flat(k.contiguous()).cpu(), flat(v.contiguous()).cpu(),
+                                 d ** -0.5, causal=causal, with_lse2=True)
+    heads = list(range(B * H))
+    if variant == "certified":  # forced fixed stabiliser: only certified heads are defined
+        heads = [h for h, c in enumerate(clis.decode_certs(certs)) if c["certified"]]
+        if dtype == torch.float16:
+            heads = [h for h in heads if clis.decode_certs(certs)[h]["B_h"] <= 15]
+    got = flat(o).float().cpu().numpy()
+    what = f"fuzz {seed}: causal={causal} d={d} B={B} H={H} Nq={Nq} Nk={Nk} {exp_fmt} {variant} strided={strided}"
+    if heads and Nk < 16:
+        # A head with a handful of keys averages nothing: one bf16-rounded weight
+        # scales a whole value row, so its 64-128 outputs share one relative error
+        # of up to 2^-9 and their mean alone sometimes exceeds 1e-3 (emulating the
+        # kernel's roundings on the CPU, tests/test_bwd_tolerance.py: a few percent of
+        # random two-key heads).  Such heads keep the per-head max bound; the mean
+        # bound applies over the case.
+        mx, _ = head_errors(got[heads], ref[heads])
+        assert mx.max() <= MAX_ABS, f"{what}: max abs err {mx.max():.3e}"
+        _, mn_all = head_errors(got[heads].reshape(1, -1), ref[heads].reshape(1, -1))
+        assert mn_all[0] <= MEAN_ABS, f"{what}: mean abs err over the case {mn_all[0]:.3e}"
+    elif heads:
+        assert_close_to_oracle(got[heads], ref[heads], what)
+    if heads:
+        np.testing.assert_allclose(lse2.cpu().numpy().reshape(rlse.shape)[heads], rlse[heads], atol=3e-3, rtol=0)
+    _, ocerts = oracle.certify(q.contiguous().cpu(), k.contiguous().cpu(), v.contiguous().cpu(), sl2,
+                               exp_fmt=exp_fmt)
+    for g, c in zip(clis.decode_certs(certs), ocerts):
+        if not c["band"]:
+            for key in ("certified", "G", "A", "C", "reason"):
+                assert g[key] == c[key], (what, key, g, c)
+
+
+@pytest.mark.parametrize("seed", range(100, 112))
+def test_random_backward_matches_oracle(seed):
+    causal, d, B, H, Nq, Nk, dtype, _, strided = _case(seed)
+    w, q, k, v = _inputs(seed, causal, d, B, H, Nq, Nk, dtype, strided)
+    do = make_dout(q.shape, device=q.device, seed=seed, dtype=dtype)
+    o, lse2 = clis.attention_fwd_lse(q, k, v, causal=causal)
+    dq, dk, dv = clis.attention_bwd(q, k, v, o, do, lse2, causal=causal)
+    torch.cuda.synchronize()
+    assert dq.stride() == q.stride() and dk.stride() == k.stride() and dv.stride() == v.stride()
+    refs = oracle.attention_bwd(q.contiguous().cpu(), k.contiguous().cpu(), v.contiguous().cpu(),
+                                do.contiguous().cpu(), d ** -0.5, causal=causal)
+    what = f"fuzz bwd {seed}: causal={causal} d={d} B={B} H={H} Nq={Nq} Nk={Nk} {dtype} strided={strided}"
+    for g, r, name in zip((dq, dk, dv), refs, ("dq", "dk", "dv")):
+        ref_max = np.abs(r).reshape(r.shape[0], -1).max(axis=1)
+        keep = ref_max > 1e-6  # a head whose gradient is zero in exact arithmetic (one key: dQ = dK = 0)
+        if keep.any():
+            assert_grads_close(flat(g.contiguous()).float().cpu().numpy()[keep], r[keep], name, what)
