@@ -180,11 +180,16 @@ def cpu_sample_plan(q, k, v, w, target_s):
     oracle.build()
     oracle.set_num_threads(os.cpu_count() or 1)
     heads = [0, 1] if w.heads > 1 else [0]
-    probe = sample_rows(w.N, 32, seed=2)
-    t0 = time.perf_counter()
-    oracle_sample_step(q, k, v, w, heads, probe)
-    dt = time.perf_counter() - t0
-    n = int(min(w.N, max(32, 32 * target_s / max(dt, 1e-3))))
+    # A step costs a + b * rows: a is the certification over all keys, b one row's
+    # attention.  Two probes separate the two so the sample lands near target_s.
+    dts = []
+    for n_probe in (32, 128):
+        t0 = time.perf_counter()
+        oracle_sample_step(q, k, v, w, heads, sample_rows(w.N, n_probe, seed=2))
+        dts.append(time.perf_counter() - t0)
+    per_row = max((dts[1] - dts[0]) / 96, 1e-6)
+    fixed = max(dts[0] - 32 * per_row, 0.0)
+    n = int(min(w.N, max(32, (target_s - fixed) / per_row)))
     return heads, sample_rows(w.N, n, seed=2)
 
 
