@@ -56,9 +56,9 @@ def parse():
     ap.add_argument("--variant", default="auto", choices=["auto", "online", "certified", "online_lazy"])
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"],
                     help="element type of Q, K, V, P and O (fp16 certifies with the FP16 exp2 budget)")
-    ap.add_argument("--extras", default="all", choices=["all", "none", "backward", "chunks"],
+    ap.add_argument("--extras", default="all", choices=["all", "none", "backward", "chunks", "e2e"],
                     help="legs after the headline step: all (online variants, ring-step chunks, backward, e2e, "
-                         "CPU baseline), none, or only the backward or the ring-step chunks (profiling runs)")
+                         "CPU baseline), none, or only the backward, the ring-step chunks or the e2e leg (profiling runs)")
     ap.add_argument("--no-extras", action="store_true", help="same as --extras none")
     return ap.parse_args()
 
@@ -414,10 +414,10 @@ def main():
                             "launches_per_step": 3, "flops": "five matmuls (2.5x the forward's count)",
                             "fwd_plus_bwd_ms": attn_avg_ms + cert_avg_ms + bwd_ms}
         del dout, dq, dk, dv, bws, lse2
-    if extras == "all":
+    if extras in ("all", "e2e"):
         # End to end through the public call (clis.attention) with pinned host
         # buffers: every step copies Q, K, V in, computes and copies O out; the
-        # call pipelines head groups over three streams.
+        # call pipelines head groups over a copy-in, two compute and a copy-out stream.
         qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
         oh = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
 
@@ -440,7 +440,7 @@ def main():
                        "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out.numel() * out.element_size(),
                        "ms_per_step": e2e_ms, "api": "certified_fixed_stabilizer_gb300.clis.attention"}
         del qh, kh, vh, oh
-        if rank == 0 and ws == 1:
+        if rank == 0 and ws == 1 and extras == "all":
             import oracle
             qc, kc, vc = (t.cpu() for t in (q, k, v))
             hs, rows = cpu_sample_plan(qc, kc, vc, w, target_s=15.0)

@@ -334,9 +334,11 @@ def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
     q, k, v: bf16 or fp16 [B, H, N, d].  Device tensors are processed in place
     on the current stream.  Host tensors (pinned for overlap) are copied to
     ``device`` (default cuda:0) and the result is written to ``out`` (a host
-    tensor, allocated if None): heads are processed in ``groups`` groups on
-    three streams so that the copies of one group overlap the compute of
-    another (heads are independent).  The call returns once ``out`` is filled,
+    tensor, allocated if None): heads are processed in ``groups`` groups, with
+    copies in and out on two streams and the kernels on two more (alternating
+    groups), so that the copies of one group overlap the compute of another
+    and one group's kernel can start on SMs the previous one has left idle
+    (heads are independent).  The call returns once ``out`` is filled,
     unless ``non_blocking``: then the current stream is ordered after the work
     and the caller synchronises it before reading ``out``.
     """
@@ -376,10 +378,14 @@ def _attention_host(q, k, v, softmax_scale, causal, variant, return_certs, dev, 
         for h0 in range(0, H, per):
             spans.append((b, h0, min(H, h0 + per)))
     cur = torch.cuda.current_stream(dev)
-    s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
-    for s in (s_in, s_run, s_out):
+    # Two compute streams, alternating by group: the persistent attention kernel of one
+    # group leaves SMs idle in its last wave, and the next group's kernel can start there.
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    s_runs = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
+    for s in (s_in, s_out) + s_runs:
         s.wait_stream(cur)
-    for b, h0, h1 in spans:
+    for gi, (b, h0, h1) in enumerate(spans):
+        s_run = s_runs[gi % 2]
         sl = (slice(b, b + 1), slice(h0, h1))
         ev_in = torch.cuda.Event()
         with torch.cuda.stream(s_in):
@@ -403,10 +409,10 @@ def _attention_host(q, k, v, softmax_scale, causal, variant, return_certs, dev, 
         with torch.cuda.stream(s_out):
             out[sl].copy_(od[sl], non_blocking=True)
     cur.wait_stream(s_out)
-    for t in (qd, kd, vd, od):
-        t.record_stream(s_in)
-        t.record_stream(s_run)
-        t.record_stream(s_out)
+    for t in (qd, kd, vd, od, kbar, certs, mu):
+        if t is not None:
+            for s in (s_in, s_out) + s_runs:
+                t.record_stream(s)
     if not non_blocking:
         s_out.synchronize()
     if return_certs:
