@@ -121,6 +121,9 @@ struct Tile {
 // groups and shortest first on odd groups; with static round-robin assignment
 // this keeps the per-CTA work within about 1% while the K/V of one group of
 // heads stays in L2.
+// Key tile processed at step j of a work tile (odd rounds sweep backwards).
+__device__ __forceinline__ int kv_tile(const Tile &T, int j) { return T.rev ? T.n_kv - 1 - j : j; }
+
 template <bool CAUSAL, int DT>
 __device__ __forceinline__ Tile decode_tile(const Params &p, int tile)
 {
@@ -192,7 +195,8 @@ __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, 
     const bool leader = elect_one();
     const uint64_t pol_kv = policy_evict_last();
     const uint64_t pol_q = policy_evict_first();
-    uint32_t it = 0;
+    uint32_t it = 0;  // K/V tiles issued (ring slot = it % NSTAGE)
+    uint32_t gq = 0;  // load groups issued (full barrier = gq % NSTAGE)
     int w = 0;
     int q_issued = -1;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
@@ -211,30 +215,41 @@ __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, 
             __syncwarp();
         }
         q_issued = w;
-        for (int j = 0; j < T.n_kv; j++) {
-#pragma unroll
-            for (int kv = 0; kv < 2; kv++) {
-                const uint32_t stage = it % C::NSTAGE;
-                const uint32_t ph = (it / C::NSTAGE) & 1;
-                if (!mbar_wait_warp(smem_u32(&c.kv_empty[stage]), ph ^ 1, ab, err, kErrProducer)) goto abort;
-                if (leader) {
-                    const uint32_t bar = smem_u32(&c.kv_full[stage]);
-                    mbar_arrive_expect_tx(bar, C::TILE_BYTES);
-                    const CUtensorMap *tm = kv ? tm_v : tm_k;
+        // K and V tiles go through the NSTAGE-slot ring in the order the MMAs use them
+        // (K_0, V_0, K_1, V_1, ...), and are signalled in groups by the step that first
+        // needs them: {K_0}, {V_0, K_1}, ..., {V_{n-2}, K_{n-1}}, {V_{n-1}}, one full
+        // barrier per group, so the MMA warp waits once per KV step.
+        for (int gi = 0; gi <= T.n_kv; gi++) {
+            const int nl = (gi == 0 || gi == T.n_kv) ? 1 : 2;
+            for (int l = 0; l < nl; l++) {
+                const uint32_t li = it + l;
+                if (!mbar_wait_warp(smem_u32(&c.kv_empty[li % C::NSTAGE]), ((li / C::NSTAGE) & 1) ^ 1, ab, err,
+                                    kErrProducer))
+                    goto abort;
+            }
+            if (leader) {
+                const uint32_t bar = smem_u32(&c.kv_full[gq % C::NSTAGE]);
+                mbar_arrive_expect_tx(bar, nl * C::TILE_BYTES);
+                for (int l = 0; l < nl; l++) {
+                    const uint32_t slot = (it + l) % C::NSTAGE;
+                    const bool is_v = gi > 0 && l == 0;  // a group's first tile is V_{gi-1}, then K_{gi}
+                    const CUtensorMap *tm = is_v ? tm_v : tm_k;
+                    const int key_tile = kv_tile(T, is_v ? gi - 1 : gi);
 #pragma unroll
                     for (int bx = 0; bx < C::NBOX; bx++)
-                        tma_load_4d_hint(sKV + stage * C::TILE_BYTES + bx * C::BOX_BYTES, tm, bar, bx * 64,
-                                         (T.rev ? T.n_kv - 1 - j : j) * BN, T.h, T.b, pol_kv);
+                        tma_load_4d_hint(sKV + slot * C::TILE_BYTES + bx * C::BOX_BYTES, tm, bar, bx * 64,
+                                         key_tile * BN, T.h, T.b, pol_kv);
                 }
-                __syncwarp();
-                ++it;
             }
+            __syncwarp();
+            it += nl;
+            ++gq;
         }
     }
     return;
 abort:
     // Let every copy already issued land before the CTA leaves.
-    for (uint32_t k = (it > C::NSTAGE ? it - C::NSTAGE : 0); k < it; k++)
+    for (uint32_t k = (gq > C::NSTAGE ? gq - C::NSTAGE : 0); k < gq; k++)
         drain_wait(smem_u32(&c.kv_full[k % C::NSTAGE]), (k / C::NSTAGE) & 1);
     if (q_issued >= 0)
         for (int t = 0; t < 2; t++) drain_wait(smem_u32(&c.q_full[t]), q_issued & 1);
@@ -280,7 +295,7 @@ __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, u
     volatile int *ab = &c.abort_flag;
     unsigned *err = &g_attn_error_word;
     const bool leader = elect_one();
-    uint32_t it = 0, g = 0, ncorr = 0;
+    uint32_t it = 0, gq = 0, g = 0, ncorr = 0;
     int w = 0;
     // Q/K descriptors: LBO unused for K-major swizzled operands, SBO = 8 rows x 128 B.
     // V descriptor: LBO = distance between the 64-column boxes, SBO = 8 rows x 128 B.
@@ -295,7 +310,9 @@ __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, u
             if (!mbar_wait_warp(smem_u32(&c.q_full[t]), w & 1, ab, err, kErrMma)) goto abort;
         {
             const uint32_t ks = it % C::NSTAGE;
-            if (!mbar_wait_warp(smem_u32(&c.kv_full[ks]), (it / C::NSTAGE) & 1, ab, err, kErrMma)) goto abort;
+            if (!mbar_wait_warp(smem_u32(&c.kv_full[gq % C::NSTAGE]), (gq / C::NSTAGE) & 1, ab, err, kErrMma))
+                goto abort;
+            ++gq;
             tc_fence_after();
             const uint64_t kd = kvd_k + stage_off(ks);
             if (leader) {
@@ -315,7 +332,10 @@ __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, u
         for (int j = 0; j < T.n_kv; j++) {
             const bool has_next = j + 1 < T.n_kv;
             const uint32_t vs = it % C::NSTAGE;
-            if (!mbar_wait_warp(smem_u32(&c.kv_full[vs]), (it / C::NSTAGE) & 1, ab, err, kErrMma)) goto abort;
+            // V_j and (if there is a next step) K_{j+1}: one load group.
+            if (!mbar_wait_warp(smem_u32(&c.kv_full[gq % C::NSTAGE]), (gq / C::NSTAGE) & 1, ab, err, kErrMma))
+                goto abort;
+            ++gq;
             const uint64_t vd = kvd_v + stage_off(vs);
             const uint32_t kn = it + 1;
             const uint32_t kns = kn % C::NSTAGE;
@@ -336,11 +356,6 @@ __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, u
                 }
                 __syncwarp();
                 if (has_next) {
-                    if (t == 0) {
-                        if (!mbar_wait_warp(smem_u32(&c.kv_full[kns]), (kn / C::NSTAGE) & 1, ab, err, kErrMma))
-                            goto abort;
-                        tc_fence_after();
-                    }
                     if (leader) {
                         issue_qk<D, DT>(tmem + (t ? C::TM_S1 : C::TM_S0), t ? qd1 : qd0, kd);
                         umma_commit(smem_u32(&c.s_full[t]));
@@ -424,7 +439,7 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
             tmem_wait_ld();
 
             // Mask keys past Nk (ragged last tile) and, if causal, keys after the row.
-            const int key0 = (T.rev ? T.n_kv - 1 - j : j) * BN;
+            const int key0 = kv_tile(T, j) * BN;
             const int lim = CAUSAL ? min(p.Nk, row + 1) : p.Nk;  // keys [0, lim) are visible
             if (key0 + BN > lim) {
 #pragma unroll
