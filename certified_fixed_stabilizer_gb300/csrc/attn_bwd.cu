@@ -237,7 +237,7 @@ struct __align__(16) KCtl {
     float nlse[BCfg<D>::LSLOT][BN], nd[BCfg<D>::LSLOT][BN];
     uint64_t kv_full, kv_empty;
     uint64_t q_full[BCfg<D>::QRING], q_empty[BCfg<D>::QRING];
-    uint64_t o_full[BCfg<D>::ORING], o_empty[BCfg<D>::ORING];
+    uint64_t o_empty[BCfg<D>::ORING];  // dO_n lands on Q_n's full barrier
     uint64_t ls_full[BCfg<D>::LSLOT], ls_empty[BCfg<D>::LSLOT];
     uint64_t s_full, dp_full, p_full, ds_full, acc_full, acc_free, drain;
     uint32_t tmem_base;
@@ -275,31 +275,27 @@ __device__ void kv_producer(const BParams &p, KCtl<D> &c, const CUtensorMap *tm_
         for (int i = 0; i < T.nq; i++) {
             const uint32_t n = nq;  // global step index
             const int qb = T.q0 + i;
+            // Q_n and dO_n are signalled together on Q_n's full barrier: the MMA warp
+            // waits once per step (before S^T_n), and dO_n has landed for dP^T_n.
             const uint32_t qs = n % C::QRING;
+            const uint32_t os = n % C::ORING;
             if (!mbar_wait_warp(smem_u32(&c.q_empty[qs]), ((n / C::QRING) & 1) ^ 1, ab, err, kErrProducer))
                 goto abort;
-            if (leader) {
-                const uint32_t bar = smem_u32(&c.q_full[qs]);
-                mbar_arrive_expect_tx(bar, C::TILE_BYTES);
-#pragma unroll
-                for (int bx = 0; bx < C::NBOX; bx++)
-                    tma_load_4d_hint(sQ + qs * C::TILE_BYTES + bx * C::BOX_BYTES, tm_q, bar, bx * 64, qb * BN, T.h,
-                                     T.b, pol_keep);
-            }
-            __syncwarp();
-            ++nq;
-            const uint32_t os = n % C::ORING;
             if (!mbar_wait_warp(smem_u32(&c.o_empty[os]), ((n / C::ORING) & 1) ^ 1, ab, err, kErrProducer))
                 goto abort;
             if (leader) {
-                const uint32_t bar = smem_u32(&c.o_full[os]);
-                mbar_arrive_expect_tx(bar, C::TILE_BYTES);
+                const uint32_t bar = smem_u32(&c.q_full[qs]);
+                mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES);
 #pragma unroll
-                for (int bx = 0; bx < C::NBOX; bx++)
+                for (int bx = 0; bx < C::NBOX; bx++) {
+                    tma_load_4d_hint(sQ + qs * C::TILE_BYTES + bx * C::BOX_BYTES, tm_q, bar, bx * 64, qb * BN, T.h,
+                                     T.b, pol_keep);
                     tma_load_4d_hint(sO + os * C::TILE_BYTES + bx * C::BOX_BYTES, tm_do, bar, bx * 64, qb * BN, T.h,
                                      T.b, pol_keep);
+                }
             }
             __syncwarp();
+            ++nq;
             ++no;
             // -lse2 and -D of the block, once the softmax warps have read the slot's
             // previous step (n - LSLOT).
@@ -323,8 +319,6 @@ __device__ void kv_producer(const BParams &p, KCtl<D> &c, const CUtensorMap *tm_
 abort:
     for (uint32_t k = (nq > C::QRING ? nq - C::QRING : 0); k < nq; k++)
         drain_wait(smem_u32(&c.q_full[k % C::QRING]), (k / C::QRING) & 1);
-    for (uint32_t k = (no > C::ORING ? no - C::ORING : 0); k < no; k++)
-        drain_wait(smem_u32(&c.o_full[k % C::ORING]), (k / C::ORING) & 1);
     if (kv_issued >= 0) drain_wait(smem_u32(&c.kv_full), kv_issued & 1);
 }
 
@@ -362,10 +356,8 @@ __device__ void kv_mma(const BParams &p, KCtl<D> &c, uint32_t tmem, uint32_t sK,
         tc_fence_after();
         if (leader) issue_s(n);
         __syncwarp();
-        if (!mbar_wait_warp(smem_u32(&c.o_full[n % C::ORING]), (n / C::ORING) & 1, ab, err, kErrMma)) goto abort;
-        tc_fence_after();
         if (leader) {
-            issue_dp(n);
+            issue_dp(n);  // dO_n landed with Q_n
             if (T.nq == 1) umma_commit(smem_u32(&c.kv_empty));
         }
         __syncwarp();
@@ -410,10 +402,8 @@ __device__ void kv_mma(const BParams &p, KCtl<D> &c, uint32_t tmem, uint32_t sK,
                     if (leader) issue_s(nx);
                     __syncwarp();
                 }
-                // dP^T of the next step after dK, which read dS^T(n) from the same columns.
-                if (!mbar_wait_warp(smem_u32(&c.o_full[nx % C::ORING]), (nx / C::ORING) & 1, ab, err, kErrMma))
-                    goto abort;
-                tc_fence_after();
+                // dP^T of the next step after dK, which read dS^T(n) from the same columns
+                // (dO_{n+1} landed with Q_{n+1}).
                 if (leader) {
                     issue_dp(nx);
                     if (i + 2 == T.nq) umma_commit(smem_u32(&c.kv_empty));
@@ -560,10 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&ctl.q_full[s]), 1);
             mbar_init(smem_u32(&ctl.q_empty[s]), 1);
         }
-        for (int s = 0; s < C::ORING; s++) {
-            mbar_init(smem_u32(&ctl.o_full[s]), 1);
-            mbar_init(smem_u32(&ctl.o_empty[s]), 1);
-        }
+        for (int s = 0; s < C::ORING; s++) mbar_init(smem_u32(&ctl.o_empty[s]), 1);
         for (int s = 0; s < C::LSLOT; s++) {
             mbar_init(smem_u32(&ctl.ls_full[s]), 1);
             mbar_init(smem_u32(&ctl.ls_empty[s]), kSoftThreads);
@@ -612,7 +599,7 @@ template <int D>
 struct __align__(16) QCtl {
     uint64_t qo_full, qo_empty;
     uint64_t k_full[BCfg<D>::KRING], k_empty[BCfg<D>::KRING];
-    uint64_t v_full[BCfg<D>::VRING], v_empty[BCfg<D>::VRING];
+    uint64_t v_empty[BCfg<D>::VRING];  // V_j lands on K_j's full barrier
     uint64_t s_full[2], dp_full, ds_full, acc_full, acc_free, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -645,32 +632,28 @@ __device__ void q_producer(const BParams &p, QCtl<D> &c, const CUtensorMap *tm_q
         }
         __syncwarp();
         q_issued = w;
+        // K_j and V_j are signalled together on K_j's full barrier: the MMA warp waits
+        // once per step (before S_j), and V_j has landed by the time dP_j needs it.
         for (int j = 0; j < T.nkv; j++) {
             const uint32_t ks = nk % C::KRING;
+            const uint32_t vs = nv % C::VRING;
             if (!mbar_wait_warp(smem_u32(&c.k_empty[ks]), ((nk / C::KRING) & 1) ^ 1, ab, err, kErrProducer))
                 goto abort;
-            if (leader) {
-                const uint32_t bar = smem_u32(&c.k_full[ks]);
-                mbar_arrive_expect_tx(bar, C::TILE_BYTES);
-#pragma unroll
-                for (int bx = 0; bx < C::NBOX; bx++)
-                    tma_load_4d_hint(sK + ks * C::TILE_BYTES + bx * C::BOX_BYTES, tm_k, bar, bx * 64, j * BN, T.h,
-                                     T.b, pol_keep);
-            }
-            __syncwarp();
-            ++nk;
-            const uint32_t vs = nv % C::VRING;
             if (!mbar_wait_warp(smem_u32(&c.v_empty[vs]), ((nv / C::VRING) & 1) ^ 1, ab, err, kErrProducer))
                 goto abort;
             if (leader) {
-                const uint32_t bar = smem_u32(&c.v_full[vs]);
-                mbar_arrive_expect_tx(bar, C::TILE_BYTES);
+                const uint32_t bar = smem_u32(&c.k_full[ks]);
+                mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES);
 #pragma unroll
-                for (int bx = 0; bx < C::NBOX; bx++)
+                for (int bx = 0; bx < C::NBOX; bx++) {
+                    tma_load_4d_hint(sK + ks * C::TILE_BYTES + bx * C::BOX_BYTES, tm_k, bar, bx * 64, j * BN, T.h,
+                                     T.b, pol_keep);
                     tma_load_4d_hint(sV + vs * C::TILE_BYTES + bx * C::BOX_BYTES, tm_v, bar, bx * 64, j * BN, T.h,
                                      T.b, pol_keep);
+                }
             }
             __syncwarp();
+            ++nk;
             ++nv;
         }
     }
@@ -679,8 +662,6 @@ abort:
     // Let every copy already issued land before the CTA leaves.
     for (uint32_t k = (nk > C::KRING ? nk - C::KRING : 0); k < nk; k++)
         drain_wait(smem_u32(&c.k_full[k % C::KRING]), (k / C::KRING) & 1);
-    for (uint32_t k = (nv > C::VRING ? nv - C::VRING : 0); k < nv; k++)
-        drain_wait(smem_u32(&c.v_full[k % C::VRING]), (k / C::VRING) & 1);
     if (q_issued >= 0) drain_wait(smem_u32(&c.qo_full), q_issued & 1);
 }
 
@@ -726,10 +707,9 @@ __device__ void q_mma(const BParams &p, QCtl<D> &c, uint32_t tmem, uint32_t sQ, 
                 }
                 __syncwarp();
             }
-            // dP_j = dO V_j^T (after dQ has read dS_{j-1} from the same columns).
+            // dP_j = dO V_j^T (after dQ has read dS_{j-1} from the same columns); V_j
+            // landed with K_j.
             const uint32_t vs = n % C::VRING;
-            if (!mbar_wait_warp(smem_u32(&c.v_full[vs]), (n / C::VRING) & 1, ab, err, kErrMma)) goto abort;
-            tc_fence_after();
             if (leader) {
                 issue_scores<D, DT>(tmem + C::TM_DP, dod, vd_k + slot_off(vs));
                 umma_commit(smem_u32(&c.dp_full));
@@ -855,10 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&ctl.k_full[s]), 1);
             mbar_init(smem_u32(&ctl.k_empty[s]), 1);
         }
-        for (int s = 0; s < C::VRING; s++) {
-            mbar_init(smem_u32(&ctl.v_full[s]), 1);
-            mbar_init(smem_u32(&ctl.v_empty[s]), 1);
-        }
+        for (int s = 0; s < C::VRING; s++) mbar_init(smem_u32(&ctl.v_empty[s]), 1);
         mbar_init(smem_u32(&ctl.s_full[0]), 1);
         mbar_init(smem_u32(&ctl.s_full[1]), 1);
         mbar_init(smem_u32(&ctl.dp_full), 1);
