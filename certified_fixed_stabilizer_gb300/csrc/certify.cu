@@ -116,44 +116,58 @@ __global__ void __launch_bounds__(kCertThreads) certify_ksum_kernel(CertArgs a, 
     if (threadIdx.x == 0) ws.kabs[static_cast<int64_t>(bh) * a.nck + chunk] = m;
 }
 
-// Step 1 (final): kbar = sum_chunks / Nk, round to nearest.
+// Step 1 (final): kbar = sum_chunks / Nk, round to nearest.  Also clears the
+// head's maxima that the norms kernel accumulates with atomicMax.
 __global__ void certify_kbar_kernel(CertArgs a, CertWorkspace ws)
 {
     const int bh = blockIdx.x;
     const int c = threadIdx.x;
+    for (int i = c; i < a.nck; i += blockDim.x) {
+        ws.knorm2[static_cast<int64_t>(bh) * a.nck + i] = 0u;
+        ws.vabs[static_cast<int64_t>(bh) * a.nck + i] = 0u;
+    }
+    for (int i = c; i < a.ncq; i += blockDim.x) {
+        ws.qnorm2[static_cast<int64_t>(bh) * a.ncq + i] = 0u;
+        ws.qabs[static_cast<int64_t>(bh) * a.ncq + i] = 0u;
+    }
     if (c >= a.d) return;
     float s = 0.f;
     for (int ch = 0; ch < a.nck; ch++) s += ws.ksum[(static_cast<int64_t>(bh) * a.nck + ch) * a.d + c];
     a.kbar[static_cast<int64_t>(bh) * a.d + c] = __fdiv_rn(s, static_cast<float>(a.Nk));
 }
 
-// Steps 2-5 (partial): one chunk of K (centred norms), Q (norms) or V (|v|).
+// Steps 2-5 (partial): one quarter of a chunk of K (centred norms), Q (norms)
+// or V (|v|).  Quarter-chunk blocks keep the last wave of the grid short; the
+// four quarters of a chunk meet in its partial maximum through atomicMax on the
+// bit patterns of non-negative floats, which is exact and order-independent.
 template <int D, int DT>
 __global__ void __launch_bounds__(kCertThreads) certify_norms_kernel(CertArgs a, CertWorkspace ws)
 {
     constexpr int VPR = D / 8;
     constexpr int RPS = kCertThreads / VPR;
+    constexpr int SUB = kCertChunkRows / kCertNormSplit;  // rows per block
     __shared__ uint32_t redu[kCertThreads / 32];
 
-    const int per_head = 2 * a.nck + a.ncq;
+    const int per_head = kCertNormSplit * (2 * a.nck + a.ncq);
     const int bh = blockIdx.x / per_head;
-    int part = blockIdx.x % per_head;
+    int sub = blockIdx.x % per_head;
     const int b = bh / a.H, h = bh % a.H;
     const int cv = threadIdx.x % VPR, rp = threadIdx.x / VPR;
 
     int kind;  // 0 = K, 1 = Q, 2 = V
-    if (part < a.nck) {
+    if (sub < kCertNormSplit * a.nck) {
         kind = 0;
-    } else if (part < a.nck + a.ncq) {
+    } else if (sub < kCertNormSplit * (a.nck + a.ncq)) {
         kind = 1;
-        part -= a.nck;
+        sub -= kCertNormSplit * a.nck;
     } else {
         kind = 2;
-        part -= a.nck + a.ncq;
+        sub -= kCertNormSplit * (a.nck + a.ncq);
     }
+    const int part = sub / kCertNormSplit;  // chunk whose partial this block feeds
     const int nrows = (kind == 1) ? a.Nq : a.Nk;
-    const int r0 = part * kCertChunkRows;
-    const int r1 = min(nrows, r0 + kCertChunkRows);
+    const int r0 = min(nrows, sub * SUB);
+    const int r1 = min(nrows, r0 + SUB);
     const int nsweeps = (r1 - r0 + RPS - 1) / RPS;  // uniform across the block
 
     if (kind == 0) {
@@ -186,7 +200,7 @@ __global__ void __launch_bounds__(kCertThreads) certify_norms_kernel(CertArgs a,
             mx = fmaxf(mx, ss);
         }
         const uint32_t m = block_max_u32(__float_as_uint(mx), redu);
-        if (threadIdx.x == 0) ws.knorm2[static_cast<int64_t>(bh) * a.nck + part] = m;
+        if (threadIdx.x == 0) atomicMax(&ws.knorm2[static_cast<int64_t>(bh) * a.nck + part], m);
     } else if (kind == 1) {
         const uint16_t *base = a.q + b * a.q_sb + h * a.q_sh + cv * 8;
         float mx = 0.f;
@@ -224,8 +238,8 @@ __global__ void __launch_bounds__(kCertThreads) certify_norms_kernel(CertArgs a,
         const uint32_t m = block_max_u32(__float_as_uint(mx), redu);
         const uint32_t am = block_max_u32(amax, redu);
         if (threadIdx.x == 0) {
-            ws.qnorm2[static_cast<int64_t>(bh) * a.ncq + part] = m;
-            ws.qabs[static_cast<int64_t>(bh) * a.ncq + part] = am;
+            atomicMax(&ws.qnorm2[static_cast<int64_t>(bh) * a.ncq + part], m);
+            atomicMax(&ws.qabs[static_cast<int64_t>(bh) * a.ncq + part], am);
         }
     } else {
         const uint16_t *base = a.v + b * a.v_sb + h * a.v_sh + cv * 8;
@@ -239,7 +253,7 @@ __global__ void __launch_bounds__(kCertThreads) certify_norms_kernel(CertArgs a,
             amax = abs_bits_max(u.w, amax);
         }
         const uint32_t am = block_max_u32(amax, redu);
-        if (threadIdx.x == 0) ws.vabs[static_cast<int64_t>(bh) * a.nck + part] = am;
+        if (threadIdx.x == 0) atomicMax(&ws.vabs[static_cast<int64_t>(bh) * a.nck + part], am);
     }
 }
 
@@ -360,7 +374,7 @@ cudaError_t launch_certify(const CertArgs &a, const CertWorkspace &ws, cudaStrea
     const int BH = a.B * a.H;
     if (BH == 0) return cudaSuccess;
     const unsigned g1 = static_cast<unsigned>(BH) * static_cast<unsigned>(a.nck);
-    const unsigned g3 = static_cast<unsigned>(BH) * static_cast<unsigned>(2 * a.nck + a.ncq);
+    const unsigned g3 = static_cast<unsigned>(BH) * static_cast<unsigned>(kCertNormSplit * (2 * a.nck + a.ncq));
     const bool f16 = a.dtype == CLIS_DT_FP16;
     if (a.d == 128) {
         if (f16) certify_ksum_kernel<128, 1><<<g1, kCertThreads, 0, stream>>>(a, ws);

@@ -14,6 +14,7 @@ namespace clis {
 // ----------------------------------------------------------- certification
 
 constexpr int kCertChunkRows = 1024;  // rows per partial-reduction chunk
+constexpr int kCertNormSplit = 4;     // norms-kernel blocks per chunk
 constexpr int kCertThreads = 256;
 
 struct CertWorkspace {
