@@ -429,7 +429,7 @@ def main():
             e2e_step()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n_e2e = max(1, min(args.steps, 5))
+        n_e2e = max(1, min(args.steps, 10))
         e0.record(stream)
         for _ in range(n_e2e):
             e2e_step()
