@@ -126,18 +126,8 @@ __device__ __forceinline__ void tma_prefetch_desc(const void *tmap)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
-// 4-D tiled bulk tensor load global -> shared, completion on an mbarrier.
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, uint32_t bar, int c0,
-                                            int c1, int c2, int c3)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-        : "memory");
-}
-
-// Same with an L2 cache-policy hint (createpolicy value).
+// 4-D tiled bulk tensor load global -> shared, completion on an mbarrier, with an
+// L2 cache-policy hint (createpolicy value).
 __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void *tmap, uint32_t bar,
                                                  int c0, int c1, int c2, int c3, uint64_t policy)
 {
@@ -147,15 +137,6 @@ __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void *tmap,
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
         "l"(policy)
         : "memory");
-}
-
-// Bring a 4-D tile into L2 ahead of its use (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2_4d(const void *tmap, int c0, int c1, int c2, int c3)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                     reinterpret_cast<uint64_t>(tmap)),
-                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-                 : "memory");
 }
 
 __device__ __forceinline__ uint64_t policy_evict_last()
