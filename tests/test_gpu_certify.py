@@ -254,3 +254,25 @@ def test_fp16_nonfinite_inputs_fail_certification(where):
     t[0, 1, 300, 9] = float("inf")
     g, oc = _compare(q, k, v, clis.scale_log2_for(w.d), exp_fmt="fp16")
     assert g[1]["reason"] == 2 and g[0]["certified"] == 1
+
+
+def test_workspace_contents_do_not_leak_between_calls():
+    """The norms pass combines the quarter-chunk maxima of a chunk with atomicMax
+    in the caller's workspace, after the k-bar step has cleared them.  A workspace
+    holding garbage (all bits set) or the maxima of larger inputs must give the
+    same certificates as a fresh one."""
+    dev = need_gpu()
+    w = WORKLOADS["480p"]
+    q, k, v = make_inputs(w, device=dev, H=3, N=3000)
+    sl2 = clis.scale_log2_for(w.d)
+    ref_kbar, ref_certs = clis.clis_certify(q, k, v, sl2)
+    ws = torch.empty(max(256, clis.clis_certify_workspace_size(clis.make_shape(q, k, v))), dtype=torch.uint8,
+                     device=dev)
+    ws.fill_(255)
+    kb1, c1 = clis.clis_certify(q, k, v, sl2, workspace=ws)
+    clis.clis_certify(q * 64, k * 64, v * 64, sl2, workspace=ws)
+    kb2, c2 = clis.clis_certify(q, k, v, sl2, workspace=ws)
+    torch.cuda.synchronize()
+    for kb, c in ((kb1, c1), (kb2, c2)):
+        assert torch.equal(kb, ref_kbar)
+        assert torch.equal(c, ref_certs)
