@@ -67,6 +67,8 @@ def load_library():
     lib.clis_certify_workspace_size.restype = i32
     lib.clis_certify.argtypes = [sp, vp, vp, vp, f32, i32, i32, vp, vp, vp, vp, sz, vp]
     lib.clis_certify.restype = i32
+    lib.clis_certify_noalloc.argtypes = [sp, vp, vp, vp, f32, i32, i32, vp, vp, vp, vp]
+    lib.clis_certify_noalloc.restype = i32
     lib.clis_attn_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp]
     lib.clis_attn_fwd.restype = i32
     lib.clis_status_string.argtypes = [i32]
@@ -153,6 +155,24 @@ def clis_certify(q, k, v, scale_log2: float, exp_fmt: str = "bf16", acc_fmt: str
                           workspace.numel(), _stream(stream))
     if st != 0:
         raise ClisError("clis_certify", st)
+    return kbar, certs
+
+
+def clis_certify_noalloc(q, k, v, scale_log2: float, exp_fmt: str = "bf16", acc_fmt: str = "fp32",
+                         kbar=None, certs=None, stream=None, mu=None):
+    """clis_certify without a workspace argument: the library's own fixed scratch
+    (CLIS_NOALLOC_SCRATCH_BYTES) stands in for it.  Returns (kbar, certs)."""
+    lib = load_library()
+    shape = make_shape(q, k, v)
+    BH, d = shape.B * shape.H, shape.d
+    if kbar is None:
+        kbar = torch.empty((max(BH, 1), d), dtype=torch.float32, device=q.device)
+    if certs is None:
+        certs = torch.empty((max(BH, 1), CERT_WORDS), dtype=torch.int32, device=q.device)
+    st = lib.clis_certify_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), float(scale_log2), FMT[exp_fmt],
+                                  FMT[acc_fmt], _ptr(kbar), _ptr(certs), _ptr(mu), _stream(stream))
+    if st != 0:
+        raise ClisError("clis_certify_noalloc", st)
     return kbar, certs
 
 

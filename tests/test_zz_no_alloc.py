@@ -24,26 +24,12 @@ SCRATCH_BYTES = 4 << 20  # CLIS_NOALLOC_SCRATCH_BYTES in include/clis.h
 CLIS_ERR_WORKSPACE = 4
 
 
-def _lib():
-    lib = clis.load_library()
-    vp = ctypes.c_void_p
-    lib.clis_certify_noalloc.argtypes = [ctypes.POINTER(clis.Shape), vp, vp, vp, ctypes.c_float,
-                                         ctypes.c_int, ctypes.c_int, vp, vp, vp, vp]
-    lib.clis_certify_noalloc.restype = ctypes.c_int
-    return lib
-
-
 def _noalloc(q, k, v, sl2):
-    shape = clis.make_shape(q, k, v)
     BH = q.shape[0] * q.shape[1]
     # Outputs start as garbage so a stale or skipped write cannot pass.
     kbar = torch.full((BH, q.shape[-1]), float("nan"), device=q.device)
     certs = torch.full((BH, clis.CERT_WORDS), -7, dtype=torch.int32, device=q.device)
-    st = _lib().clis_certify_noalloc(ctypes.byref(shape), q.data_ptr(), k.data_ptr(), v.data_ptr(), sl2,
-                                     clis.FMT["bf16"], clis.FMT["fp32"], kbar.data_ptr(), certs.data_ptr(),
-                                     None, torch.cuda.current_stream().cuda_stream)
-    assert st == 0, clis.clis_status_string(st)
-    return kbar, certs
+    return clis.clis_certify_noalloc(q, k, v, sl2, kbar=kbar, certs=certs)
 
 
 def _check_same(q, k, v, sl2):
@@ -88,5 +74,6 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
         setattr(s, f"{t}_sb", 64 * 600000 * 128)
     assert clis.clis_certify_workspace_size(s) > SCRATCH_BYTES
     fake = 0x100000
-    st = _lib().clis_certify_noalloc(ctypes.byref(s), fake, fake, fake, 0.1, 1, 2, fake, fake, None, None)
+    st = clis.load_library().clis_certify_noalloc(ctypes.byref(s), fake, fake, fake, 0.1, 1, 2, fake, fake, None,
+                                                  None)
     assert st == CLIS_ERR_WORKSPACE
