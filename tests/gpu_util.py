@@ -70,9 +70,12 @@ def assert_paths_agree(a, b, what: str = ""):
 # roundings on the CPU and shows they alone stay within half of these bounds.
 # dQ gets the widest bound: dQ_i = scale sum_j dS_ij k_j where the keys share
 # a large per-head bias that cancels in exact arithmetic (sum_j dS_ij = 0) but
-# not in the bf16-rounded dS (up to 2.7e-2 of max |dQ| on diffuse 720p-like
-# heads); dK and dV sum terms with no common offset.
-GRAD_TOL = {"dq": (6e-2, 4e-3), "dk": (1.2e-2, 2e-3), "dv": (1.2e-2, 2e-3)}
+# not in the bf16-rounded dS (up to 4.1e-2 of max |dQ| over 320 diffuse heads).
+# dK's bound covers causal heads whose early rows one key dominates: the
+# certified forward gives that key's weight 2^x its bf16 rounding, so O and
+# D_i = dO_i . O_i are off by up to 2^-9 relative and the key's dK collects it
+# from every such row (up to 1.9e-2 of max |dK| over 320 short causal heads).
+GRAD_TOL = {"dq": (9e-2, 5e-3), "dk": (4e-2, 2e-3), "dv": (1.2e-2, 2e-3)}
 
 
 def grad_errors(got: np.ndarray, ref: np.ndarray):

@@ -3,56 +3,73 @@
 The backward kernels compute in fp32 except at three points: P and dS are
 rounded to the input format (bf16) before they enter the matmuls, O enters
 D_i = dO_i . O_i as the forward's bf16 output, and dQ, dK, dV are rounded to
-bf16 once at the end.  This test applies exactly those roundings to an fp64
-computation and measures the error against the oracle on the workload
-distributions: it must stay within half of the GPU tests' bounds
-(gpu_util.GRAD_TOL), leaving the other half for fp32 summation order and the
-hardware exp2.
+bf16 once at the end.  The forward's O itself comes from the certified kernel:
+unnormalised weights p = exp2(scale_log2 * s - mu_i) with the fixed stabiliser,
+rounded to bf16 for the P V product, divided by their fp32 sum.  A row that
+one key dominates therefore gets that key's V off by the bf16 rounding of a
+weight 2^x (up to 2^-9 relative; online softmax gives the dominant key the
+exact weight 1), and D_i carries that error into every dS of the row, which is
+largest for keys that early causal rows see.  This test applies exactly those
+roundings to an fp64 computation on populations of heads drawn like the
+workloads and measures the largest per-head error against the oracle: it must
+stay within half of the GPU tests' bounds (gpu_util.GRAD_TOL), leaving the
+other half for fp32 summation order and the hardware exp2.
 """
+import dataclasses
 import math
 
 import numpy as np
 import pytest
 import torch
 
+from certified_fixed_stabilizer_gb300.workloads import WORKLOADS, make_dout, make_inputs
 from gpu_util import GRAD_TOL, grad_errors
+
+LOG2E = 1.4426950408889634
 
 
 def _bf(x):
     return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
 
 
-@pytest.mark.parametrize("seed", [0, 1, 2])
-@pytest.mark.parametrize("causal,N,qs,ks,bs", [
-    (True, 512, 1.0, 1.0, math.sqrt(2.0)),   # causal LLM distributions
-    (False, 1024, 0.5, 0.5, 2.0),           # 480p / 720p DiT distributions
-    (False, 384, 1.0, 1.0, 2.0),
-])
-def test_rounding_alone_uses_at_most_half_the_bound(oracle_mod, causal, N, qs, ks, bs, seed):
-    rng = np.random.default_rng(1000 * seed + N + int(causal))
-    d = 128
-    scale = 1.0 / math.sqrt(d)
-    bias = rng.standard_normal(d) * bs
-    q = _bf(rng.standard_normal((N, d)) * qs)
-    k = _bf(rng.standard_normal((N, d)) * ks + bias)
-    v = _bf(rng.standard_normal((N, d)))
-    g = _bf(rng.standard_normal((N, d)))
-    ref = oracle_mod.attention_bwd(q[None], k[None], v[None], g[None], scale, causal=causal)
-
-    s = scale * (q @ k.T)
+def _emulated_grads(q, k, v, g, scale, causal):
+    """dQ, dK, dV of one head with the certified forward's and the backward's roundings."""
+    N = q.shape[0]
+    sl2 = scale * LOG2E
+    mu = sl2 * (q @ k.mean(axis=0))  # fixed per-row stabiliser
+    x = sl2 * (q @ k.T) - mu[:, None]
     if causal:
-        s = np.where(np.tril(np.ones((N, N))) > 0, s, -np.inf)
-    P = np.exp(s - s.max(axis=1, keepdims=True))
-    P /= P.sum(axis=1, keepdims=True)
-    O = _bf(P @ v)                                   # forward output, bf16
-    dV = _bf(_bf(P).T @ g)                           # P rounded for the matmul
+        x = np.where(np.tril(np.ones((N, N))) > 0, x, -np.inf)
+    p = np.exp2(x)
+    l = p.sum(axis=1, keepdims=True)
+    O = _bf((_bf(p) @ v) / l)         # forward output: P rounded for P V, fp32 row sum
+    P = p / l
+    dV = _bf(_bf(P).T @ g)            # P rounded for the matmul
     dS = _bf(P * (g @ v.T - (g * O).sum(axis=1, keepdims=True)))
-    dQ = _bf(scale * (dS @ k))
-    dK = _bf(scale * (dS.T @ q))
-    for got, r, name in ((dQ, ref[0], "dq"), (dK, ref[1], "dk"), (dV, ref[2], "dv")):
-        mx, mn = grad_errors(got[None], r)
-        assert mx.max() <= GRAD_TOL[name][0] / 2, (name, mx.max())
-        assert mn.max() <= GRAD_TOL[name][1] / 2, (name, mn.max())
+    return _bf(scale * (dS @ k)), _bf(scale * (dS.T @ q)), dV
+
+
+@pytest.mark.parametrize("name,B,H,N,seed", [
+    ("causal", 8, 40, 300, 61),   # 320 short causal heads: the dominated-row tail
+    ("causal", 1, 32, 512, 62),
+    ("480p", 1, 32, 1024, 63),    # diffuse DiT rows: dQ's tail
+])
+def test_rounding_alone_uses_at_most_half_the_bound(oracle_mod, name, B, H, N, seed):
+    w = dataclasses.replace(WORKLOADS[name], B=B)
+    q, k, v = make_inputs(w, device="cpu", N=N, H=H, seed=seed)
+    g = make_dout(q.shape, device="cpu", seed=seed)
+    flat = [t.reshape(-1, N, w.d) for t in (q, k, v, g)]
+    ref = oracle_mod.attention_bwd(*flat, w.softmax_scale(), causal=w.causal)
+    qf, kf, vf, gf = (t.double().numpy() for t in flat)
+    worst = {n: [0.0, 0.0] for n in ("dq", "dk", "dv")}
+    for h in range(qf.shape[0]):
+        got = _emulated_grads(qf[h], kf[h], vf[h], gf[h], w.softmax_scale(), w.causal)
+        for x, r, n in zip(got, (ref[0][h], ref[1][h], ref[2][h]), ("dq", "dk", "dv")):
+            mx, mn = grad_errors(x[None], r[None])
+            worst[n] = [max(worst[n][0], mx[0]), max(worst[n][1], mn[0])]
+    for n, (mx, mn) in worst.items():
+        assert mx <= GRAD_TOL[n][0] / 2, (name, N, n, mx)
+        assert mn <= GRAD_TOL[n][1] / 2, (name, N, n, mn)
 
 
 @pytest.mark.parametrize("nk", [2, 3, 5])
