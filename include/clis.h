@@ -25,7 +25,8 @@
  *  - All results are deterministic: every floating-point sum has a fixed
  *    order.  (The one place that adds through memory, the KV-chunk merge of
  *    certified heads, adds one value per accumulator element per launch, so
- *    the order is the launch order.)
+ *    the order is the launch order.  The certification combines partial
+ *    maxima with atomic max operations, which are exact in any order.)
  */
 #ifndef CLIS_H
 #define CLIS_H
