@@ -83,6 +83,9 @@ def _load():
         i64, i32, dbl, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
         lib.oracle_certify.argtypes = [i64, i64, i64, i64, vp, vp, vp, i32, dbl, i32, i32, vp, vp]
         lib.oracle_certify.restype = i32
+        lib.oracle_certify_prefix_tiles.argtypes = [i64, i64, i64, i64, vp, vp, vp, i32, dbl, i32, i32, vp, vp,
+                                                    vp]
+        lib.oracle_certify_prefix_tiles.restype = i32
         for name in ("oracle_attn_bf16", "oracle_attn_fp16", "oracle_attn_f64"):
             f = getattr(lib, name)
             f.argtypes = [i64, i64, i64, i64, vp, vp, vp, dbl, i32, i64, vp, vp, vp]
@@ -203,6 +206,32 @@ def certify(q, k, v, scale_log2: float, exp_fmt: str = "bf16", acc_fmt: str = "f
         c = certs[h]
         out.append({f: getattr(c, f) for f, _ in OracleCert._fields_})
     return kbar, out
+
+
+def certify_prefix_tiles(q, k, v, scale_log2: float, tile_rows: int = 256, exp_fmt: str = "bf16",
+                         acc_fmt: str = "fp32"):
+    """Per-prefix certificates of causal heads (Nq == Nk), one per block of
+    ``tile_rows`` query rows: block b is certified when every input of the head
+    is finite and B_b = scale_log2 * max_{i in b} ||q_i|| * max_{j <= last row of
+    b} ||k_j - kbar|| <= C, the head's budget.  Returns (certified, band, B),
+    each [BH, ceil(N / tile_rows)] (int32, int32, float64)."""
+    (qb, fq), (kb, fk), (vb, fv) = (as_bits(t) for t in (q, k, v))
+    if not fq == fk == fv:
+        raise TypeError("q, k, v must share one format")
+    qb, kb, vb = (_heads_first(a) for a in (qb, kb, vb))
+    BH, N, d = qb.shape
+    if kb.shape[1] != N:
+        raise ValueError("per-prefix certificates are for causal heads (Nq == Nk)")
+    nb = -(-N // tile_rows)
+    cert = np.zeros((BH, nb), dtype=np.int32)
+    band = np.zeros((BH, nb), dtype=np.int32)
+    B = np.zeros((BH, nb), dtype=np.float64)
+    rc = _load().oracle_certify_prefix_tiles(BH, N, d, int(tile_rows), _ptr(qb), _ptr(kb), _ptr(vb), IN_FMT[fq],
+                                             float(scale_log2), FMT[exp_fmt], FMT[acc_fmt], _ptr(cert), _ptr(band),
+                                             _ptr(B))
+    if rc != 0:
+        raise ValueError(f"oracle_certify_prefix_tiles rejected its arguments (rc={rc})")
+    return cert, band, B
 
 
 def attention(q, k, v, scale: float, causal: bool = False, rows=None,

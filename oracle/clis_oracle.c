@@ -20,6 +20,9 @@
  *                   step 7; the decision used here is "all inputs finite and
  *                   B_h <= C" (readings listed below).
  *
+ *  oracle_certify_prefix_tiles  per-prefix certificates of causal heads, one
+ *                   per block of query rows (a finer reading; see there).
+ *
  *  oracle_attn_*    O_i = sum_j softmax_j(scale * q_i . k_j) v_j, two passes
  *                   per row (max, then exp/sum/PV), optional causal mask
  *                   (key j visible to query i iff j <= i).  Since a stabiliser
@@ -237,6 +240,102 @@ int oracle_certify(int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
         if (kbar_out)
             for (int64_t c = 0; c < d; c++) kbar_out[h * d + c] = kbar[c];
         free(kbar);
+    }
+    return 0;
+}
+
+/* Per-prefix certificates for causal attention (Nq == Nk), one per block of
+ * tile_rows consecutive query rows.  Reading (the pages certify causal heads
+ * with the head's bound and state no finer rule): a causal row i sees keys
+ * 0..i only, so |scale_log2 q_i . (k_j - kbar)| <= scale_log2 ||q_i|| kappa_i
+ * with kappa_i = max_{j <= i} ||k_j - kbar||.  Over the rows of block b this
+ * gives B_b = scale_log2 * max_{i in b} ||q_i|| * max_{j <= last row of b}
+ * ||k_j - kbar||, compared with the head's budget C (steps 5-7 over the whole
+ * head).  kbar is the head's mean, as the stabiliser mu_i uses it.
+ * Outputs [BH][nb], nb = ceil(Nq / tile_rows): certified, band, B. */
+int oracle_certify_prefix_tiles(int64_t BH, int64_t N, int64_t d, int64_t tile_rows,
+                                const uint16_t *q, const uint16_t *k, const uint16_t *v, int in_fmt,
+                                double scale_log2, int exp_fmt, int acc_fmt,
+                                int32_t *cert_out, int32_t *band_out, double *B_out)
+{
+    if (in_fmt != ORC_IN_BF16 && in_fmt != ORC_IN_FP16) return 1;
+    if (BH < 0 || N < 1 || d < 1 || tile_rows < 1 || !cert_out || !band_out || !B_out) return 1;
+    if (!isfinite(format_max_finite(exp_fmt)) || !isfinite(format_max_finite(acc_fmt))) return 1;
+    const int64_t nb = (N + tile_rows - 1) / tile_rows;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t h = 0; h < BH; h++) {
+        const uint16_t *qh = q + h * N * d;
+        const uint16_t *kh = k + h * N * d;
+        const uint16_t *vh = v + h * N * d;
+        double *kbar = (double *)malloc((size_t)d * sizeof(double));
+        double *kpre = (double *)malloc((size_t)N * sizeof(double));
+        int finite = 1;
+        for (int64_t c = 0; c < d; c++) kbar[c] = 0.0;
+        for (int64_t r = 0; r < N; r++)
+            for (int64_t c = 0; c < d; c++) {
+                double x = bits_to_double(kh[r * d + c], in_fmt);
+                if (!isfinite(x)) finite = 0;
+                kbar[c] += x;
+            }
+        for (int64_t c = 0; c < d; c++) kbar[c] /= (double)N;
+        /* prefix maxima of the centred key norms */
+        double run = 0.0;
+        for (int64_t r = 0; r < N; r++) {
+            double ss = 0.0;
+            for (int64_t c = 0; c < d; c++) {
+                double t = bits_to_double(kh[r * d + c], in_fmt) - kbar[c];
+                ss += t * t;
+            }
+            double nrm = sqrt(ss);
+            if (nrm > run) run = nrm;
+            kpre[r] = run;
+        }
+        double m = 0.0;
+        for (int64_t r = 0; r < N; r++)
+            for (int64_t c = 0; c < d; c++) {
+                double x = bits_to_double(vh[r * d + c], in_fmt);
+                if (!isfinite(x)) finite = 0;
+                else if (fabs(x) > m) m = fabs(x);
+            }
+        int32_t C = 0;
+        if (finite) {
+            int32_t A = oracle_ceil_log2_count(N) + oracle_v_exponent(m);
+            C = oracle_exponent_budget(exp_fmt, acc_fmt, A);
+        }
+        for (int64_t b = 0; b < nb; b++) {
+            const int64_t r0 = b * tile_rows;
+            const int64_t r1 = (r0 + tile_rows < N) ? r0 + tile_rows : N;
+            double qmax = 0.0;
+            for (int64_t r = r0; r < r1; r++) {
+                double ss = 0.0;
+                for (int64_t c = 0; c < d; c++) {
+                    double x = bits_to_double(qh[r * d + c], in_fmt);
+                    if (!isfinite(x)) finite = 0;
+                    ss += x * x;
+                }
+                double nrm = sqrt(ss);
+                if (nrm > qmax) qmax = nrm;
+            }
+            const int64_t o = h * nb + b;
+            B_out[o] = scale_log2 * qmax * kpre[r1 - 1];
+            cert_out[o] = 0;
+            band_out[o] = 0;
+        }
+        /* a non-finite value anywhere in the head (Q rows of later blocks
+         * included) leaves every block uncertified */
+        for (int64_t b = 0; b < nb && finite; b++) {
+            const int64_t o = h * nb + b;
+            const double B = B_out[o];
+            cert_out[o] = (B <= (double)C) ? 1 : 0;
+            int lo = B * (1.0 - ldexp(1.0, -12)) <= (double)C;
+            int hi = B * (1.0 + ldexp(1.0, -12)) <= (double)C;
+            band_out[o] = (lo != hi);
+        }
+        if (!finite)
+            for (int64_t b = 0; b < nb; b++) B_out[h * nb + b] = INFINITY;
+        free(kbar);
+        free(kpre);
     }
     return 0;
 }

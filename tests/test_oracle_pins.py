@@ -423,3 +423,76 @@ def test_centred_scores_have_nonnegative_row_max_and_stay_within_bound(oracle_mo
         assert np.exp2(x).sum(axis=1).min() >= 1.0 - 1e-12
         assert np.abs(x).max() <= certs[h]["B_h"] * (1 + 1e-12)
         assert np.abs(x).max() >= 0.25 * certs[h]["B_h"]  # and not vacuous (a few-fold inflated B_h fails)
+
+
+# ---------------------------------------------------------------------------
+# Per-prefix certificates of causal heads (one per block of query rows)
+
+
+def _prefix_head(a, b, c, d=64, N=512):
+    """Keys of rows 0-255 at +-a e1 in pairs and of rows 256-511 at +-b e1, so kbar = 0
+    exactly and the prefix maxima of ||k - kbar|| are a (first block) and b (second);
+    every query is c e1.  V = 0.5 everywhere (G = 0)."""
+    k = torch.zeros(1, N, d)
+    k[0, 0:256:2, 0], k[0, 1:256:2, 0] = a, -a
+    k[0, 256::2, 0], k[0, 257::2, 0] = b, -b
+    q = torch.zeros(1, N, d)
+    q[0, :, 0] = c
+    v = torch.full((1, N, d), 0.5)
+    return tuple(t.to(torch.bfloat16) for t in (q, k, v))
+
+
+@pytest.mark.parametrize("c,first_certified", [(59.0, 1), (59.25, 0)])
+def test_prefix_tiles_hand_built(oracle_mod, c, first_certified):
+    """N = 512, G = 0: A = 9, C = 127 - 9 = 118.  B_0 = c * 2 and B_1 = c * 8 with
+    scale_log2 = 1: c = 59 puts block 0 exactly on the budget (a tie certifies) while
+    the head (B_h = 472) fails; c = 59.25 fails block 0 as well."""
+    q, k, v = _prefix_head(2.0, 8.0, c)
+    cert, band, B = oracle_mod.certify_prefix_tiles(q, k, v, 1.0)
+    _, heads = oracle_mod.certify(q, k, v, 1.0)
+    assert heads[0]["C"] == 118 and heads[0]["certified"] == 0 and heads[0]["B_h"] == c * 8
+    np.testing.assert_array_equal(B[0], [c * 2, c * 8])
+    np.testing.assert_array_equal(cert[0], [first_certified, 0])
+
+
+def test_prefix_tiles_bound_every_visible_exponent(oracle_mod):
+    """What a block certificate promises, checked by enumeration: in a certified
+    block every causal exp2 argument scale_log2 q_i . (k_j - kbar), j <= i, lies in
+    [-C, C]; and the block bounds never exceed the head's bound."""
+    gen = torch.Generator().manual_seed(17)
+    BH, N, d, T = 6, 96, 16, 16
+    q = torch.randn(BH, N, d, generator=gen)
+    k = torch.randn(BH, N, d, generator=gen) * 0.5
+    k[:, 72:] += 10.0  # the last quarter of the keys sits far from the rest
+    v = torch.randn(BH, N, d, generator=gen)
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    sl2 = 0.9
+    cert, _, B = oracle_mod.certify_prefix_tiles(q, k, v, sl2, tile_rows=T)
+    kbar, heads = oracle_mod.certify(q, k, v, sl2)
+    qd, kd = q.double().numpy(), k.double().numpy()
+    n_cert = 0
+    for h in range(BH):
+        C = heads[h]["C"]
+        assert np.all(B[h] <= heads[h]["B_h"] * (1 + 1e-12))
+        if heads[h]["certified"]:
+            assert cert[h].all()
+        x = sl2 * qd[h] @ (kd[h] - kbar[h]).T
+        for b in range(cert.shape[1]):
+            rows = range(b * T, min(N, (b + 1) * T))
+            worst = max(np.abs(x[i, :i + 1]).max() for i in rows)
+            assert worst <= B[h, b] * (1 + 1e-12)
+            if cert[h, b]:
+                n_cert += 1
+                assert worst <= C
+    # the far keys only enter the last blocks' prefixes: early blocks certify, late ones not,
+    # and no head certifies as a whole
+    assert 0 < n_cert < cert.size
+    assert not any(hd["certified"] for hd in heads)
+
+
+def test_prefix_tiles_nonfinite_head(oracle_mod):
+    q, k, v = _prefix_head(1.0, 1.0, 1.0)
+    q = q.clone()
+    q[0, 300, 5] = float("nan")  # a row of the second block
+    cert, _, B = oracle_mod.certify_prefix_tiles(q, k, v, 1.0)
+    assert not cert.any() and np.all(np.isinf(B))
