@@ -56,9 +56,10 @@ def parse():
     ap.add_argument("--variant", default="auto", choices=["auto", "online", "certified", "online_lazy"])
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"],
                     help="element type of Q, K, V, P and O (fp16 certifies with the FP16 exp2 budget)")
-    ap.add_argument("--extras", default="all", choices=["all", "none", "backward", "chunks", "e2e"],
+    ap.add_argument("--extras", default="all", choices=["all", "none", "backward", "chunks", "e2e", "tiles"],
                     help="legs after the headline step: all (online variants, ring-step chunks, backward, e2e, "
-                         "CPU baseline), none, or only the backward, the ring-step chunks or the e2e leg (profiling runs)")
+                         "CPU baseline, per-prefix certificates for causal configs), none, or only the backward, the "
+                         "ring-step chunks, the e2e leg or the per-prefix leg (profiling runs)")
     ap.add_argument("--no-extras", action="store_true", help="same as --extras none")
     return ap.parse_args()
 
@@ -352,6 +353,33 @@ def main():
         line["online_lazy"] = {"value": flops / (statistics.mean(lz_attn) * 1e-3) / 1e12, "unit": "TFLOP/s",
                                "ms": statistics.mean(lz_attn)}
         line["certified_speedup_vs_online_lazy"] = statistics.mean(lz_attn) / attn_avg_ms
+    if extras in ("all", "tiles") and w.causal:
+        # Per-prefix certificates (clis_certify_tiles + clis_attn_fwd_tiles): query
+        # blocks of heads that fail as a whole still take the fixed stabiliser
+        # when their prefix certifies.  Same inputs, same timing as the step.
+        nqb = -(-w.N // 256)
+        tiles = torch.empty((heads, nqb), dtype=torch.uint8, device=dev)
+        tev = []
+        for i in range(args.warmup + args.steps):
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            clis.clis_certify_tiles(q, k, v, sl2, kbar=kbar, certs=certs, tile_certs=tiles, workspace=wsp, mu=mu,
+                                    exp_fmt=exp_fmt)
+            e1.record(stream)
+            clis.clis_attn_fwd_tiles(q, k, v, sl2, kbar, certs, tiles, out=out, mu=mu)
+            e2.record(stream)
+            if i >= args.warmup:
+                tev.append((e0, e1, e2))
+        torch.cuda.synchronize()
+        t_step = statistics.mean(a.elapsed_time(c) for a, _, c in tev)
+        t_attn = statistics.mean(b.elapsed_time(c) for _, b, c in tev)
+        n_heads_cert = sum(c["certified"] for c in clis.decode_certs(certs))
+        line["per_prefix"] = {
+            "value": flops / (t_step * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": t_step,
+            "attention_only": flops / (t_attn * 1e-3) / 1e12,
+            "certified_blocks": f"{int(tiles.sum().item())}/{heads * nqb}",
+            "blocks_of_certified_heads": f"{n_heads_cert * nqb}/{heads * nqb}",
+            "speedup_vs_per_head_step": ms_per_step / t_step}
     if extras in ("all", "chunks"):
         # Ring-step form: K/V in 8 chunks, each merged into fp32 accumulators
         # (clis_attn_fwd_chunk), then clis_attn_chunk_finalize.  Certified heads

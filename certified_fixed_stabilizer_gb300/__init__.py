@@ -12,7 +12,8 @@ from __future__ import annotations
 import importlib
 
 _BINDING_NAMES = {
-    "clis_certify", "clis_certify_workspace_size", "clis_certify_noalloc", "clis_attn_fwd",
+    "clis_certify", "clis_certify_workspace_size", "clis_certify_noalloc", "clis_certify_tiles", "clis_attn_fwd",
+    "clis_attn_fwd_tiles",
     "clis_status_string", "clis_get_device_error", "clis_clear_device_error",
     "ClisError", "attention", "certify", "Cert", "VARIANT", "FMT", "STATUS",
     "library_path", "load_library", "decode_certs", "make_shape", "scale_log2_for",

@@ -69,6 +69,10 @@ def load_library():
     lib.clis_certify.restype = i32
     lib.clis_certify_noalloc.argtypes = [sp, vp, vp, vp, f32, i32, i32, vp, vp, vp, vp]
     lib.clis_certify_noalloc.restype = i32
+    lib.clis_certify_tiles.argtypes = [sp, vp, vp, vp, f32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+    lib.clis_certify_tiles.restype = i32
+    lib.clis_attn_fwd_tiles.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp]
+    lib.clis_attn_fwd_tiles.restype = i32
     lib.clis_attn_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp]
     lib.clis_attn_fwd.restype = i32
     lib.clis_status_string.argtypes = [i32]
@@ -174,6 +178,48 @@ def clis_certify_noalloc(q, k, v, scale_log2: float, exp_fmt: str = "bf16", acc_
     if st != 0:
         raise ClisError("clis_certify_noalloc", st)
     return kbar, certs
+
+
+def clis_certify_tiles(q, k, v, scale_log2: float, exp_fmt: str = "bf16", acc_fmt: str = "fp32",
+                       kbar=None, certs=None, tile_certs=None, workspace=None, stream=None, mu=None):
+    """clis_certify plus per-prefix certificates of causal heads (Nq == Nk): one
+    uint8 flag per block of 256 query rows.  Returns (kbar, certs, tile_certs
+    uint8 [B*H, ceil(Nq / 256)])."""
+    lib = load_library()
+    shape = make_shape(q, k, v)
+    BH, d = shape.B * shape.H, shape.d
+    dev = q.device
+    if kbar is None:
+        kbar = torch.empty((max(BH, 1), d), dtype=torch.float32, device=dev)
+    if certs is None:
+        certs = torch.empty((max(BH, 1), CERT_WORDS), dtype=torch.int32, device=dev)
+    if tile_certs is None:
+        tile_certs = torch.empty((max(BH, 1), max(1, -(-shape.Nq // 256))), dtype=torch.uint8, device=dev)
+    need = clis_certify_workspace_size(shape)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    st = lib.clis_certify_tiles(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), float(scale_log2),
+                                FMT[exp_fmt], FMT[acc_fmt], _ptr(kbar), _ptr(certs), _ptr(mu), _ptr(tile_certs),
+                                _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != 0:
+        raise ClisError("clis_certify_tiles", st)
+    return kbar, certs, tile_certs
+
+
+def clis_attn_fwd_tiles(q, k, v, scale_log2: float, kbar, certs, tile_certs, out=None, lse2=None, stream=None,
+                        mu=None):
+    """Causal AUTO forward that lets query blocks certified by their prefix
+    (clis_certify_tiles) take the fixed stabiliser; returns ``out``."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    shape = make_shape(q, k, v, out)
+    st = lib.clis_attn_fwd_tiles(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse2),
+                                 _ptr(kbar), _ptr(certs), _ptr(tile_certs), _ptr(mu), float(scale_log2), 1,
+                                 VARIANT["auto"], _stream(stream))
+    if st != 0:
+        raise ClisError("clis_attn_fwd_tiles", st)
+    return out
 
 
 def clis_attn_fwd(q, k, v, scale_log2: float, kbar=None, certs=None, causal: bool = False,

@@ -92,6 +92,7 @@ struct Params {
     // chunk (overwrite).
     int chunk_mode;
     float *o_acc, *l_acc, *m_acc;
+    const uint8_t *tile_certs;  // optional per-prefix certificates [B*H][nqb] (causal AUTO)
 };
 
 struct __align__(8) Ctl {
@@ -164,6 +165,12 @@ __device__ __forceinline__ Tile decode_tile(const Params &p, int tile)
             const int cc = __ldg(&p.certs[t.bh].C);
             t.cert = bh <= static_cast<float>(cc < 15 ? cc : 15);
         }
+        // A causal head that failed as a whole can still certify this query
+        // block by its prefix (its rows see keys up to the block's end only);
+        // with FP16 P only if the head's budget already respects 2^15.
+        if (CAUSAL && !t.cert && p.tile_certs)
+            t.cert = __ldg(&p.tile_certs[static_cast<int64_t>(t.bh) * p.nqb + t.qb]) != 0 &&
+                     (!DT || __ldg(&p.certs[t.bh].C) <= 15);
     }
     return t;
 }
@@ -848,6 +855,7 @@ clis_status_t launch_impl(const AttnArgs &a, cudaStream_t stream)
     p.kbar = a.kbar;
     p.certs = a.certs;
     p.mu = a.mu;
+    p.tile_certs = a.tile_certs;
     p.q_sb = a.q_sb;
     p.q_sh = a.q_sh;
     p.q_sn = a.q_sn;

@@ -200,7 +200,10 @@ __global__ void __launch_bounds__(kCertThreads) certify_norms_kernel(CertArgs a,
             mx = fmaxf(mx, ss);
         }
         const uint32_t m = block_max_u32(__float_as_uint(mx), redu);
-        if (threadIdx.x == 0) atomicMax(&ws.knorm2[static_cast<int64_t>(bh) * a.nck + part], m);
+        if (threadIdx.x == 0) {
+            atomicMax(&ws.knorm2[static_cast<int64_t>(bh) * a.nck + part], m);
+            ws.knorm2s[static_cast<int64_t>(bh) * kCertNormSplit * a.nck + sub] = m;
+        }
     } else if (kind == 1) {
         const uint16_t *base = a.q + b * a.q_sb + h * a.q_sh + cv * 8;
         float mx = 0.f;
@@ -240,6 +243,7 @@ __global__ void __launch_bounds__(kCertThreads) certify_norms_kernel(CertArgs a,
         if (threadIdx.x == 0) {
             atomicMax(&ws.qnorm2[static_cast<int64_t>(bh) * a.ncq + part], m);
             atomicMax(&ws.qabs[static_cast<int64_t>(bh) * a.ncq + part], am);
+            ws.qnorm2s[static_cast<int64_t>(bh) * kCertNormSplit * a.ncq + sub] = m;
         }
     } else {
         const uint16_t *base = a.v + b * a.v_sb + h * a.v_sh + cv * 8;
@@ -321,6 +325,22 @@ __global__ void certify_finalize_kernel(CertArgs a, CertWorkspace ws, int BH)
         c.reason = c.certified ? 0 : 1;
     }
     a.certs[bh] = c;
+    if (a.tile_certs) {
+        // Per-prefix certificates of a causal head: query block b (rows 256b ..
+        // 256b + 255) sees keys 0 .. 256b + 255 only, so its bound takes the
+        // block's largest query norm and the largest centred key norm of that
+        // prefix, rounded up as B_h is; it is compared with the head's budget C.
+        uint8_t *tc = a.tile_certs + bh * a.nqb;
+        const uint32_t *ks = ws.knorm2s + bh * kCertNormSplit * a.nck;
+        const uint32_t *qs = ws.qnorm2s + bh * kCertNormSplit * a.ncq;
+        uint32_t kpre = 0;
+        for (int b = 0; b < a.nqb; b++) {
+            kpre = max(kpre, ks[b]);
+            const float Bb = __fmul_ru(__fmul_ru(a.scale_log2, __fsqrt_ru(__uint_as_float(qs[b]))),
+                                       __fsqrt_ru(__uint_as_float(kpre)));
+            tc[b] = (finite && Bb <= static_cast<float>(c.C)) ? 1 : 0;
+        }
+    }
 }
 
 }  // namespace
@@ -341,6 +361,10 @@ size_t cert_workspace_layout(int64_t BH, int64_t nck, int64_t ncq, int64_t d, vo
     off = up(off + static_cast<size_t>(BH * ncq) * 4);
     const size_t o_vabs = off;
     off = up(off + static_cast<size_t>(BH * nck) * 4);
+    const size_t o_knorms = off;
+    off = up(off + static_cast<size_t>(BH * kCertNormSplit * nck) * 4);
+    const size_t o_qnorms = off;
+    off = up(off + static_cast<size_t>(BH * kCertNormSplit * ncq) * 4);
     if (ws && base) {
         char *p = static_cast<char *>(base);
         ws->ksum = reinterpret_cast<float *>(p + o_ksum);
@@ -349,6 +373,8 @@ size_t cert_workspace_layout(int64_t BH, int64_t nck, int64_t ncq, int64_t d, vo
         ws->kabs = reinterpret_cast<uint32_t *>(p + o_kabs);
         ws->qabs = reinterpret_cast<uint32_t *>(p + o_qabs);
         ws->vabs = reinterpret_cast<uint32_t *>(p + o_vabs);
+        ws->knorm2s = reinterpret_cast<uint32_t *>(p + o_knorms);
+        ws->qnorm2s = reinterpret_cast<uint32_t *>(p + o_qnorms);
     }
     return off;
 }

@@ -61,10 +61,14 @@ clis_status_t clis_certify_workspace_size(const clis_shape_t *shape, size_t *byt
     return CLIS_OK;
 }
 
-clis_status_t clis_certify(const clis_shape_t *shape, const void *q, const void *k, const void *v,
+}  // extern "C"
+
+namespace {
+
+clis_status_t certify_impl(const clis_shape_t *shape, const void *q, const void *k, const void *v,
                            float scale_log2, clis_fmt_t exp_fmt, clis_fmt_t acc_fmt, float *kbar,
-                           clis_head_cert_t *certs, float *mu, void *workspace, size_t ws_bytes,
-                           clis_stream_t stream)
+                           clis_head_cert_t *certs, float *mu, uint8_t *tile_certs, void *workspace,
+                           size_t ws_bytes, clis_stream_t stream)
 {
     clis_status_t st = check_shape(shape, false);
     if (st != CLIS_OK) return st;
@@ -109,16 +113,47 @@ clis_status_t clis_certify(const clis_shape_t *shape, const void *q, const void 
     a.kbar = kbar;
     a.certs = certs;
     a.mu = mu;
-    if (BH * (2 * a.nck + a.ncq) > kMaxN) return CLIS_ERR_UNSUPPORTED;
+    a.tile_certs = tile_certs;
+    a.nqb = static_cast<int>(div_up(shape->Nq, 256));
+    if (clis::kCertNormSplit * BH * (2 * a.nck + a.ncq) > kMaxN) return CLIS_ERR_UNSUPPORTED;
     clis::CertWorkspace ws;
     clis::cert_workspace_layout(BH, a.nck, a.ncq, a.d, workspace, &ws);
     return clis::launch_certify(a, ws, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? CLIS_OK
                                                                                               : CLIS_ERR_CUDA;
 }
 
-clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, const void *k, const void *v, void *o,
-                            float *lse2, const float *kbar, const clis_head_cert_t *certs, const float *mu,
-                            float scale_log2, int causal, clis_variant_t variant, clis_stream_t stream)
+}  // namespace
+
+extern "C" {
+
+clis_status_t clis_certify(const clis_shape_t *shape, const void *q, const void *k, const void *v,
+                           float scale_log2, clis_fmt_t exp_fmt, clis_fmt_t acc_fmt, float *kbar,
+                           clis_head_cert_t *certs, float *mu, void *workspace, size_t ws_bytes,
+                           clis_stream_t stream)
+{
+    return certify_impl(shape, q, k, v, scale_log2, exp_fmt, acc_fmt, kbar, certs, mu, nullptr, workspace,
+                        ws_bytes, stream);
+}
+
+clis_status_t clis_certify_tiles(const clis_shape_t *shape, const void *q, const void *k, const void *v,
+                                 float scale_log2, clis_fmt_t exp_fmt, clis_fmt_t acc_fmt, float *kbar,
+                                 clis_head_cert_t *certs, float *mu, uint8_t *tile_certs, void *workspace,
+                                 size_t ws_bytes, clis_stream_t stream)
+{
+    if (!shape || !tile_certs) return CLIS_ERR_INVALID_ARG;
+    if (shape->Nq != shape->Nk) return CLIS_ERR_UNSUPPORTED;  // per-prefix: causal heads only
+    return certify_impl(shape, q, k, v, scale_log2, exp_fmt, acc_fmt, kbar, certs, mu, tile_certs, workspace,
+                        ws_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+clis_status_t attn_fwd_impl(const clis_shape_t *shape, const void *q, const void *k, const void *v, void *o,
+                            float *lse2, const float *kbar, const clis_head_cert_t *certs,
+                            const uint8_t *tile_certs, const float *mu, float scale_log2, int causal,
+                            clis_variant_t variant, clis_stream_t stream)
 {
     clis_status_t st = check_shape(shape, true);
     if (st != CLIS_OK) return st;
@@ -167,9 +202,32 @@ clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, const void
     a.scale_log2 = scale_log2;
     a.causal = causal;
     a.variant = variant;
+    a.tile_certs = tile_certs;
     const int64_t tiles = shape->B * shape->H * div_up(shape->Nq, 256);
     if (tiles > kMaxN) return CLIS_ERR_UNSUPPORTED;
     return clis::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, const void *k, const void *v, void *o,
+                            float *lse2, const float *kbar, const clis_head_cert_t *certs, const float *mu,
+                            float scale_log2, int causal, clis_variant_t variant, clis_stream_t stream)
+{
+    return attn_fwd_impl(shape, q, k, v, o, lse2, kbar, certs, nullptr, mu, scale_log2, causal, variant, stream);
+}
+
+clis_status_t clis_attn_fwd_tiles(const clis_shape_t *shape, const void *q, const void *k, const void *v, void *o,
+                                  float *lse2, const float *kbar, const clis_head_cert_t *certs,
+                                  const uint8_t *tile_certs, const float *mu, float scale_log2, int causal,
+                                  clis_variant_t variant, clis_stream_t stream)
+{
+    if (!shape || !tile_certs) return CLIS_ERR_INVALID_ARG;
+    if (!causal || variant != CLIS_AUTO) return CLIS_ERR_INVALID_ARG;  // per-prefix: causal AUTO only
+    return attn_fwd_impl(shape, q, k, v, o, lse2, kbar, certs, tile_certs, mu, scale_log2, causal, variant,
+                         stream);
 }
 
 clis_status_t clis_certify_noalloc(const clis_shape_t *shape, const void *q, const void *k, const void *v,

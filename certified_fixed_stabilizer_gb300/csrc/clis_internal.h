@@ -24,6 +24,10 @@ struct CertWorkspace {
     uint32_t *kabs;    // [BH][nck]     per-chunk max of |k| as bf16 bits (& 0x7FFF)
     uint32_t *qabs;    // [BH][ncq]
     uint32_t *vabs;    // [BH][nck]
+    // Per 256-row block (kCertChunkRows / kCertNormSplit rows) maxima of the
+    // norms pass, for the per-prefix certificates of causal heads.
+    uint32_t *knorm2s;  // [BH][kCertNormSplit * nck]
+    uint32_t *qnorm2s;  // [BH][kCertNormSplit * ncq]
 };
 
 struct CertArgs {
@@ -37,6 +41,8 @@ struct CertArgs {
     float *kbar;
     clis_head_cert_t *certs;
     float *mu;  // optional per-row stabilisers [B*H*Nq]
+    uint8_t *tile_certs = nullptr;  // optional per-prefix certificates [B*H][nqb] (causal, Nq == Nk)
+    int nqb = 0;                    // 256-row query blocks per head
 };
 
 // Carves the workspace for the given sizes; returns the bytes needed.
@@ -58,6 +64,7 @@ struct AttnArgs {
     const float *kbar;
     const clis_head_cert_t *certs;
     const float *mu = nullptr;  // optional per-row stabilisers from clis_certify
+    const uint8_t *tile_certs = nullptr;  // optional per-prefix certificates (causal AUTO)
     int64_t q_sb, q_sh, q_sn, k_sb, k_sh, k_sn, v_sb, v_sh, v_sn, o_sb, o_sh, o_sn;
     int B, H, Nq, Nk, d;
     int dtype = CLIS_DT_BF16;

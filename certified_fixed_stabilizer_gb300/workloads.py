@@ -37,6 +37,7 @@ class Workload:
     outlier_frac: float = 0.0  # fraction of key rows scaled in an injected head
     outlier_scale: float = 64.0
     v_inject_max: float = 4096.0  # largest |V| entry planted in an injected head
+    late_outliers: bool = False   # outlier keys are the head's last rows instead of random ones
     seed: int = 0
     note: str = field(default="", compare=False)
 
@@ -76,6 +77,14 @@ WORKLOADS = {
     "causal": Workload("causal", B=4, H=32, N=8192, d=128, causal=True,
                        q_sigma=1.0, k_sigma=1.0, bias_sigma=math.sqrt(2.0),
                        note="Q,K ~ N(0,1), key bias ~ N(0,2), V ~ N(0,1), causal"),
+    # The causal shape with large keys at the end of a seed-chosen 25% of heads
+    # (the last 1% of rows x 64, plus the mixed workload's V entries): those heads
+    # fail the per-head certificate, while every query block whose prefix ends
+    # before the large keys certifies by its prefix (clis_certify_tiles).
+    "causal_late": Workload("causal_late", B=4, H=32, N=8192, d=128, causal=True,
+                            q_sigma=1.0, k_sigma=1.0, bias_sigma=math.sqrt(2.0),
+                            inject_frac=0.25, outlier_frac=0.01, late_outliers=True,
+                            note="causal distributions, last 1% of keys x64 in 32 of 128 heads"),
 }
 
 
@@ -143,7 +152,10 @@ def _inject(w: Workload, q, k, v, seed: int) -> None:
         b, h = divmod(flat, w.H)
         if h >= H:
             continue
-        rows = torch.randperm(N, generator=g)[:n_out].to(k.device)
+        rows = torch.randperm(N, generator=g)[:n_out]
+        if w.late_outliers:
+            rows = torch.arange(N - n_out, N)
+        rows = rows.to(k.device)
         k[b, h, rows] = (k[b, h, rows].float() * w.outlier_scale).to(k.dtype)
         n_v = 8
         vr = torch.randint(0, N, (n_v,), generator=g)

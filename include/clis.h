@@ -207,6 +207,39 @@ CLIS_API clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, c
                             const clis_head_cert_t *certs, const float *mu, float scale_log2,
                             int causal, clis_variant_t variant, clis_stream_t stream);
 
+/* Per-prefix certificates for causal attention: clis_certify plus one flag per
+ * block of 256 query rows.  The pages certify causal heads with the head's
+ * bound (Table 3) and state no finer rule; this entry point is a finer reading
+ * of the same Cauchy-Schwarz bound.  A causal row i sees keys 0..i only, so
+ * for query block b (rows 256b .. 256b + 255) every exp2 argument is bounded
+ * by B_b = scale_log2 * max_{i in b} ||q_i|| * max_{j <= 256b + 255}
+ * ||k_j - kbar|| (rounded upward as B_h is), and the block is safe when the
+ * head's inputs are finite and B_b <= C, the head's budget.  A certified head
+ * has every block certified; a head that fails can still certify the blocks
+ * whose prefixes exclude its large keys.
+ *   tile_certs  device uint8 out [B*H][ceil(Nq / 256)]: 1 = the block may take
+ *               the fixed stabiliser in clis_attn_fwd_tiles
+ *   (other arguments as for clis_certify; Nq must equal Nk)
+ * Errors as for clis_certify; CLIS_ERR_INVALID_ARG for a null tile_certs,
+ * CLIS_ERR_UNSUPPORTED if Nq != Nk. */
+CLIS_API clis_status_t clis_certify_tiles(const clis_shape_t *shape, const void *q, const void *k,
+                                          const void *v, float scale_log2, clis_fmt_t exp_fmt,
+                                          clis_fmt_t acc_fmt, float *kbar, clis_head_cert_t *certs,
+                                          float *mu, uint8_t *tile_certs, void *workspace,
+                                          size_t ws_bytes, clis_stream_t stream);
+
+/* clis_attn_fwd for causal attention (causal = 1, variant = CLIS_AUTO) that
+ * also takes the per-prefix certificates of clis_certify_tiles: a query block
+ * of a head that failed certification as a whole still takes the fixed
+ * stabiliser when its block flag is set (for FP16 data only if the head's
+ * budget C <= 15).  Errors as for clis_attn_fwd; CLIS_ERR_INVALID_ARG for a
+ * null tile_certs, causal = 0 or another variant. */
+CLIS_API clis_status_t clis_attn_fwd_tiles(const clis_shape_t *shape, const void *q, const void *k,
+                                           const void *v, void *o, float *lse2, const float *kbar,
+                                           const clis_head_cert_t *certs, const uint8_t *tile_certs,
+                                           const float *mu, float scale_log2, int causal,
+                                           clis_variant_t variant, clis_stream_t stream);
+
 /* One KV chunk of a ring / context-parallel attention step (paper: Table 7,
  * the ring and 2D-ring columns, and Figure 6, one ring attention step).  The
  * keys and values of a head are split into chunks that arrive one at a time;

@@ -28,7 +28,7 @@ def test_header_declares_the_boundary():
     for n in ("clis_certify_workspace_size", "clis_certify", "clis_attn_fwd", "clis_status_string",
               "clis_get_device_error", "clis_clear_device_error", "clis_debug_wait_selftest",
               "clis_attn_fwd_chunk", "clis_attn_chunk_finalize", "clis_certify_noalloc",
-              "clis_attn_bwd_workspace_size", "clis_attn_bwd"):
+              "clis_attn_bwd_workspace_size", "clis_attn_bwd", "clis_certify_tiles", "clis_attn_fwd_tiles"):
         assert n in names
 
 
@@ -167,6 +167,26 @@ def test_chunk_entry_points_reject_bad_arguments(clis):
     assert lib.clis_attn_chunk_finalize(ctypes.byref(s), vp(FAKE), vp(FAKE), vp(FAKE), vp(0), None, None) == 1
     s2 = _shape(clis, d=80)
     assert lib.clis_attn_chunk_finalize(ctypes.byref(s2), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, None) == 2
+
+
+def test_tile_entry_points_reject_bad_arguments(clis):
+    """Per-prefix certificates: causal (Nq == Nk) only, AUTO only, tile flags required
+    (rejected on the host, before any launch; the fake pointers are never touched)."""
+    lib = clis.load_library()
+    vp = ctypes.c_void_p
+    s = _shape(clis)
+    cert = lambda shape, tiles=FAKE: lib.clis_certify_tiles(ctypes.byref(shape), vp(FAKE), vp(FAKE), vp(FAKE), 0.1,
+                                                            1, 2, vp(FAKE), vp(FAKE), None, vp(tiles), vp(FAKE),
+                                                            1 << 20, None)
+    assert cert(s, tiles=0) == 1
+    assert cert(_shape(clis, Nq=300, Nk=400)) == 2
+    attn = lambda shape, causal=1, variant=0, tiles=FAKE: lib.clis_attn_fwd_tiles(
+        ctypes.byref(shape), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE), vp(FAKE), vp(tiles), None,
+        0.1, causal, variant, None)
+    assert attn(s, tiles=0) == 1
+    assert attn(s, causal=0) == 1
+    assert attn(s, variant=1) == 1
+    assert attn(_shape(clis, Nq=300, Nk=400)) == 2
 
 
 def _bwd(clis, shape=None, ws_bytes=1 << 20, scale=0.1, causal=0, **ptrs):

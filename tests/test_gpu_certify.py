@@ -62,7 +62,7 @@ def _compare(q, k, v, sl2, exp_fmt="bf16", acc_fmt="fp32", expect_no_band=True):
     return g, oc
 
 
-@pytest.mark.parametrize("name", ["tiny", "480p", "720p", "mixed", "causal"])
+@pytest.mark.parametrize("name", ["tiny", "480p", "720p", "mixed", "causal", "causal_late"])
 def test_workload_certificates_match_oracle(name):
     dev = need_gpu()
     w = WORKLOADS[name]
@@ -70,9 +70,9 @@ def test_workload_certificates_match_oracle(name):
     sl2 = clis.scale_log2_for(w.d)
     g, oc = _compare(q, k, v, sl2)
     flags = [c["certified"] for c in g]
-    if name == "mixed":
+    if w.inject_frac > 0:  # mixed: 16 of 64 heads; causal_late: 32 of 128
         inj = set(injected_heads(w))
-        assert len(inj) == 16
+        assert len(inj) == {"mixed": 16, "causal_late": 32}[name]
         assert flags == [0 if h in inj else 1 for h in range(w.heads)]
         for h in inj:
             assert g[h]["G"] == 12 and g[h]["reason"] == 1
