@@ -276,3 +276,39 @@ def test_workspace_contents_do_not_leak_between_calls():
     for kb, c in ((kb1, c1), (kb2, c2)):
         assert torch.equal(kb, ref_kbar)
         assert torch.equal(c, ref_certs)
+
+
+@pytest.mark.parametrize("H", [2, 7, 13])
+def test_long_heads_with_prefix_flags(H):
+    """Heads of 40,000 keys at d = 64: 40 column-sum chunks and 157 query blocks
+    each, the last ones ragged.  Head 0 has its last 64 keys scaled by 16: it
+    fails as a head while its earlier query blocks certify by their prefix.
+    Certificates, kbar, mu and the per-prefix flags against the oracle."""
+    dev = need_gpu()
+    N, d = 40000, 64
+    g = torch.Generator(device=dev)
+    g.manual_seed(100 + H)
+    q = (torch.randn(1, H, N, d, generator=g, device=dev) * 0.5).to(torch.bfloat16)
+    k = (torch.randn(1, H, N, d, generator=g, device=dev) * 0.7 + 1.5).to(torch.bfloat16)
+    v = (torch.randn(1, H, N, d, generator=g, device=dev) * 3).to(torch.bfloat16)
+    k[0, 0, N - 64:] *= 16  # exactly the last 256-row block's keys (rows 39,936 on)
+    sl2 = clis.scale_log2_for(d)
+    gc, oc = _compare(q, k, v, sl2)
+    assert [c["certified"] for c in gc] == [0] + [1] * (H - 1)
+    mu = torch.full((H * N,), float("nan"), device=dev)
+    kbar, certs, tiles = clis.clis_certify_tiles(q, k, v, sl2, mu=mu)
+    kbar2, certs2 = clis.clis_certify(q, k, v, sl2)
+    torch.cuda.synchronize()
+    assert torch.equal(kbar, kbar2) and torch.equal(certs, certs2)
+    ocert, oband, _ = oracle.certify_prefix_tiles(q.cpu(), k.cpu(), v.cpu(), sl2)
+    t = tiles.cpu().numpy().astype(np.int32)
+    assert not oband.any()
+    np.testing.assert_array_equal(t, ocert)
+    assert t[0, :-1].all() and t[0, -1] == 0 and t[1:].all()
+    okbar, _ = oracle.certify(q, k, v, sl2)
+    qf = oracle.bf16_bits_to_f64(oracle.as_bf16_bits(q)).reshape(H, N, d)
+    ref = sl2 * np.einsum("hnd,hd->hn", qf, okbar)
+    got = mu.cpu().double().numpy().reshape(ref.shape)
+    scale = sl2 * np.linalg.norm(qf, axis=2) * np.linalg.norm(okbar, axis=1)[:, None]
+    assert np.all(np.abs(got - ref) <= 1e-5 * scale + 1e-6)
+
