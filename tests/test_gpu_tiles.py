@@ -147,3 +147,26 @@ def test_causal_late_workload_full_size():
     rows = sample_rows(w.N, 24, seed=7)
     ref = oracle.attention(flat(q).cpu(), flat(k).cpu(), flat(v).cpu(), w.softmax_scale(), causal=True, rows=rows)
     assert_close_to_oracle(flat(o)[:, rows].float().cpu().numpy(), ref, "causal_late with per-prefix certificates")
+
+
+@pytest.mark.parametrize("N", [1, 255, 256, 257, 513])
+def test_tiles_degenerate_and_ragged_sizes(N):
+    """One block (N = 1, 255, 256), a second block of a single row (257) and a
+    ragged third block (513): flags bit-exact against the oracle, and the output
+    of the per-prefix forward against the oracle."""
+    w = dataclasses.replace(WORKLOADS["causal"], B=2)
+    q, k, v = make_inputs(w, device=need_gpu(), N=N, H=3, seed=200 + N)
+    k = k.clone()
+    k[:, 1, -1:] *= 64  # head 1 of each batch: its last key is far out
+    k = k.contiguous()
+    sl2 = clis.scale_log2_for(w.d)
+    kbar, certs, tiles = clis.clis_certify_tiles(q, k, v, sl2)
+    o = clis.clis_attn_fwd_tiles(q, k, v, sl2, kbar, certs, tiles)
+    torch.cuda.synchronize()
+    assert tiles.shape == (6, -(-N // 256))
+    ocert, oband, _ = oracle.certify_prefix_tiles(q.cpu(), k.cpu(), v.cpu(), sl2)
+    g = tiles.cpu().numpy().astype(np.int32)
+    keep = oband == 0
+    np.testing.assert_array_equal(g[keep], ocert[keep])
+    ref = oracle.attention(flat(q).cpu(), flat(k).cpu(), flat(v).cpu(), w.softmax_scale(), causal=True)
+    assert_close_to_oracle(flat(o).float().cpu().numpy(), ref, f"causal N={N} with per-prefix certificates")
