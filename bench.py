@@ -162,8 +162,9 @@ def oracle_sample_step(q, k, v, w, heads, rows):
     """Oracle work for one sampled step: certification of the sampled heads
     (full length) and attention on `rows` of each sampled head."""
     import oracle
-    from certified_fixed_stabilizer_gb300.clis import LOG2E
-    sl2 = w.softmax_scale() * LOG2E
+    # scale_log2 = softmax scale * log2(e), formed here so that the oracle legs
+    # import nothing from the CUDA library's binding.
+    sl2 = w.softmax_scale() * math.log2(math.e)
     qs, ks, vs = (t.reshape(-1, t.shape[2], t.shape[3])[heads] for t in (q, k, v))
     oracle.certify(qs, ks, vs, sl2)
     oracle.attention(qs, ks, vs, w.softmax_scale(), causal=w.causal, rows=rows)
