@@ -3,8 +3,8 @@
 //  * certified (CLiS): the per-row stabiliser mu_i = scale_log2 * (q_i . kbar)
 //    is fixed before the KV loop ("CLiS: Plug-and-Play Attention Acceleration
 //    for Video Diffusion on TPUs via Certified Stabilization", abstract and
-//    Figure 5(a): a loop-invariant stabiliser removes the reduction and
-//    rescaling chain).  p_ij = exp2(scale_log2 * s_ij - mu_i) is accumulated
+//    Figure 5(a): once mu_i is fixed before the loop, the loop carries no
+//    maximum and no rescaling).  p_ij = exp2(scale_log2 * s_ij - mu_i) is accumulated
 //    directly: no row maximum, no alpha, no rescaling of O.  With the
 //    certificate of Algorithm 1 (B_h <= C) every exp2 argument lies in
 //    [-B_h, B_h], so p never overflows the BF16 P operand and the FP32
@@ -48,6 +48,8 @@ namespace {
 
 constexpr int BM = 128;            // rows per query tile
 constexpr int BN = 128;            // keys per KV tile
+// A work tile is two query tiles; per-prefix certificates are kept per work tile.
+static_assert(2 * BM == kQueryBlockRows, "work tile and per-prefix certificate block differ");
 constexpr int kThreads = 512;
 constexpr int kNStageMax = 8;
 // Lazy online softmax keeps a stale row maximum until the true one exceeds it

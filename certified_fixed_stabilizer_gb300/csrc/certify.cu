@@ -379,20 +379,69 @@ size_t cert_workspace_layout(int64_t BH, int64_t nck, int64_t ncq, int64_t d, vo
     return off;
 }
 
-void *certify_static_scratch()
+namespace {
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+// cuCtxGetCurrent through the runtime's driver entry point (no libcuda link).
+CtxGetCurrentFn get_ctx_fn()
 {
-    constexpr int kMaxDevices = 64;
-    static std::mutex mu;
-    static void *addr[kMaxDevices] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    static const CtxGetCurrentFn fn = []() -> CtxGetCurrentFn {
         void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_certify_scratch) != cudaSuccess) return nullptr;
-        addr[dev] = ptr;
+        cudaDriverEntryPointQueryResult qres;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &qres) ==
+                cudaSuccess &&
+            qres == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<CtxGetCurrentFn>(ptr);
+        return nullptr;
+    }();
+    return fn;
+}
+
+}  // namespace
+
+void *certify_static_scratch(cudaStream_t stream)
+{
+    // The array's device address belongs to one context (each context loads
+    // its own copy of the module, and a device reset replaces the primary
+    // context), so addresses are kept per (device, context).  Outside stream
+    // capture the address is looked up afresh on every call; during capture the
+    // one looked up by the last call outside capture in the same context is used.
+    constexpr int kSlots = 64;
+    struct Slot {
+        int dev;
+        CUcontext ctx;
+        void *addr;
+    };
+    static std::mutex mu;
+    static Slot slots[kSlots];
+    static int used = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return nullptr;
+    void *ptr = nullptr;
+    // Outside capture: look the address up first (this also makes the device's
+    // primary context current when the thread has no context yet).
+    if (cs == cudaStreamCaptureStatusNone &&
+        (cudaGetSymbolAddress(&ptr, g_certify_scratch) != cudaSuccess || !ptr))
+        return nullptr;
+    CtxGetCurrentFn ctx_fn = get_ctx_fn();
+    CUcontext ctx = nullptr;
+    if (!ctx_fn || ctx_fn(&ctx) != CUDA_SUCCESS || !ctx) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    int slot = -1;
+    for (int i = 0; i < used; i++)
+        if (slots[i].dev == dev && slots[i].ctx == ctx) slot = i;
+    if (cs != cudaStreamCaptureStatusNone) return slot >= 0 ? slots[slot].addr : nullptr;
+    if (slot < 0) {
+        // Table full (many contexts over the process's life): reuse the first slot.
+        slot = used < kSlots ? used++ : 0;
+        slots[slot].dev = dev;
+        slots[slot].ctx = ctx;
     }
-    return addr[dev];
+    slots[slot].addr = ptr;
+    return ptr;
 }
 
 cudaError_t launch_certify(const CertArgs &a, const CertWorkspace &ws, cudaStream_t stream)

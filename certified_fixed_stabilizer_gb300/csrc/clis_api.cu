@@ -65,10 +65,10 @@ clis_status_t clis_certify_workspace_size(const clis_shape_t *shape, size_t *byt
 
 namespace {
 
-clis_status_t certify_impl(const clis_shape_t *shape, const void *q, const void *k, const void *v,
-                           float scale_log2, clis_fmt_t exp_fmt, clis_fmt_t acc_fmt, float *kbar,
-                           clis_head_cert_t *certs, float *mu, uint8_t *tile_certs, void *workspace,
-                           size_t ws_bytes, clis_stream_t stream)
+// Every check of the certification arguments except the workspace.
+clis_status_t check_certify_args(const clis_shape_t *shape, const void *q, const void *k, const void *v,
+                                 float scale_log2, clis_fmt_t exp_fmt, clis_fmt_t acc_fmt, const float *kbar,
+                                 const clis_head_cert_t *certs, const float *mu)
 {
     clis_status_t st = check_shape(shape, false);
     if (st != CLIS_OK) return st;
@@ -79,6 +79,16 @@ clis_status_t certify_impl(const clis_shape_t *shape, const void *q, const void 
     if ((q && !aligned16(q)) || !aligned16(k) || !aligned16(v) || !aligned16(kbar) || !aligned16(certs) ||
         (mu && (reinterpret_cast<uintptr_t>(mu) & 3u)))
         return CLIS_ERR_MISALIGNED;
+    return CLIS_OK;
+}
+
+clis_status_t certify_impl(const clis_shape_t *shape, const void *q, const void *k, const void *v,
+                           float scale_log2, clis_fmt_t exp_fmt, clis_fmt_t acc_fmt, float *kbar,
+                           clis_head_cert_t *certs, float *mu, uint8_t *tile_certs, void *workspace,
+                           size_t ws_bytes, clis_stream_t stream)
+{
+    const clis_status_t st = check_certify_args(shape, q, k, v, scale_log2, exp_fmt, acc_fmt, kbar, certs, mu);
+    if (st != CLIS_OK) return st;
     size_t need = 0;
     clis_certify_workspace_size(shape, &need);
     if (need > 0 && (!workspace || ws_bytes < need)) return CLIS_ERR_WORKSPACE;
@@ -114,7 +124,7 @@ clis_status_t certify_impl(const clis_shape_t *shape, const void *q, const void 
     a.certs = certs;
     a.mu = mu;
     a.tile_certs = tile_certs;
-    a.nqb = static_cast<int>(div_up(shape->Nq, 256));
+    a.nqb = static_cast<int>(div_up(shape->Nq, clis::kQueryBlockRows));
     if (clis::kCertNormSplit * BH * (2 * a.nck + a.ncq) > kMaxN) return CLIS_ERR_UNSUPPORTED;
     clis::CertWorkspace ws;
     clis::cert_workspace_layout(BH, a.nck, a.ncq, a.d, workspace, &ws);
@@ -203,7 +213,7 @@ clis_status_t attn_fwd_impl(const clis_shape_t *shape, const void *q, const void
     a.causal = causal;
     a.variant = variant;
     a.tile_certs = tile_certs;
-    const int64_t tiles = shape->B * shape->H * div_up(shape->Nq, 256);
+    const int64_t tiles = shape->B * shape->H * div_up(shape->Nq, clis::kQueryBlockRows);
     if (tiles > kMaxN) return CLIS_ERR_UNSUPPORTED;
     return clis::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -234,11 +244,15 @@ clis_status_t clis_certify_noalloc(const clis_shape_t *shape, const void *q, con
                                    float scale_log2, clis_fmt_t exp_fmt, clis_fmt_t acc_fmt, float *kbar,
                                    clis_head_cert_t *certs, float *mu, clis_stream_t stream)
 {
-    size_t need = 0;
-    const clis_status_t st = clis_certify_workspace_size(shape, &need);
+    // Argument errors first, so a shape that is invalid or unsupported reports
+    // that rather than its scratch size.
+    clis_status_t st = check_certify_args(shape, q, k, v, scale_log2, exp_fmt, acc_fmt, kbar, certs, mu);
     if (st != CLIS_OK) return st;
+    size_t need = 0;
+    if ((st = clis_certify_workspace_size(shape, &need)) != CLIS_OK) return st;
     if (need > CLIS_NOALLOC_SCRATCH_BYTES) return CLIS_ERR_WORKSPACE;
-    void *scratch = clis::certify_static_scratch();
+    if (shape->B * shape->H == 0) return CLIS_OK;
+    void *scratch = clis::certify_static_scratch(reinterpret_cast<cudaStream_t>(stream));
     if (!scratch) return CLIS_ERR_CUDA;
     return clis_certify(shape, q, k, v, scale_log2, exp_fmt, acc_fmt, kbar, certs, mu, scratch,
                         CLIS_NOALLOC_SCRATCH_BYTES, stream);
@@ -265,7 +279,7 @@ clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void *q, cons
         (reinterpret_cast<uintptr_t>(l_acc) & 3u) || (reinterpret_cast<uintptr_t>(m_acc) & 3u) ||
         (mu && (reinterpret_cast<uintptr_t>(mu) & 3u)))
         return CLIS_ERR_MISALIGNED;
-    const int64_t tiles = shape->B * shape->H * div_up(shape->Nq, 256);
+    const int64_t tiles = shape->B * shape->H * div_up(shape->Nq, clis::kQueryBlockRows);
     if (tiles > kMaxN) return CLIS_ERR_UNSUPPORTED;
 
     clis::AttnArgs a;

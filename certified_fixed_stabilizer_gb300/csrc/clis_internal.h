@@ -17,6 +17,14 @@ constexpr int kCertChunkRows = 1024;  // rows per partial-reduction chunk
 constexpr int kCertNormSplit = 4;     // norms-kernel blocks per chunk
 constexpr int kCertThreads = 256;
 
+// Query rows per work tile of the attention kernel, which is also the block
+// of the per-prefix certificates: the norms pass keeps one maximum per block
+// of kCertChunkRows / kCertNormSplit rows, and the certificate of query block
+// b is read by the attention work tile with the same rows.
+constexpr int kQueryBlockRows = 256;
+static_assert(kCertChunkRows % kCertNormSplit == 0 && kCertChunkRows / kCertNormSplit == kQueryBlockRows,
+              "per-prefix certificates need one norms block per attention work tile");
+
 struct CertWorkspace {
     float *ksum;       // [BH][nck][d]  per-chunk column sums of K
     uint32_t *knorm2;  // [BH][nck]     per-chunk max of ||k - kbar||^2 (fp32 bits, rounded up)
@@ -51,9 +59,11 @@ size_t cert_workspace_layout(int64_t BH, int64_t nck, int64_t ncq, int64_t d, vo
 
 cudaError_t launch_certify(const CertArgs &a, const CertWorkspace &ws, cudaStream_t stream);
 
-// Device address of the library-owned certification scratch array on the
-// current device (looked up once per device); nullptr on failure.
-void *certify_static_scratch();
+// Device address of the library-owned certification scratch array in the
+// current context: looked up on every call outside stream capture, taken from
+// the last such lookup in the same (device, context) while `stream` is being
+// captured; nullptr on failure or when no lookup was made before the capture.
+void *certify_static_scratch(cudaStream_t stream);
 
 // ---------------------------------------------------------------- attention
 

@@ -57,15 +57,15 @@ typedef enum {
     CLIS_ERR_TIMEOUT = 6       /* a kernel pipeline wait exceeded its limit (device error word) */
 } clis_status_t;
 
-/* Floating-point formats of Figure 3 ("Approximate numerical limits of
- * exp2(x) = 2^x for FP16, BF16, and FP32").  U_exp and U_acc of Algorithm 1
- * step 7 are the exp2 overflow limits of these formats. */
+/* Floating-point formats whose exp2 overflow limits Figure 3 tabulates (FP16,
+ * BF16, FP32).  U_exp and U_acc of Algorithm 1 step 7 are those limits for
+ * the format holding exp2 outputs and for the accumulator format. */
 typedef enum { CLIS_FMT_FP16 = 0, CLIS_FMT_BF16 = 1, CLIS_FMT_FP32 = 2 } clis_fmt_t;
 
 /* Which softmax the attention kernel runs per head:
  *  CLIS_AUTO              certified heads use the fixed stabiliser, the rest
- *                         fall back to online softmax (abstract: "falling back
- *                         to online softmax when certification fails");
+ *                         fall back to online softmax (the fallback the
+ *                         abstract describes for heads that fail);
  *  CLIS_ONLINE            every head uses online softmax that rescales the
  *                         accumulator after every KV block (the baseline);
  *  CLIS_CERTIFIED_FORCED  every head uses the fixed stabiliser, ignoring the
@@ -126,9 +126,9 @@ typedef struct {
 CLIS_API clis_status_t clis_certify_workspace_size(const clis_shape_t *shape, size_t *bytes);
 
 /* Certification pre-pass, Algorithm 1 steps 1-7 plus the decision, for all
- * B*H heads (paper: Algorithm 1 "CLiS forward pass for one dense attention
- * head", steps 1-7; the decision after step 7 is lost from the text and is
- * read here as "finite inputs and B_h <= C").
+ * B*H heads (Algorithm 1 certifies one dense attention head; here every
+ * (b, h) pair is one such head).  The decision after step 7 is lost from the
+ * text; it is read here as: every input finite and B_h <= C.
  *   q, k, v     device bf16 [B,H,Nq,d] / [B,H,Nk,d] / [B,H,Nk,d]
  *   scale_log2  softmax scale times log2(e) (> 0, finite); scores enter
  *               exp2 as scale_log2 * q.k
@@ -167,27 +167,31 @@ CLIS_API clis_status_t clis_certify(const clis_shape_t *shape, const void *q, co
  * until the process exits.  The caller still provides q, k, v, kbar and
  * certs.  Nothing is allocated or freed, by this call or by any routine it
  * uses.
- *   - The first call on a device (with that device current) looks up the
- *     array's device address with cudaGetSymbolAddress; make that first call
- *     before starting any stream capture on that device.
+ *   - Each call made outside stream capture looks up the array's device
+ *     address in the current context with cudaGetSymbolAddress (the first
+ *     such call on a device does this set-up; it allocates nothing).  A call
+ *     made while `stream` is being captured uses the address found by the last
+ *     call outside capture in the same context, so make one call on each
+ *     device (and again after a device reset) before capturing; without one
+ *     the call returns CLIS_ERR_CUDA.
  *   - All calls share the one array and it keeps what the last call left in
  *     it.  The kernels overwrite every scratch word they read, so nothing
  *     needs clearing between calls, but calls that overlap on the GPU (two
  *     streams, two host threads) race on it: serialise them.
- *   - Shapes whose clis_certify_workspace_size() exceeds
+ *   - Arguments are checked first, with the statuses of clis_certify.  Then
+ *     shapes whose clis_certify_workspace_size() exceeds
  *     CLIS_NOALLOC_SCRATCH_BYTES return CLIS_ERR_WORKSPACE before anything
  *     is launched (about B*H*ceil(Nk/1024)*d*4 bytes; B*H = 40 heads of
  *     75,600 keys at d = 128 need 1.6 MB).
- *   - CLIS_ERR_CUDA if the address lookup fails; argument errors as in
- *     clis_certify. */
+ *   - CLIS_ERR_CUDA if the address lookup fails. */
 CLIS_API clis_status_t clis_certify_noalloc(const clis_shape_t *shape, const void *q, const void *k,
                                    const void *v, float scale_log2, clis_fmt_t exp_fmt,
                                    clis_fmt_t acc_fmt, float *kbar, clis_head_cert_t *certs,
                                    float *mu, clis_stream_t stream);
 
-/* Fused attention forward O = softmax(scale * Q K^T) V (paper: abstract and
- * Figure 5(a), "a loop-invariant stabilizer mu_i removes the reduction and
- * rescaling chain").  One persistent kernel; each 256-row query block of a
+/* Fused attention forward O = softmax(scale * Q K^T) V (abstract and
+ * Figure 5(a): with mu_i fixed before the KV loop, the loop needs no running
+ * maximum and no rescaling).  One persistent kernel; each 256-row query block of a
  * head runs either
  *   - the certified path: mu_i = scale_log2 * (q_i . kbar) fixed before the
  *     KV loop, p_ij = exp2(scale_log2 * s_ij - mu_i), no row maximum, no

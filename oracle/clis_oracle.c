@@ -35,8 +35,9 @@
  *                   algorithm; this is the plain chain rule through softmax.
  *
  * Readings of the pages (where they are silent or garbled):
- *  - kappa ("a conservative upper bound on max_r ||k~_r||_2", Alg. 1 step 3):
- *    the oracle computes the exact fp64 maximum of the centred key norms.
+ *  - kappa (Alg. 1 step 3 asks only for an upper bound of the largest centred
+ *    key norm, without saying how tight): the oracle computes the exact fp64
+ *    maximum of the centred key norms.
  *  - BoundUp (Alg. 1 step 4, never defined): Cauchy-Schwarz,
  *    BoundUp(q, kappa) = scale_log2 * ||q||_2 * kappa, so B_h is a bound on
  *    |scale_log2 * q_r . (k_j - kbar)| in exp2-argument units.
