@@ -1,0 +1,63 @@
+"""Rounding model of the certified forward and of the backward kernels (test
+infrastructure; CPU, numpy fp64).
+
+The kernels compute in fp32 and round to the input format (bf16) at a few
+fixed points.  This module applies exactly those roundings to an otherwise
+fp64 computation, so its results differ from the kernels' only by fp32
+accumulation order and the hardware exp2 (relative 1e-6 or less on any
+intermediate) and by the bf16 roundings those differences tip over.  It is
+written from the arithmetic each kernel performs, not from the kernels' code,
+and is used two ways: to derive the fp64-oracle tolerances (how far these
+roundings alone move a result from the exact one) and, in the tight GPU
+checks, as the element-wise reference for the kernels themselves.
+
+Rounding points:
+  forward (certified path): p = exp2(scale_log2 * s - mu_i) with
+      mu_i = scale_log2 * (q_i . kbar); P rounded to bf16 for the P V product;
+      row sum l of the unrounded p; O = O_acc / l rounded to bf16 once;
+      lse2 = mu_i + log2 l in fp32.
+  backward: P = exp2(scale_log2 * s - lse2_i) from the given lse2; P rounded
+      to bf16 for dV = P^T dO; dS = P (dP - D_i) with the unrounded P, rounded
+      to bf16 for dQ = scale dS K and dK = scale dS^T Q; D_i = dO_i . O_i from
+      the given (bf16) O; dQ, dK, dV rounded to bf16 once at the end (the
+      functions below return them before that last rounding).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+LOG2E = 1.4426950408889634
+
+
+def bf16(x) -> np.ndarray:
+    """Round to the nearest bf16 value (ties to even); returns float64."""
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def _mask(x: np.ndarray, causal: bool) -> np.ndarray:
+    if not causal:
+        return x
+    nq, nk = x.shape
+    return np.where(np.arange(nk)[None, :] <= np.arange(nq)[:, None], x, -np.inf)
+
+
+def certified_forward(q, k, v, scale: float, causal: bool):
+    """One head: (O as bf16 values, lse2 as fp32 values), both float64 arrays."""
+    sl2 = scale * LOG2E
+    mu = sl2 * (q @ k.mean(axis=0))
+    p = np.exp2(_mask(sl2 * (q @ k.T) - mu[:, None], causal))
+    l = p.sum(axis=1)
+    o = bf16((bf16(p) @ v) / l[:, None])
+    lse2 = (mu + np.log2(l)).astype(np.float32).astype(np.float64)
+    return o, lse2
+
+
+def backward(q, k, v, o, g, lse2, scale: float, causal: bool):
+    """One head: dQ, dK, dV before their final rounding to bf16 (float64)."""
+    sl2 = scale * LOG2E
+    P = np.exp2(_mask(sl2 * (q @ k.T) - lse2[:, None], causal))
+    D = (g * o).sum(axis=1, keepdims=True)
+    dV = bf16(P).T @ g
+    dS = bf16(P * (g @ v.T - D))
+    return scale * (dS @ k), scale * (dS.T @ q), dV

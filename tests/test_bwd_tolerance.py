@@ -25,28 +25,16 @@ import torch
 from certified_fixed_stabilizer_gb300.workloads import WORKLOADS, make_dout, make_inputs
 from gpu_util import GRAD_TOL, grad_errors
 
-LOG2E = 1.4426950408889634
+import rounding_model as rm
 
-
-def _bf(x):
-    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+LOG2E = rm.LOG2E
+_bf = rm.bf16
 
 
 def _emulated_grads(q, k, v, g, scale, causal):
     """dQ, dK, dV of one head with the certified forward's and the backward's roundings."""
-    N = q.shape[0]
-    sl2 = scale * LOG2E
-    mu = sl2 * (q @ k.mean(axis=0))  # fixed per-row stabiliser
-    x = sl2 * (q @ k.T) - mu[:, None]
-    if causal:
-        x = np.where(np.tril(np.ones((N, N))) > 0, x, -np.inf)
-    p = np.exp2(x)
-    l = p.sum(axis=1, keepdims=True)
-    O = _bf((_bf(p) @ v) / l)         # forward output: P rounded for P V, fp32 row sum
-    P = p / l
-    dV = _bf(_bf(P).T @ g)            # P rounded for the matmul
-    dS = _bf(P * (g @ v.T - (g * O).sum(axis=1, keepdims=True)))
-    return _bf(scale * (dS @ k)), _bf(scale * (dS.T @ q)), dV
+    o, lse2 = rm.certified_forward(q, k, v, scale, causal)
+    return tuple(_bf(x) for x in rm.backward(q, k, v, o, g, lse2, scale, causal))
 
 
 @pytest.mark.parametrize("name,B,H,N,seed", [
@@ -107,3 +95,63 @@ def test_few_key_heads_forward_rounding(nk):
     for c in range(0, 1500, 15):
         _, per_case = head_errors(got[c:c + 15].reshape(1, -1), ref[c:c + 15].reshape(1, -1))
         assert per_case[0] <= 0.7 * MEAN_ABS
+
+
+def _noisy_backward(q, k, v, o, g, lse2, scale, causal, rng, eps):
+    """rm.backward with relative noise eps on P and dP before the bf16
+    roundings: what fp32 accumulation order and the hardware exp2 can do."""
+    sl2 = scale * LOG2E
+    P = np.exp2(rm._mask(sl2 * (q @ k.T) - lse2[:, None], causal))
+    P = P * (1 + eps * rng.standard_normal(P.shape))
+    dP = g @ v.T
+    dP = dP + eps * (np.abs(g) @ np.abs(v.T)) * rng.standard_normal(dP.shape)
+    D = (g * o).sum(axis=1, keepdims=True)
+    dV = _bf(P).T @ g
+    dS = _bf(P * (dP - D))
+    return scale * (dS @ k), scale * (dS.T @ q), dV
+
+
+@pytest.mark.parametrize("name,B,H,N,seed", [
+    ("causal", 8, 40, 300, 61),
+    ("480p", 1, 32, 1024, 63),
+])
+def test_tight_backward_bounds(oracle_mod, name, B, H, N, seed):
+    """The tight GPU check (gpu_util.TIGHT_TOL) leaves room for fp32 order but
+    not for a slip: fp32-sized noise (relative 1e-5 on P and dP) passes it,
+    while planted mistakes -- dQ 3% too large, or D_i dropped from 2% of the
+    rows -- fail it although they pass the fp64-oracle bounds (GRAD_TOL)."""
+    from gpu_util import GRAD_TOL, TIGHT_TOL, tight_errors
+    w = dataclasses.replace(WORKLOADS[name], B=B)
+    q, k, v = make_inputs(w, device="cpu", N=N, H=H, seed=seed)
+    g = make_dout(q.shape, device="cpu", seed=seed)
+    flat = [t.reshape(-1, N, w.d) for t in (q, k, v, g)]
+    ref = oracle_mod.attention_bwd(*flat, w.softmax_scale(), causal=w.causal)
+    qf, kf, vf, gf = (t.double().numpy() for t in flat)
+    rng = np.random.default_rng(seed)
+    sc = w.softmax_scale()
+    worst = {"noise": np.zeros((3, 2)), "slip_dq": np.zeros((3, 2)), "drop_d": np.zeros((3, 2)),
+             "slip_vs_oracle": np.zeros(3)}
+    nh = min(qf.shape[0], 64)
+    drop = rng.random(N) < 0.02
+    for h in range(nh):
+        o, lse2 = rm.certified_forward(qf[h], kf[h], vf[h], sc, w.causal)
+        model = rm.backward(qf[h], kf[h], vf[h], o, gf[h], lse2, sc, w.causal)
+        noisy = _noisy_backward(qf[h], kf[h], vf[h], o, gf[h], lse2, sc, w.causal, rng, 1e-5)
+        slip = (model[0] * 1.03, model[1], model[2])
+        o_drop = np.where(drop[:, None], 0.0, o)  # D_i = dO_i . O_i becomes 0 on those rows
+        dropped = rm.backward(qf[h], kf[h], vf[h], o_drop, gf[h], lse2, sc, w.causal)
+        for key, grads in (("noise", noisy), ("slip_dq", slip), ("drop_d", dropped)):
+            for i, (x, m) in enumerate(zip(grads, model)):
+                mx, mn = tight_errors(_bf(x)[None], m[None])
+                worst[key][i] = np.maximum(worst[key][i], [mx[0], mn[0]])
+        for i, (x, r) in enumerate(zip(slip, (ref[0][h], ref[1][h], ref[2][h]))):
+            worst["slip_vs_oracle"][i] = max(worst["slip_vs_oracle"][i], grad_errors(_bf(x)[None], r[None])[0][0])
+    names = ("dq", "dk", "dv")
+    for i, n in enumerate(names):
+        assert worst["noise"][i][0] <= TIGHT_TOL[n][0] and worst["noise"][i][1] <= TIGHT_TOL[n][1], \
+            (n, worst["noise"][i])
+    # The slip passes the outer bound but not the tight one.
+    assert worst["slip_vs_oracle"][0] <= GRAD_TOL["dq"][0]
+    assert worst["slip_dq"][0][0] > TIGHT_TOL["dq"][0] or worst["slip_dq"][0][1] > TIGHT_TOL["dq"][1]
+    assert any(worst["drop_d"][i][0] > TIGHT_TOL[n][0] or worst["drop_d"][i][1] > TIGHT_TOL[n][1]
+               for i, n in enumerate(names))
