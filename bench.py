@@ -337,7 +337,7 @@ def main():
                     "hbm_peak_gbs": peaks["hbm_gbs"]},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": achieved / peak_tf, "traffic": traffic,
-                     "kernel": "attn_fwd_kernel<128,%s>" % ("true" if w.causal else "false"),
+                     "kernel": "attn_fwd_kernel<%d,%d,%d>" % (w.d, 1 if w.causal else 0, 1 if args.dtype == "fp16" else 0),
                      "peak_source": f"{peak_src} bf16_tflops_sustained (cuBLAS, seconds-long loop)"},
         "clocks": clocks,
     }
@@ -385,37 +385,44 @@ def main():
         # Ring-step form: K/V in 8 chunks, each merged into fp32 accumulators
         # (clis_attn_fwd_chunk), then clis_attn_chunk_finalize.  Certified heads
         # add their partials with no rescaling; online heads rescale per chunk.
-        if not w.causal:
-            n_chunks = 8
-            bounds = [round(i * w.N / n_chunks) for i in range(n_chunks + 1)]
-            bounds = [b - b % 8 if 0 < b < w.N else b for b in bounds]
-            o_acc = torch.empty((heads * w.N, w.d), dtype=torch.float32, device=dev)
-            l_acc = torch.empty((heads * w.N,), dtype=torch.float32, device=dev)
-            m_acc = torch.empty((heads * w.N,), dtype=torch.float32, device=dev)
+        # Causal configs use clis_attn_fwd_chunk_causal: chunk c holds keys
+        # bounds[c] .. bounds[c+1] - 1, and query blocks ending before its first
+        # key are not launched.
+        n_chunks = 8
+        bounds = [round(i * w.N / n_chunks) for i in range(n_chunks + 1)]
+        bounds = [b - b % 8 if 0 < b < w.N else b for b in bounds]
+        o_acc = torch.empty((heads * w.N, w.d), dtype=torch.float32, device=dev)
+        l_acc = torch.empty((heads * w.N,), dtype=torch.float32, device=dev)
+        m_acc = torch.empty((heads * w.N,), dtype=torch.float32, device=dev)
 
-            def chunk_pass(variant):
-                for i, (a, b) in enumerate(zip(bounds[:-1], bounds[1:])):
-                    clis.clis_attn_fwd_chunk(q, k[:, :, a:b], v[:, :, a:b], sl2, o_acc, l_acc, m_acc, kbar=kbar,
-                                             certs=certs, first=(i == 0), variant=variant, mu=mu)
-                clis.clis_attn_chunk_finalize(q, o_acc, l_acc, m_acc, out=out)
+        def chunk_pass(variant):
+            for i, (a, b) in enumerate(zip(bounds[:-1], bounds[1:])):
+                if w.causal:
+                    clis.clis_attn_fwd_chunk_causal(q, k[:, :, a:b], v[:, :, a:b], sl2, o_acc, l_acc, m_acc, a,
+                                                    kbar=kbar, certs=certs, first=(i == 0), variant=variant,
+                                                    mu=mu)
+                else:
+                    clis.clis_attn_fwd_chunk(q, k[:, :, a:b], v[:, :, a:b], sl2, o_acc, l_acc, m_acc,
+                                             kbar=kbar, certs=certs, first=(i == 0), variant=variant, mu=mu)
+            clis.clis_attn_chunk_finalize(q, o_acc, l_acc, m_acc, out=out)
 
-            chunked = {"chunks": n_chunks}
-            for variant in ("auto", "online"):
-                for _ in range(args.warmup):
-                    chunk_pass(variant)
-                torch.cuda.synchronize()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                for _ in range(args.steps):
-                    chunk_pass(variant)
-                e1.record(stream)
-                torch.cuda.synchronize()
-                ms = e0.elapsed_time(e1) / args.steps
-                chunked["certified" if variant == "auto" else "online"] = {
-                    "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms": ms}
-            chunked["certified_speedup_vs_online"] = chunked["online"]["ms"] / chunked["certified"]["ms"]
-            line["chunked"] = chunked
-            del o_acc, l_acc, m_acc
+        chunked = {"chunks": n_chunks, "causal": w.causal}
+        for variant in ("auto", "online"):
+            for _ in range(args.warmup):
+                chunk_pass(variant)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                chunk_pass(variant)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / args.steps
+            chunked["certified" if variant == "auto" else "online"] = {
+                "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms": ms}
+        chunked["certified_speedup_vs_online"] = chunked["online"]["ms"] / chunked["certified"]["ms"]
+        line["chunked"] = chunked
+        del o_acc, l_acc, m_acc
     if extras in ("all", "backward"):
         # Backward (clis_attn_bwd: row dots, dK/dV kernel, dQ kernel) on the same
         # inputs, from a forward that also wrote lse2, for a seeded dO.  FLOPs

@@ -17,7 +17,8 @@ _BINDING_NAMES = {
     "clis_status_string", "clis_get_device_error", "clis_clear_device_error",
     "ClisError", "attention", "certify", "Cert", "VARIANT", "FMT", "STATUS",
     "library_path", "load_library", "decode_certs", "make_shape", "scale_log2_for",
-    "Shape", "CERT_WORDS", "LOG2E", "clis_debug_wait_selftest", "clis_attn_fwd_chunk", "clis_attn_chunk_finalize",
+    "Shape", "CERT_WORDS", "LOG2E", "clis_debug_wait_selftest", "clis_attn_fwd_chunk", "clis_attn_fwd_chunk_causal",
+    "clis_attn_chunk_finalize",
     "clis_attn_bwd", "clis_attn_bwd_workspace_size", "attention_bwd", "attention_fwd_lse", "attention_autograd",
     "AttentionFunction",
 }

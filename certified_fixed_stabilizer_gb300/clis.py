@@ -83,6 +83,9 @@ def load_library():
     lib.clis_clear_device_error.restype = i32
     lib.clis_attn_fwd_chunk.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp]
     lib.clis_attn_fwd_chunk.restype = i32
+    lib.clis_attn_fwd_chunk_causal.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, ctypes.c_int64, i32,
+                                               i32, vp]
+    lib.clis_attn_fwd_chunk_causal.restype = i32
     lib.clis_attn_chunk_finalize.argtypes = [sp, vp, vp, vp, vp, vp, vp]
     lib.clis_attn_chunk_finalize.restype = i32
     lib.clis_debug_wait_selftest.argtypes = [ctypes.c_uint32, vp]
@@ -249,6 +252,22 @@ def clis_attn_fwd_chunk(q, k, v, scale_log2: float, o_acc, l_acc, m_acc, kbar=No
                                  VARIANT[variant], _stream(stream))
     if st != 0:
         raise ClisError("clis_attn_fwd_chunk", st)
+
+
+def clis_attn_fwd_chunk_causal(q, k, v, scale_log2: float, o_acc, l_acc, m_acc, key_offset: int, kbar=None,
+                               certs=None, tile_certs=None, first: bool = False, variant: str = "auto", stream=None,
+                               mu=None):
+    """Merge one causal KV chunk (k, v: [B, H, Nk_chunk, d], keys key_offset ..
+    key_offset + Nk_chunk - 1 of each head) into the accumulators, as
+    clis_attn_fwd_chunk does; query i sees chunk key j iff key_offset + j <= i."""
+    lib = load_library()
+    shape = make_shape(q, k, v)
+    st = lib.clis_attn_fwd_chunk_causal(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(o_acc), _ptr(l_acc),
+                                        _ptr(m_acc), _ptr(kbar), _ptr(certs), _ptr(tile_certs), _ptr(mu),
+                                        float(scale_log2), int(key_offset), int(bool(first)), VARIANT[variant],
+                                        _stream(stream))
+    if st != 0:
+        raise ClisError("clis_attn_fwd_chunk_causal", st)
 
 
 def clis_attn_chunk_finalize(q, o_acc, l_acc, m_acc, out=None, lse2=None, stream=None):

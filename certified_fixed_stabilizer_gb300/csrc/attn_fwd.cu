@@ -46,6 +46,10 @@ __device__ unsigned int g_attn_error_word = 0;
 
 namespace {
 
+// CAUSAL template argument: no mask, the causal mask, or the causal mask of a
+// KV chunk that starts at key k_off of the head.
+constexpr int kNonCausal = 0, kCausal = 1, kCausalChunk = 2;
+
 constexpr int BM = 128;            // rows per query tile
 constexpr int BN = 128;            // keys per KV tile
 // A work tile is two query tiles; per-prefix certificates are kept per work tile.
@@ -95,6 +99,10 @@ struct Params {
     int chunk_mode;
     float *o_acc, *l_acc, *m_acc;
     const uint8_t *tile_certs;  // optional per-prefix certificates [B*H][nqb] (causal AUTO)
+    // Causal KV chunk: key j of the chunk is key k_off + j of the head, visible
+    // to query i iff k_off + j <= i.  Query blocks before qb0 = k_off / 256 see
+    // none of the chunk's keys and are not launched (0 and 0 otherwise).
+    int k_off, qb0;
 };
 
 struct __align__(8) Ctl {
@@ -127,21 +135,27 @@ struct Tile {
 // Key tile processed at step j of a work tile (odd rounds sweep backwards).
 __device__ __forceinline__ int kv_tile(const Tile &T, int j) { return T.rev ? T.n_kv - 1 - j : j; }
 
-template <bool CAUSAL, int DT>
+template <int CAUSAL, int DT>
 __device__ __forceinline__ Tile decode_tile(const Params &p, int tile)
 {
     Tile t;
     if (CAUSAL) {
-        const int per_grp = p.grp * p.nqb;
+        // Query blocks qb0 .. nqb-1 of each head (qb0 = 0 except for a causal KV chunk).
+        const int qb0 = CAUSAL == kCausalChunk ? p.qb0 : 0;
+        const int nqb = p.nqb - qb0;
+        const int per_grp = p.grp * nqb;
         const int gi = tile / per_grp;
         const int r = tile % per_grp;
         const int BH = p.B * p.H;
         const int heads = min(p.grp, BH - gi * p.grp);
         const int qi = r / heads;
         t.bh = gi * p.grp + r % heads;
-        t.qb = (gi & 1) ? qi : (p.nqb - 1 - qi);
+        t.qb = qb0 + ((gi & 1) ? qi : (nqb - 1 - qi));
+        // KV tiles of this launch that the block's last row sees (at least one:
+        // the block holds a row >= k_off).
         const int last_row = min(p.Nq, (t.qb + 1) * 2 * BM) - 1;
-        t.n_kv = min(p.n_kv_full, last_row / BN + 1);
+        const int k_off = CAUSAL == kCausalChunk ? p.k_off : 0;
+        t.n_kv = min(p.n_kv_full, (last_row - k_off) / BN + 1);
     } else {
         t.bh = tile / p.nqb;
         t.qb = tile % p.nqb;
@@ -194,7 +208,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
 // Runs on all 32 lanes of its warp (warp-uniform control flow); one elected
 // lane issues the copies.
 
-template <int D, bool CAUSAL, int DT>
+template <int D, int CAUSAL, int DT>
 __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                               const CUtensorMap *tm_v, uint32_t sQ0, uint32_t sKV)
 {
@@ -297,7 +311,7 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
         umma_ts(o_tmem, p_tmem + kk * 8, vd + ((kk * 2048) >> 4), IDESC_O, (accumulate | kk) ? 1u : 0u);
 }
 
-template <int D, bool CAUSAL, int DT>
+template <int D, int CAUSAL, int DT>
 __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, uint32_t sKV)
 {
     using C = Cfg<D>;
@@ -388,7 +402,7 @@ abort:
 
 // ------------------------------------------------------------------- softmax
 
-template <int D, bool CAUSAL, int DT>
+template <int D, int CAUSAL, int DT>
 __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, int lane)
 {
     using C = Cfg<D>;
@@ -447,9 +461,11 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
             tmem_ld32(tS + 96, s + 96);
             tmem_wait_ld();
 
-            // Mask keys past Nk (ragged last tile) and, if causal, keys after the row.
+            // Mask keys past Nk (ragged last tile) and, if causal, keys after the row
+            // (key j of a causal KV chunk is key k_off + j of the head).
             const int key0 = kv_tile(T, j) * BN;
-            const int lim = CAUSAL ? min(p.Nk, row + 1) : p.Nk;  // keys [0, lim) are visible
+            const int lim = CAUSAL ? min(p.Nk, row + 1 - (CAUSAL == kCausalChunk ? p.k_off : 0))
+                                   : p.Nk;  // keys [0, lim) are visible
             if (key0 + BN > lim) {
 #pragma unroll
                 for (int cc = 0; cc < BN; cc++)
@@ -662,7 +678,7 @@ __device__ __forceinline__ void write_row(const Params &p, const Tile &T, uint32
 
 // ---------------------------------------------------------------- correction
 
-template <int D, bool CAUSAL, int DT>
+template <int D, int CAUSAL, int DT>
 __device__ void correction_role(const Params &p, Ctl &c, uint32_t tmem, int warp, int lane)
 {
     using C = Cfg<D>;
@@ -715,7 +731,9 @@ __device__ void correction_role(const Params &p, Ctl &c, uint32_t tmem, int warp
             if (!mbar_wait(smem_u32(&c.pv_done[t]), (g - 1) & 1, ab, err, kErrCorrection)) return;
             tc_fence_after();
             const int row = T.qb * 2 * BM + t * BM + rl;
-            write_row<D, DT>(p, T, tmem + (t ? C::TM_O1 : C::TM_O0) + lane_off, row, row < p.Nq, c.epi_l[t][rl],
+            // Rows before a causal KV chunk's first key saw none of its keys: nothing to merge.
+            write_row<D, DT>(p, T, tmem + (t ? C::TM_O1 : C::TM_O0) + lane_off, row, row < p.Nq && (CAUSAL != kCausalChunk || row >= p.k_off),
+                             c.epi_l[t][rl],
                          c.epi_shift[t][rl]);
             tc_fence_before();
             mbar_arrive(smem_u32(&c.o_free[t]));
@@ -725,7 +743,7 @@ __device__ void correction_role(const Params &p, Ctl &c, uint32_t tmem, int warp
 
 // -------------------------------------------------------------------- kernel
 
-template <int D, bool CAUSAL, int DT>
+template <int D, int CAUSAL, int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params p)
@@ -833,7 +851,7 @@ bool make_map(CUtensorMap *map, const void *base, int dtype, int64_t B, int64_t 
     return r == CUDA_SUCCESS;
 }
 
-template <int D, bool CAUSAL, int DT>
+template <int D, int CAUSAL, int DT>
 clis_status_t launch_impl(const AttnArgs &a, cudaStream_t stream)
 {
     using C = Cfg<D>;
@@ -871,18 +889,25 @@ clis_status_t launch_impl(const AttnArgs &a, cudaStream_t stream)
     p.nqb = (a.Nq + 2 * BM - 1) / (2 * BM);
     p.n_kv_full = (a.Nk + BN - 1) / BN;
     p.num_tiles = a.B * a.H * p.nqb;
-    // Causal scheduling groups: enough heads that a group spans about two
-    // waves of CTAs.
-    p.grp = (2 * nsm + p.nqb - 1) / p.nqb;
-    if (p.grp > a.B * a.H) p.grp = a.B * a.H;
-    if (p.grp < 1) p.grp = 1;
+    p.grp = 1;
     p.scale_log2 = a.scale_log2;
     p.variant = a.variant;
     p.chunk_mode = a.chunk_mode;
     p.o_acc = a.o_acc;
     p.l_acc = a.l_acc;
     p.m_acc = a.m_acc;
-    if (p.num_tiles == 0) return CLIS_OK;
+    p.k_off = CAUSAL == kCausalChunk ? a.k_off : 0;
+    p.qb0 = p.k_off / (2 * BM);
+    if (CAUSAL) {
+        const int nqb = p.nqb - p.qb0;
+        p.num_tiles = a.B * a.H * nqb;
+        // Causal scheduling groups: enough heads that a group spans about two
+        // waves of CTAs.
+        p.grp = (2 * nsm + nqb - 1) / nqb;
+        if (p.grp > a.B * a.H) p.grp = a.B * a.H;
+        if (p.grp < 1) p.grp = 1;
+    }
+    if (p.num_tiles <= 0) return CLIS_OK;
     const int grid = p.num_tiles < nsm ? p.num_tiles : nsm;
     attn_fwd_kernel<D, CAUSAL, DT><<<grid, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? CLIS_OK : CLIS_ERR_CUDA;
@@ -955,13 +980,23 @@ clis_status_t launch_wait_selftest(uint32_t limit_us, cudaStream_t stream)
 
 clis_status_t launch_attn_fwd(const AttnArgs &a, cudaStream_t stream)
 {
-    if (a.dtype == CLIS_DT_FP16) {
-        if (a.d == 128)
-            return a.causal ? launch_impl<128, true, 1>(a, stream) : launch_impl<128, false, 1>(a, stream);
-        return a.causal ? launch_impl<64, true, 1>(a, stream) : launch_impl<64, false, 1>(a, stream);
+    // Causal mode: plain causal, or a causal KV chunk (a separate instantiation,
+    // so the key offset costs the plain causal kernel nothing).
+    const int cm = !a.causal ? kNonCausal : (a.chunk_mode ? kCausalChunk : kCausal);
+    const bool f16 = a.dtype == CLIS_DT_FP16;
+#define CLIS_FWD_LAUNCH(D, DT)                                                            \
+    switch (cm) {                                                                      \
+    case kNonCausal: return launch_impl<D, kNonCausal, DT>(a, stream);                 \
+    case kCausal: return launch_impl<D, kCausal, DT>(a, stream);                       \
+    default: return launch_impl<D, kCausalChunk, DT>(a, stream);                       \
     }
-    if (a.d == 128) return a.causal ? launch_impl<128, true, 0>(a, stream) : launch_impl<128, false, 0>(a, stream);
-    return a.causal ? launch_impl<64, true, 0>(a, stream) : launch_impl<64, false, 0>(a, stream);
+    if (a.d == 128) {
+        if (f16) { CLIS_FWD_LAUNCH(128, 1) }
+        CLIS_FWD_LAUNCH(128, 0)
+    }
+    if (f16) { CLIS_FWD_LAUNCH(64, 1) }
+    CLIS_FWD_LAUNCH(64, 0)
+#undef CLIS_FWD_LAUNCH
 }
 
 clis_status_t read_device_error(uint32_t *code)

@@ -258,10 +258,14 @@ clis_status_t clis_certify_noalloc(const clis_shape_t *shape, const void *q, con
                         CLIS_NOALLOC_SCRATCH_BYTES, stream);
 }
 
-clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void *q, const void *k, const void *v,
-                                  float *o_acc, float *l_acc, float *m_acc, const float *kbar,
-                                  const clis_head_cert_t *certs, const float *mu, float scale_log2, int first,
-                                  clis_variant_t variant, clis_stream_t stream)
+}  // extern "C"
+
+namespace {
+
+clis_status_t attn_chunk_impl(const clis_shape_t *shape, const void *q, const void *k, const void *v, float *o_acc,
+                              float *l_acc, float *m_acc, const float *kbar, const clis_head_cert_t *certs,
+                              const uint8_t *tile_certs, const float *mu, float scale_log2, int causal,
+                              int64_t key_offset, int first, clis_variant_t variant, clis_stream_t stream)
 {
     clis_status_t st = check_shape(shape, false);
     if (st != CLIS_OK) return st;
@@ -274,6 +278,14 @@ clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void *q, cons
         return CLIS_ERR_INVALID_ARG;
     if ((variant == CLIS_AUTO || variant == CLIS_CERTIFIED_FORCED) && !kbar) return CLIS_ERR_INVALID_ARG;
     if (variant == CLIS_AUTO && !certs) return CLIS_ERR_INVALID_ARG;
+    if (tile_certs && variant != CLIS_AUTO) return CLIS_ERR_INVALID_ARG;
+    if (causal) {
+        if (key_offset < 0) return CLIS_ERR_INVALID_ARG;
+        // The first chunk initialises every row's accumulators, so it must be
+        // the one holding key 0 (the only chunk every query row sees).
+        if (first && key_offset != 0) return CLIS_ERR_INVALID_ARG;
+        if (key_offset + shape->Nk > shape->Nq) return CLIS_ERR_UNSUPPORTED;
+    }
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_acc)) return CLIS_ERR_MISALIGNED;
     if ((kbar && !aligned16(kbar)) || (certs && !aligned16(certs)) ||
         (reinterpret_cast<uintptr_t>(l_acc) & 3u) || (reinterpret_cast<uintptr_t>(m_acc) & 3u) ||
@@ -291,6 +303,7 @@ clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void *q, cons
     a.kbar = kbar;
     a.certs = certs;
     a.mu = mu;
+    a.tile_certs = tile_certs;
     a.q_sb = shape->q_sb;
     a.q_sh = shape->q_sh;
     a.q_sn = shape->q_sn;
@@ -308,13 +321,37 @@ clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void *q, cons
     a.d = static_cast<int>(shape->d);
     a.dtype = static_cast<int>(shape->dtype);
     a.scale_log2 = scale_log2;
-    a.causal = 0;
+    a.causal = causal;
+    a.k_off = causal ? static_cast<int>(key_offset) : 0;
     a.variant = variant;
     a.chunk_mode = first ? 2 : 1;
     a.o_acc = o_acc;
     a.l_acc = l_acc;
     a.m_acc = m_acc;
     return clis::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void *q, const void *k, const void *v,
+                                  float *o_acc, float *l_acc, float *m_acc, const float *kbar,
+                                  const clis_head_cert_t *certs, const float *mu, float scale_log2, int first,
+                                  clis_variant_t variant, clis_stream_t stream)
+{
+    return attn_chunk_impl(shape, q, k, v, o_acc, l_acc, m_acc, kbar, certs, nullptr, mu, scale_log2, 0, 0, first,
+                           variant, stream);
+}
+
+clis_status_t clis_attn_fwd_chunk_causal(const clis_shape_t *shape, const void *q, const void *k, const void *v,
+                                         float *o_acc, float *l_acc, float *m_acc, const float *kbar,
+                                         const clis_head_cert_t *certs, const uint8_t *tile_certs, const float *mu,
+                                         float scale_log2, int64_t key_offset, int first, clis_variant_t variant,
+                                         clis_stream_t stream)
+{
+    return attn_chunk_impl(shape, q, k, v, o_acc, l_acc, m_acc, kbar, certs, tile_certs, mu, scale_log2, 1,
+                           key_offset, first, variant, stream);
 }
 
 clis_status_t clis_attn_chunk_finalize(const clis_shape_t *shape, const float *o_acc, const float *l_acc,

@@ -83,6 +83,7 @@ struct AttnArgs {
     int variant;
     int chunk_mode = 0;  // 0 off, 1 merge into the accumulators, 2 first chunk
     float *o_acc = nullptr, *l_acc = nullptr, *m_acc = nullptr;
+    int k_off = 0;  // causal KV chunk: index of the chunk's first key in the head
 };
 
 struct ChunkFinalizeArgs {

@@ -260,13 +260,42 @@ CLIS_API clis_status_t clis_attn_fwd_tiles(const clis_shape_t *shape, const void
  * rescaling to the larger maximum.  Calls on one set of accumulators must
  * be ordered (one stream, or events between streams).  kbar, certs (and mu, optional) must come from
  * clis_certify over the whole key sequence (for a ring: the k-bar partials and norm maxima of all
- * chunks reduced before the first step).  Non-causal only; shape->o_* ignored.
+ * chunks reduced before the first step).  Non-causal (clis_attn_fwd_chunk_causal is the causal
+ * form); shape->o_* ignored.
  * Errors as clis_attn_fwd. */
 CLIS_API clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void *q, const void *k,
                                   const void *v, float *o_acc, float *l_acc, float *m_acc,
                                   const float *kbar, const clis_head_cert_t *certs,
                                   const float *mu, float scale_log2, int first,
                                   clis_variant_t variant, clis_stream_t stream);
+
+/* Causal form of clis_attn_fwd_chunk (Table 7's ring columns and Figure 6's
+ * ring step, for the causal training setting of Table 3): the chunk holds keys
+ * key_offset .. key_offset + shape->Nk - 1 of the head (k and v point at the
+ * chunk's first key), q all shape->Nq query rows, and query i sees chunk key j
+ * iff key_offset + j <= i.  Rows before key_offset see none of the chunk's
+ * keys and their accumulators are left untouched; query blocks of 256 rows that
+ * end before key_offset are not computed at all.  The partials merge as in
+ * clis_attn_fwd_chunk: a certified row's shift is its fixed mu_i in every chunk,
+ * so its partial is added with no rescaling, in any chunk order.
+ *   key_offset  >= 0, with key_offset + shape->Nk <= shape->Nq
+ *               (CLIS_ERR_UNSUPPORTED otherwise)
+ *   first       1 overwrites the accumulators of every row: only the chunk
+ *               with key_offset = 0 may be first (CLIS_ERR_INVALID_ARG
+ *               otherwise); the other chunks follow in any order
+ *   tile_certs  optional per-prefix certificates from clis_certify_tiles over
+ *               the whole sequence (NULL: per-head flags only); a query block
+ *               whose flag is set takes the fixed stabiliser in every chunk
+ *               (CLIS_AUTO only; CLIS_ERR_INVALID_ARG with another variant)
+ *   kbar, certs, mu  from clis_certify (or clis_certify_tiles) over the whole
+ *               sequence
+ * Other arguments and errors as clis_attn_fwd_chunk. */
+CLIS_API clis_status_t clis_attn_fwd_chunk_causal(const clis_shape_t *shape, const void *q, const void *k,
+                                                  const void *v, float *o_acc, float *l_acc, float *m_acc,
+                                                  const float *kbar, const clis_head_cert_t *certs,
+                                                  const uint8_t *tile_certs, const float *mu, float scale_log2,
+                                                  int64_t key_offset, int first, clis_variant_t variant,
+                                                  clis_stream_t stream);
 
 /* After the last chunk: o = o_acc / l_acc (bf16, strides shape->o_*) and, if
  * lse2 is not NULL, lse2 = m_acc + log2(l_acc). */

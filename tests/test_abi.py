@@ -28,7 +28,8 @@ def test_header_declares_the_boundary():
     for n in ("clis_certify_workspace_size", "clis_certify", "clis_attn_fwd", "clis_status_string",
               "clis_get_device_error", "clis_clear_device_error", "clis_debug_wait_selftest",
               "clis_attn_fwd_chunk", "clis_attn_chunk_finalize", "clis_certify_noalloc",
-              "clis_attn_bwd_workspace_size", "clis_attn_bwd", "clis_certify_tiles", "clis_attn_fwd_tiles"):
+              "clis_attn_bwd_workspace_size", "clis_attn_bwd", "clis_certify_tiles", "clis_attn_fwd_tiles",
+              "clis_attn_fwd_chunk_causal"):
         assert n in names
 
 
@@ -167,6 +168,27 @@ def test_chunk_entry_points_reject_bad_arguments(clis):
     assert lib.clis_attn_chunk_finalize(ctypes.byref(s), vp(FAKE), vp(FAKE), vp(FAKE), vp(0), None, None) == 1
     s2 = _shape(clis, d=80)
     assert lib.clis_attn_chunk_finalize(ctypes.byref(s2), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, None) == 2
+
+
+def test_causal_chunk_entry_point_rejects_bad_arguments(clis):
+    """Causal KV chunks: the chunk must lie inside the query range, only the
+    chunk holding key 0 may be first, per-prefix flags need AUTO (all rejected
+    on the host; the fake pointers are never touched)."""
+    lib = clis.load_library()
+    vp = ctypes.c_void_p
+    s = _shape(clis, Nq=1000, Nk=300)
+
+    def call(off, first=0, tiles=None, variant=0, oa=FAKE):
+        return lib.clis_attn_fwd_chunk_causal(ctypes.byref(s), vp(FAKE), vp(FAKE), vp(FAKE), vp(oa), vp(FAKE),
+                                              vp(FAKE), vp(FAKE), vp(FAKE), tiles, None, 0.1, off, first, variant,
+                                              None)
+    assert call(-1) == 1                      # negative key offset
+    assert call(256, first=1) == 1            # a first chunk that does not hold key 0
+    assert call(701) == 2                     # keys past the last query row
+    assert call(0, tiles=vp(FAKE), variant=1) == 1  # per-prefix flags outside AUTO
+    assert call(0, first=2) == 1
+    assert call(100, oa=0) == 1
+    assert call(100, oa=FAKE + 4) == 3
 
 
 def test_tile_entry_points_reject_bad_arguments(clis):
