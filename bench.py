@@ -34,6 +34,8 @@ import torch  # noqa: E402
 from certified_fixed_stabilizer_gb300.workloads import WORKLOADS, make_dout, make_inputs, sample_rows  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
+NOMINAL_BF16_TFLOPS = 2250.0       # GB300 dense BF16, vendor nominal
+TENSOR_FLOP_PER_CLK_SM = 8192.0    # 2*128*128*16 FLOP per 64 cycles (tcgen05 kind::f16, measured)
 METRIC = "attention fwd TFLOP/s (BF16, 1xGB300); CLiS step = certification + fused attention (AUTO)"
 
 
@@ -310,6 +312,8 @@ def main():
     dev_err = clis.clis_get_device_error()
 
     peaks, peak_src = measured_peaks()
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    clock_peak = (TENSOR_FLOP_PER_CLK_SM * n_sm * clocks["sm_mhz"] * 1e6 / 1e12) if clocks["sm_mhz"] else None
     peak_tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
     achieved = flops / (attn_avg_ms * 1e-3) / 1e12
     traffic = None
@@ -338,11 +342,48 @@ def main():
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": achieved / peak_tf, "traffic": traffic,
                      "kernel": "attn_fwd_kernel<%d,%d,%d>" % (w.d, 1 if w.causal else 0, 1 if args.dtype == "fp16" else 0),
-                     "peak_source": f"{peak_src} bf16_tflops_sustained (cuBLAS, seconds-long loop)"},
+                     "peak_source": f"{peak_src} bf16_tflops_sustained (cuBLAS, seconds-long loop)",
+                     # Two more denominators: the vendor's nominal dense BF16 figure, and the
+                     # tensor pipe's instruction rate (a 128x128x16 MMA per 64 cycles per SM,
+                     # measured) at the SM clock seen during the timed region.
+                     "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
+                     "nominal_peak": NOMINAL_BF16_TFLOPS,
+                     "frac_of_clock_peak": (achieved / clock_peak) if clock_peak else None,
+                     "clock_peak": clock_peak},
         "clocks": clocks,
     }
 
     extras = "none" if args.no_extras else args.extras
+    if extras in ("all", "e2e"):
+        # (Timed right after the headline step, in the same thermal and power
+        # state, before the other legs heat the chip.)
+        # End to end through the public call (clis.attention) with pinned host
+        # buffers: every step copies Q, K, V in, computes and copies O out; the
+        # call pipelines head groups over a copy-in, two compute and a copy-out stream.
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        oh = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+
+        def e2e_step():
+            clis.attention(qh, kh, vh, causal=w.causal, variant=args.variant, device=dev, out=oh,
+                           non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(args.steps, 10))
+        with ClockSampler(local) as cs_e2e:
+            e0.record(stream)
+            for _ in range(n_e2e):
+                e2e_step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, ws)
+        line["e2e"] = {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out.numel() * out.element_size(),
+                       "ms_per_step": e2e_ms, "api": "certified_fixed_stabilizer_gb300.clis.attention",
+                       "clocks": cs_e2e.summary()}
+        del qh, kh, vh, oh
     if extras == "all":
         # Online-softmax baseline (same kernel skeleton, every head on the online path).
         on_total, _, on_attn = timed_loop("online", args.steps, args.warmup)
@@ -457,45 +498,20 @@ def main():
                             "launches_per_step": 3, "flops": "five matmuls (2.5x the forward's count)",
                             "fwd_plus_bwd_ms": attn_avg_ms + cert_avg_ms + bwd_ms}
         del dout, dq, dk, dv, bws, lse2
-    if extras in ("all", "e2e"):
-        # End to end through the public call (clis.attention) with pinned host
-        # buffers: every step copies Q, K, V in, computes and copies O out; the
-        # call pipelines head groups over a copy-in, two compute and a copy-out stream.
-        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
-        oh = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
-
-        def e2e_step():
-            clis.attention(qh, kh, vh, causal=w.causal, variant=args.variant, device=dev, out=oh,
-                           non_blocking=True)
-
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n_e2e = max(1, min(args.steps, 10))
-        e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, ws)
-        line["e2e"] = {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                       "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out.numel() * out.element_size(),
-                       "ms_per_step": e2e_ms, "api": "certified_fixed_stabilizer_gb300.clis.attention"}
-        del qh, kh, vh, oh
-        if rank == 0 and ws == 1 and extras == "all":
-            import oracle
-            qc, kc, vc = (t.cpu() for t in (q, k, v))
-            hs, rows = cpu_sample_plan(qc, kc, vc, w, target_s=15.0)
-            t0 = time.perf_counter()
-            oracle_sample_step(qc, kc, vc, w, hs, rows)
-            dt = time.perf_counter() - t0
-            line["cpu_baseline"] = {
-                "value": sample_flops(w, len(hs), rows) / dt / 1e12, "unit": "TFLOP/s",
-                "cores": oracle.num_threads(), "kind": "oracle",
-                "sample": (f"heads 0-{hs[-1]} ({len(hs)} of {qc.shape[0] * qc.shape[1]}): certification "
-                           f"over all {w.N} keys + attention for {len(rows)} seed-chosen query rows per head; "
-                           f"{dt:.1f} s")}
+    if rank == 0 and ws == 1 and extras == "all":
+        # CPU baseline: the oracle on a bounded sample of this workload.
+        import oracle
+        qc, kc, vc = (t.cpu() for t in (q, k, v))
+        hs, rows = cpu_sample_plan(qc, kc, vc, w, target_s=15.0)
+        t0 = time.perf_counter()
+        oracle_sample_step(qc, kc, vc, w, hs, rows)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {
+            "value": sample_flops(w, len(hs), rows) / dt / 1e12, "unit": "TFLOP/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": (f"heads 0-{hs[-1]} ({len(hs)} of {qc.shape[0] * qc.shape[1]}): certification "
+                       f"over all {w.N} keys + attention for {len(rows)} seed-chosen query rows per head; "
+                       f"{dt:.1f} s")}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
