@@ -58,10 +58,11 @@ def parse():
     ap.add_argument("--variant", default="auto", choices=["auto", "online", "certified", "online_lazy"])
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"],
                     help="element type of Q, K, V, P and O (fp16 certifies with the FP16 exp2 budget)")
-    ap.add_argument("--extras", default="all", choices=["all", "none", "backward", "chunks", "e2e", "tiles"],
+    ap.add_argument("--extras", default="all", choices=["all", "none", "backward", "chunks", "e2e", "tiles", "fp8"],
                     help="legs after the headline step: all (online variants, ring-step chunks, backward, e2e, "
-                         "CPU baseline, per-prefix certificates for causal configs), none, or only the backward, the "
-                         "ring-step chunks, the e2e leg or the per-prefix leg (profiling runs)")
+                         "CPU baseline, per-prefix certificates for causal configs, FP8 P.V for non-causal BF16 "
+                         "configs), none, or only the backward, the ring-step chunks, the e2e leg, the per-prefix "
+                         "leg or the FP8 P.V leg (profiling runs)")
     ap.add_argument("--no-extras", action="store_true", help="same as --extras none")
     return ap.parse_args()
 
@@ -395,6 +396,36 @@ def main():
         line["online_lazy"] = {"value": flops / (statistics.mean(lz_attn) * 1e-3) / 1e12, "unit": "TFLOP/s",
                                "ms": statistics.mean(lz_attn)}
         line["certified_speedup_vs_online_lazy"] = statistics.mean(lz_attn) / attn_avg_ms
+    if extras in ("all", "fp8") and not w.causal and args.dtype == "bf16" and w.d == 128:
+        # FP8 P.V (E4M3 P and V for eligible certified heads; the others as in the
+        # headline step).  A reduced-precision leg beside the BF16 headline: step =
+        # certification + V -> E4M3 transpose + attention.
+        vt8 = torch.empty((heads, w.d, -(-w.N // 16) * 16), dtype=torch.uint8, device=dev)
+        fev = []
+        for i in range(args.warmup + args.steps):
+            if flush_buf is not None:
+                flush_buf.zero_()
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            clis.clis_certify(q, k, v, sl2, kbar=kbar, certs=certs, workspace=wsp, mu=mu, exp_fmt=exp_fmt)
+            clis.clis_v_to_e4m3(v, vt8)
+            e1.record(stream)
+            clis.clis_attn_fwd_fp8pv(q, k, v, vt8, sl2, kbar=kbar, certs=certs, out=out, mu=mu)
+            e2.record(stream)
+            if i >= args.warmup:
+                fev.append((e0, e1, e2))
+        torch.cuda.synchronize()
+        f_step = statistics.mean(a.elapsed_time(c) for a, _, c in fev)
+        f_attn = statistics.mean(b.elapsed_time(c) for _, b, c in fev)
+        n_f8 = sum(1 for c in clis.decode_certs(certs)
+                   if c["certified"] and c["B_h"] <= min(8, c["C"]) and c["G"] <= 8 and w.N >= 4096)
+        line["fp8_pv"] = {
+            "value": flops / (f_step * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": f_step,
+            "attention_only": flops / (f_attn * 1e-3) / 1e12, "attention_ms": f_attn,
+            "prepass_ms": f_step - f_attn, "fp8_heads": f"{n_f8}/{heads}",
+            "speedup_vs_bf16_attention": attn_avg_ms / f_attn,
+            "precision": "P and V in E4M3 for the P.V product (kind::f8f6f4); Q K^T in BF16; fp32 accumulators"}
+        del vt8
     if extras in ("all", "tiles") and w.causal:
         # Per-prefix certificates (clis_certify_tiles + clis_attn_fwd_tiles): query
         # blocks of heads that fail as a whole still take the fixed stabiliser

@@ -86,6 +86,12 @@ def load_library():
     lib.clis_attn_fwd_chunk_causal.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, ctypes.c_int64, i32,
                                                i32, vp]
     lib.clis_attn_fwd_chunk_causal.restype = i32
+    lib.clis_v_e4m3_size.argtypes = [sp, ctypes.POINTER(sz)]
+    lib.clis_v_e4m3_size.restype = i32
+    lib.clis_v_to_e4m3.argtypes = [sp, vp, vp, vp]
+    lib.clis_v_to_e4m3.restype = i32
+    lib.clis_attn_fwd_fp8pv.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, vp]
+    lib.clis_attn_fwd_fp8pv.restype = i32
     lib.clis_attn_chunk_finalize.argtypes = [sp, vp, vp, vp, vp, vp, vp]
     lib.clis_attn_chunk_finalize.restype = i32
     lib.clis_debug_wait_selftest.argtypes = [ctypes.c_uint32, vp]
@@ -237,6 +243,45 @@ def clis_attn_fwd(q, k, v, scale_log2: float, kbar=None, certs=None, causal: boo
                            VARIANT[variant], _stream(stream))
     if st != 0:
         raise ClisError("clis_attn_fwd", st)
+    return out
+
+
+def clis_v_e4m3_size(shape: Shape) -> int:
+    n = ctypes.c_size_t(0)
+    st = load_library().clis_v_e4m3_size(ctypes.byref(shape), ctypes.byref(n))
+    if st != 0:
+        raise ClisError("clis_v_e4m3_size", st)
+    return n.value
+
+
+def clis_v_to_e4m3(v, vt8=None, stream=None):
+    """E4M3 transpose of V for the FP8 P.V path: uint8 [B*H, d, pitch],
+    pitch = Nk rounded up to 16."""
+    lib = load_library()
+    shape = make_shape(v, v, v)
+    B, H, Nk, d = v.shape
+    pitch = -(-Nk // 16) * 16
+    if vt8 is None:
+        vt8 = torch.empty((B * H, d, pitch), dtype=torch.uint8, device=v.device)
+    st = lib.clis_v_to_e4m3(ctypes.byref(shape), _ptr(v), _ptr(vt8), _stream(stream))
+    if st != 0:
+        raise ClisError("clis_v_to_e4m3", st)
+    return vt8
+
+
+def clis_attn_fwd_fp8pv(q, k, v, vt8, scale_log2: float, kbar=None, certs=None, variant: str = "auto", out=None,
+                        lse2=None, stream=None, mu=None):
+    """Attention forward whose eligible certified heads run P.V in E4M3
+    (vt8 from clis_v_to_e4m3); returns ``out``."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    shape = make_shape(q, k, v, out)
+    st = lib.clis_attn_fwd_fp8pv(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(vt8), _ptr(out), _ptr(lse2),
+                                 _ptr(kbar), _ptr(certs), _ptr(mu), float(scale_log2), VARIANT[variant],
+                                 _stream(stream))
+    if st != 0:
+        raise ClisError("clis_attn_fwd_fp8pv", st)
     return out
 
 

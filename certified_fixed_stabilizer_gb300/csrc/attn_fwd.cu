@@ -60,6 +60,18 @@ constexpr int kNStageMax = 8;
 // by more than this (exp2 units), so p <= 2^kLazyTau; FlashAttention-4 uses 8.
 constexpr float kLazyTau = 8.0f;
 
+// FP8 P.V path (E4M3 P and V, kind::f8f6f4): exp2 outputs must stay below the
+// largest finite E4M3 value, 448 = 2^8.807, so the budget is floor(U_exp) = 8;
+// V fits E4M3 without saturating when G <= 8 (max |V| <= 256).
+constexpr int kE4m3Budget = 8;
+constexpr int kE4m3MaxG = 8;
+// The certificate makes E4M3 safe (no overflow); accuracy needs enough keys to
+// average V's E4M3 rounding (relative error up to 2^-4 per entry): on diffuse
+// heads the mean output error is about 0.033 / sqrt(Nk), so AUTO routes a head
+// to E4M3 only from 4096 keys on (at most half of the 1e-3 mean bound).
+constexpr int kE4m3MinKeys = 4096;
+constexpr int kVt8TileBytes = BN * 128;  // one E4M3 V^T tile: 128 rows of d x 128 keys
+
 // Error-word bits: which wait gave up.
 constexpr unsigned kErrProducer = 1u << 0;
 constexpr unsigned kErrMma = 1u << 1;
@@ -121,6 +133,7 @@ struct __align__(8) Ctl {
 struct Tile {
     int bh, b, h, qb, n_kv;
     bool cert;  // fixed stabiliser, no rescale
+    bool f8;    // certified tile whose P.V runs in E4M3 (kernels built for the FP8 P.V path only)
     bool lazy;  // online, rescale only when the row maximum grows by more than kLazyTau
     bool rev;   // sweep the KV tiles last to first
 };
@@ -135,7 +148,7 @@ struct Tile {
 // Key tile processed at step j of a work tile (odd rounds sweep backwards).
 __device__ __forceinline__ int kv_tile(const Tile &T, int j) { return T.rev ? T.n_kv - 1 - j : j; }
 
-template <int CAUSAL, int DT>
+template <int CAUSAL, int DT, bool PV8>
 __device__ __forceinline__ Tile decode_tile(const Params &p, int tile)
 {
     Tile t;
@@ -188,6 +201,20 @@ __device__ __forceinline__ Tile decode_tile(const Params &p, int tile)
             t.cert = __ldg(&p.tile_certs[static_cast<int64_t>(t.bh) * p.nqb + t.qb]) != 0 &&
                      (!DT || __ldg(&p.certs[t.bh].C) <= 15);
     }
+    // FP8 P.V: a certified head whose bound also fits the E4M3 budget
+    // (B_h <= min(8, C)), whose V fits E4M3 (G <= 8) and which has at least
+    // kE4m3MinKeys keys; forced for every head by CLIS_CERTIFIED_FORCED.
+    t.f8 = false;
+    if (PV8 && t.cert) {
+        if (p.variant == CLIS_CERTIFIED_FORCED) {
+            t.f8 = true;
+        } else {
+            const float bh = __ldg(&p.certs[t.bh].B_h);
+            const int cc = __ldg(&p.certs[t.bh].C);
+            t.f8 = bh <= static_cast<float>(cc < kE4m3Budget ? cc : kE4m3Budget) &&
+                   __ldg(&p.certs[t.bh].G) <= kE4m3MaxG && p.Nk >= kE4m3MinKeys;
+        }
+    }
     return t;
 }
 
@@ -208,9 +235,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
 // Runs on all 32 lanes of its warp (warp-uniform control flow); one elected
 // lane issues the copies.
 
-template <int D, int CAUSAL, int DT>
+template <int D, int CAUSAL, int DT, bool PV8>
 __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
-                              const CUtensorMap *tm_v, uint32_t sQ0, uint32_t sKV)
+                              const CUtensorMap *tm_v, const CUtensorMap *tm_vt8, uint32_t sQ0, uint32_t sKV)
 {
     using C = Cfg<D>;
     volatile int *ab = &c.abort_flag;
@@ -223,7 +250,7 @@ __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, 
     int w = 0;
     int q_issued = -1;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
-        const Tile T = decode_tile<CAUSAL, DT>(p, tile);
+        const Tile T = decode_tile<CAUSAL, DT, PV8>(p, tile);
         for (int t = 0; t < 2; t++) {
             if (!mbar_wait_warp(smem_u32(&c.q_empty[t]), (w & 1) ^ 1, ab, err, kErrProducer)) goto abort;
             if (leader) {
@@ -252,12 +279,20 @@ __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, 
             }
             if (leader) {
                 const uint32_t bar = smem_u32(&c.kv_full[gq % C::NSTAGE]);
-                mbar_arrive_expect_tx(bar, nl * C::TILE_BYTES);
+                // An FP8 tile's V is its E4M3 transpose (16 KB), loaded into the first
+                // half of its ring slot.
+                const bool v8 = PV8 && T.f8 && gi > 0;
+                mbar_arrive_expect_tx(bar, nl * C::TILE_BYTES - (v8 ? C::TILE_BYTES - kVt8TileBytes : 0));
                 for (int l = 0; l < nl; l++) {
                     const uint32_t slot = (it + l) % C::NSTAGE;
                     const bool is_v = gi > 0 && l == 0;  // a group's first tile is V_{gi-1}, then K_{gi}
-                    const CUtensorMap *tm = is_v ? tm_v : tm_k;
                     const int key_tile = kv_tile(T, is_v ? gi - 1 : gi);
+                    if (PV8 && is_v && T.f8) {
+                        // V^T [B*H][d][Nk] E4M3: keys x (128 bytes), d rows, head.
+                        tma_load_3d_hint(sKV + slot * C::TILE_BYTES, tm_vt8, bar, key_tile * BN, 0, T.bh, pol_kv);
+                        continue;
+                    }
+                    const CUtensorMap *tm = is_v ? tm_v : tm_k;
 #pragma unroll
                     for (int bx = 0; bx < C::NBOX; bx++)
                         tma_load_4d_hint(sKV + slot * C::TILE_BYTES + bx * C::BOX_BYTES, tm, bar, bx * 64,
@@ -311,7 +346,19 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
         umma_ts(o_tmem, p_tmem + kk * 8, vd + ((kk * 2048) >> 4), IDESC_O, (accumulate | kk) ? 1u : 0u);
 }
 
-template <int D, int CAUSAL, int DT>
+// P V with E4M3 operands: P (E4M3, four keys per 32-bit TMEM column) from TMEM,
+// V^T (E4M3, d rows of 128 keys, K-major, 128-byte swizzle) from shared memory;
+// K = 32 keys = 32 bytes per instruction.
+template <int D>
+__device__ __forceinline__ void issue_pv8(uint32_t o_tmem, uint32_t p_tmem, uint64_t vtd, uint32_t accumulate)
+{
+    constexpr uint32_t IDESC_O8 = idesc_e4m3_f32(BM, D);
+#pragma unroll
+    for (int kk = 0; kk < BN / 32; kk++)
+        umma_ts_f8(o_tmem, p_tmem + kk * 8, vtd + ((kk * 32) >> 4), IDESC_O8, (accumulate | kk) ? 1u : 0u);
+}
+
+template <int D, int CAUSAL, int DT, bool PV8>
 __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, uint32_t sKV)
 {
     using C = Cfg<D>;
@@ -328,7 +375,7 @@ __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, u
     const uint64_t kvd_v = sdesc_sw128(sKV, C::BOX_BYTES, 1024);
     auto stage_off = [](uint32_t s) -> uint64_t { return (s * C::TILE_BYTES) >> 4; };
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
-        const Tile T = decode_tile<CAUSAL, DT>(p, tile);
+        const Tile T = decode_tile<CAUSAL, DT, PV8>(p, tile);
         for (int t = 0; t < 2; t++)
             if (!mbar_wait_warp(smem_u32(&c.q_full[t]), w & 1, ab, err, kErrMma)) goto abort;
         {
@@ -372,8 +419,12 @@ __device__ void mma_role(const Params &p, Ctl &c, uint32_t tmem, uint32_t sQ0, u
                     if (!mbar_wait_warp(smem_u32(&c.o_free[t]), (w & 1) ^ 1, ab, err, kErrMma)) goto abort;
                 tc_fence_after();
                 if (leader) {
-                    issue_pv<D, DT>(tmem + (t ? C::TM_O1 : C::TM_O0), tmem + (t ? C::TM_S1 : C::TM_S0), vd,
-                                j > 0 ? 1u : 0u);
+                    if (PV8 && T.f8)
+                        issue_pv8<D>(tmem + (t ? C::TM_O1 : C::TM_O0), tmem + (t ? C::TM_S1 : C::TM_S0),
+                                     kvd_k + stage_off(vs), j > 0 ? 1u : 0u);
+                    else
+                        issue_pv<D, DT>(tmem + (t ? C::TM_O1 : C::TM_O0), tmem + (t ? C::TM_S1 : C::TM_S0), vd,
+                                        j > 0 ? 1u : 0u);
                     umma_commit(smem_u32(&c.pv_done[t]));
                     if (t == 1) umma_commit(smem_u32(&c.kv_empty[vs]));
                 }
@@ -402,7 +453,7 @@ abort:
 
 // ------------------------------------------------------------------- softmax
 
-template <int D, int CAUSAL, int DT>
+template <int D, int CAUSAL, int DT, bool PV8>
 __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, int lane)
 {
     using C = Cfg<D>;
@@ -419,7 +470,7 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
     int w = 0;
 
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
-        const Tile T = decode_tile<CAUSAL, DT>(p, tile);
+        const Tile T = decode_tile<CAUSAL, DT, PV8>(p, tile);
         const int row = T.qb * 2 * BM + t * BM + rl;  // query index within the head
         const bool row_ok = row < p.Nq;
 
@@ -515,20 +566,43 @@ __device__ void softmax_role(const Params &p, Ctl &c, uint32_t tmem, int warp, i
             // two MUFU ex2, one packed add into the row sum, one bf16x2 pack.
             const float2 sc2 = make_float2(sl2, sl2), sh2 = make_float2(nshift, nshift);
             float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
+            if (PV8 && T.f8) {
+                // E4M3 P: four keys per 32-bit column, the first 32 columns of S.
 #pragma unroll
-            for (int c32 = 0; c32 < BN / 32; c32++) {
-                uint32_t pk[16];
+                for (int c32 = 0; c32 < BN / 32; c32++) {
+                    uint32_t pk[8];
 #pragma unroll
-                for (int e = 0; e < 16; e++) {
-                    const float2 x = ffma2(make_float2(__uint_as_float(s[c32 * 32 + 2 * e]),
-                                                       __uint_as_float(s[c32 * 32 + 2 * e + 1])),
-                                           sc2, sh2);
-                    const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                    if (e & 1) lb = fadd2(lb, pp);
-                    else la = fadd2(la, pp);
-                    pk[e] = pack2<DT>(pp.x, pp.y);
+                    for (int e = 0; e < 16; e += 2) {
+                        const float2 x0 = ffma2(make_float2(__uint_as_float(s[c32 * 32 + 2 * e]),
+                                                            __uint_as_float(s[c32 * 32 + 2 * e + 1])),
+                                                sc2, sh2);
+                        const float2 x1 = ffma2(make_float2(__uint_as_float(s[c32 * 32 + 2 * e + 2]),
+                                                            __uint_as_float(s[c32 * 32 + 2 * e + 3])),
+                                                sc2, sh2);
+                        const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+                        const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+                        la = fadd2(la, p0);
+                        lb = fadd2(lb, p1);
+                        pk[e >> 1] = pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
+                    }
+                    tmem_st8(tS + c32 * 8, pk);
                 }
-                tmem_st16(tS + c32 * 16, pk);
+            } else {
+#pragma unroll
+                for (int c32 = 0; c32 < BN / 32; c32++) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; e++) {
+                        const float2 x = ffma2(make_float2(__uint_as_float(s[c32 * 32 + 2 * e]),
+                                                           __uint_as_float(s[c32 * 32 + 2 * e + 1])),
+                                               sc2, sh2);
+                        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        if (e & 1) lb = fadd2(lb, pp);
+                        else la = fadd2(la, pp);
+                        pk[e] = pack2<DT>(pp.x, pp.y);
+                    }
+                    tmem_st16(tS + c32 * 16, pk);
+                }
             }
             const float2 lab = fadd2(la, lb);
             l_run = l_run * alpha + (lab.x + lab.y);
@@ -678,7 +752,7 @@ __device__ __forceinline__ void write_row(const Params &p, const Tile &T, uint32
 
 // ---------------------------------------------------------------- correction
 
-template <int D, int CAUSAL, int DT>
+template <int D, int CAUSAL, int DT, bool PV8>
 __device__ void correction_role(const Params &p, Ctl &c, uint32_t tmem, int warp, int lane)
 {
     using C = Cfg<D>;
@@ -690,7 +764,7 @@ __device__ void correction_role(const Params &p, Ctl &c, uint32_t tmem, int warp
     uint32_t g = 0, ncorr = 0;
     int w = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
-        const Tile T = decode_tile<CAUSAL, DT>(p, tile);
+        const Tile T = decode_tile<CAUSAL, DT, PV8>(p, tile);
         if (T.cert || T.lazy) {
             g += T.n_kv;
         } else {
@@ -743,10 +817,11 @@ __device__ void correction_role(const Params &p, Ctl &c, uint32_t tmem, int warp
 
 // -------------------------------------------------------------------- kernel
 
-template <int D, int CAUSAL, int DT>
+template <int D, int CAUSAL, int DT, bool PV8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const Params p)
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_vt8,
+                    const Params p)
 {
     using C = Cfg<D>;
     extern __shared__ uint8_t dsmem[];
@@ -781,6 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        if (PV8) tma_prefetch_desc(&tm_vt8);
     }
     if (warp == 13) {
         tmem_alloc(smem_u32(&ctl.tmem_base), C::TMEM_COLS);
@@ -795,14 +871,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // correction 128 x 80, producer/MMA group 128 x 80 -> 45056 + 10240 + 10240 = 65536.
     if (warp < 8) {
         setmaxnreg_inc<176>();
-        softmax_role<D, CAUSAL, DT>(p, ctl, tmem, warp, lane);
+        softmax_role<D, CAUSAL, DT, PV8>(p, ctl, tmem, warp, lane);
     } else if (warp < 12) {
         setmaxnreg_dec<80>();
-        correction_role<D, CAUSAL, DT>(p, ctl, tmem, warp, lane);
+        correction_role<D, CAUSAL, DT, PV8>(p, ctl, tmem, warp, lane);
     } else {
         setmaxnreg_dec<80>();
-        if (warp == 12) producer_role<D, CAUSAL, DT>(p, ctl, &tm_q, &tm_k, &tm_v, sQ0, sKV);
-        if (warp == 13) mma_role<D, CAUSAL, DT>(p, ctl, tmem, sQ0, sKV);
+        if (warp == 12) producer_role<D, CAUSAL, DT, PV8>(p, ctl, &tm_q, &tm_k, &tm_v, &tm_vt8, sQ0, sKV);
+        if (warp == 13) mma_role<D, CAUSAL, DT, PV8>(p, ctl, tmem, sQ0, sKV);
     }
 
     tc_fence_before();
@@ -851,7 +927,23 @@ bool make_map(CUtensorMap *map, const void *base, int dtype, int64_t B, int64_t 
     return r == CUDA_SUCCESS;
 }
 
-template <int D, int CAUSAL, int DT>
+// 3-D map over the E4M3 V^T buffer [B*H][d][Nk] (row pitch `pitch` bytes,
+// innermost first: keys, d, head), 128 x 128 boxes, 128-byte swizzle.
+bool make_map_vt8(CUtensorMap *map, const void *base, int64_t BH, int64_t Nk, int64_t d, int64_t pitch)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(Nk), static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch), static_cast<cuuint64_t>(pitch * d)};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D, int CAUSAL, int DT, bool PV8 = false>
 clis_status_t launch_impl(const AttnArgs &a, cudaStream_t stream)
 {
     using C = Cfg<D>;
@@ -859,14 +951,19 @@ clis_status_t launch_impl(const AttnArgs &a, cudaStream_t stream)
     if (cudaGetDevice(&dev) != cudaSuccess) return CLIS_ERR_CUDA;
     int nsm = 0;
     if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return CLIS_ERR_CUDA;
-    if (cudaFuncSetAttribute(attn_fwd_kernel<D, CAUSAL, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_fwd_kernel<D, CAUSAL, DT, PV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
         return CLIS_ERR_CUDA;
 
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mvt8;
     if (!make_map(&mq, a.q, DT, a.B, a.H, a.Nq, D, a.q_sb, a.q_sh, a.q_sn)) return CLIS_ERR_CUDA;
     if (!make_map(&mk, a.k, DT, a.B, a.H, a.Nk, D, a.k_sb, a.k_sh, a.k_sn)) return CLIS_ERR_CUDA;
     if (!make_map(&mv, a.v, DT, a.B, a.H, a.Nk, D, a.v_sb, a.v_sh, a.v_sn)) return CLIS_ERR_CUDA;
+    if (PV8) {
+        if (!make_map_vt8(&mvt8, a.vt8, static_cast<int64_t>(a.B) * a.H, a.Nk, D, a.vt8_pitch)) return CLIS_ERR_CUDA;
+    } else {
+        mvt8 = mv;  // never read
+    }
 
     Params p;
     p.q = a.q;
@@ -909,7 +1006,7 @@ clis_status_t launch_impl(const AttnArgs &a, cudaStream_t stream)
     }
     if (p.num_tiles <= 0) return CLIS_OK;
     const int grid = p.num_tiles < nsm ? p.num_tiles : nsm;
-    attn_fwd_kernel<D, CAUSAL, DT><<<grid, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+    attn_fwd_kernel<D, CAUSAL, DT, PV8><<<grid, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, mvt8, p);
     return cudaGetLastError() == cudaSuccess ? CLIS_OK : CLIS_ERR_CUDA;
 }
 
@@ -961,6 +1058,52 @@ __global__ void chunk_finalize_kernel(ChunkFinalizeArgs a)
     if (a.lse2 && c8 == 0) a.lse2[ridx] = a.m_acc[ridx] + log2f(l);
 }
 
+// V -> its E4M3 transpose V^T [B*H][d][pitch] (round to nearest even,
+// saturating at +-448; keys from Nk up to the pitch are zero).  One block per
+// 128 keys of one head: the tile goes through shared memory so that both the
+// bf16 reads (rows of d) and the byte writes (rows of keys) are coalesced.
+__global__ void __launch_bounds__(256) v_to_e4m3t_kernel(VtArgs a)
+{
+    __shared__ uint32_t tile[128][128 / 4 + 1];  // [d][keys / 4], four E4M3 keys per word (+1 word: banks)
+    const int bh = blockIdx.y;
+    const int b = bh / a.H, h = bh % a.H;
+    const int key0 = blockIdx.x * 128;
+    const int d = a.d;
+    const int vpr = d / 8;  // 16-byte vectors per V row
+    const uint16_t *vh = a.v + b * a.v_sb + h * a.v_sh;
+    // Phase 1: each thread converts 8 consecutive d of 4 consecutive keys, so
+    // one word per d holds those 4 keys.
+    for (int it = threadIdx.x; it < 32 * vpr; it += blockDim.x) {
+        const int kq = it / vpr;  // key quad 0..31
+        const int c8 = it % vpr;  // d vector
+        float x[4][8];
+#pragma unroll
+        for (int r = 0; r < 4; r++) {
+            const int key = key0 + 4 * kq + r;
+            uint4 u = make_uint4(0u, 0u, 0u, 0u);
+            if (key < a.Nk) u = *reinterpret_cast<const uint4 *>(vh + static_cast<int64_t>(key) * a.v_sn + c8 * 8);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                x[r][2 * e] = __uint_as_float(w[e] << 16);
+                x[r][2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; e++) tile[c8 * 8 + e][kq] = pack_e4m3x4(x[0][e], x[1][e], x[2][e], x[3][e]);
+    }
+    __syncthreads();
+    // Phase 2: each row of V^T (one d) gets 128 bytes = eight 16-byte chunks.
+    uint8_t *out = a.vt + static_cast<int64_t>(bh) * d * a.pitch;
+    for (int it = threadIdx.x; it < d * 8; it += blockDim.x) {
+        const int c = it / 8, ch = it % 8;
+        const int k = key0 + ch * 16;
+        if (k >= a.pitch) continue;
+        const uint4 val = make_uint4(tile[c][4 * ch], tile[c][4 * ch + 1], tile[c][4 * ch + 2], tile[c][4 * ch + 3]);
+        *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(c) * a.pitch + k) = val;
+    }
+}
+
 }  // namespace
 
 clis_status_t launch_chunk_finalize(const ChunkFinalizeArgs &a, cudaStream_t stream)
@@ -972,6 +1115,15 @@ clis_status_t launch_chunk_finalize(const ChunkFinalizeArgs &a, cudaStream_t str
     return cudaGetLastError() == cudaSuccess ? CLIS_OK : CLIS_ERR_CUDA;
 }
 
+clis_status_t launch_v_to_e4m3t(const VtArgs &a, cudaStream_t stream)
+{
+    const int64_t BH = static_cast<int64_t>(a.B) * a.H;
+    if (BH == 0) return CLIS_OK;
+    const dim3 grid(static_cast<unsigned>((a.pitch + 127) / 128), static_cast<unsigned>(BH));
+    v_to_e4m3t_kernel<<<grid, 256, 0, stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? CLIS_OK : CLIS_ERR_CUDA;
+}
+
 clis_status_t launch_wait_selftest(uint32_t limit_us, cudaStream_t stream)
 {
     wait_selftest_kernel<<<1, 32, 0, stream>>>(static_cast<uint64_t>(limit_us) * 1000ull);
@@ -980,6 +1132,8 @@ clis_status_t launch_wait_selftest(uint32_t limit_us, cudaStream_t stream)
 
 clis_status_t launch_attn_fwd(const AttnArgs &a, cudaStream_t stream)
 {
+    // FP8 P.V: d = 128, BF16 data, no mask (checked by the caller).
+    if (a.vt8) return launch_impl<128, kNonCausal, 0, true>(a, stream);
     // Causal mode: plain causal, or a causal KV chunk (a separate instantiation,
     // so the key offset costs the plain causal kernel nothing).
     const int cm = !a.causal ? kNonCausal : (a.chunk_mode ? kCausalChunk : kCausal);

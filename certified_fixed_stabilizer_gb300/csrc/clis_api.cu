@@ -45,6 +45,10 @@ int fmt_emax(int f) { return f == CLIS_FMT_FP16 ? 15 : 127; }
 
 int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Bytes per row of the E4M3 V^T buffer: Nk rounded up to 16 (TMA strides are
+// multiples of 16 bytes).
+int64_t vt8_pitch(int64_t Nk) { return div_up(Nk, 16) * 16; }
+
 }  // namespace
 
 extern "C" {
@@ -163,7 +167,7 @@ namespace {
 clis_status_t attn_fwd_impl(const clis_shape_t *shape, const void *q, const void *k, const void *v, void *o,
                             float *lse2, const float *kbar, const clis_head_cert_t *certs,
                             const uint8_t *tile_certs, const float *mu, float scale_log2, int causal,
-                            clis_variant_t variant, clis_stream_t stream)
+                            clis_variant_t variant, clis_stream_t stream, const void *vt8 = nullptr)
 {
     clis_status_t st = check_shape(shape, true);
     if (st != CLIS_OK) return st;
@@ -213,6 +217,8 @@ clis_status_t attn_fwd_impl(const clis_shape_t *shape, const void *q, const void
     a.causal = causal;
     a.variant = variant;
     a.tile_certs = tile_certs;
+    a.vt8 = static_cast<const uint8_t *>(vt8);
+    a.vt8_pitch = vt8_pitch(shape->Nk);
     const int64_t tiles = shape->B * shape->H * div_up(shape->Nq, clis::kQueryBlockRows);
     if (tiles > kMaxN) return CLIS_ERR_UNSUPPORTED;
     return clis::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream));
@@ -238,6 +244,52 @@ clis_status_t clis_attn_fwd_tiles(const clis_shape_t *shape, const void *q, cons
     if (!causal || variant != CLIS_AUTO) return CLIS_ERR_INVALID_ARG;  // per-prefix: causal AUTO only
     return attn_fwd_impl(shape, q, k, v, o, lse2, kbar, certs, tile_certs, mu, scale_log2, causal, variant,
                          stream);
+}
+
+clis_status_t clis_v_e4m3_size(const clis_shape_t *shape, size_t *bytes)
+{
+    if (!shape || !bytes) return CLIS_ERR_INVALID_ARG;
+    if (shape->B < 0 || shape->H < 0 || shape->Nk < 1 || shape->d < 1) return CLIS_ERR_INVALID_ARG;
+    *bytes = static_cast<size_t>(shape->B * shape->H * shape->d * vt8_pitch(shape->Nk));
+    return CLIS_OK;
+}
+
+clis_status_t clis_v_to_e4m3(const clis_shape_t *shape, const void *v, void *vt8, clis_stream_t stream)
+{
+    clis_status_t st = check_shape(shape, false);
+    if (st != CLIS_OK) return st;
+    if (shape->dtype != CLIS_DT_BF16) return CLIS_ERR_UNSUPPORTED;
+    if (shape->B * shape->H == 0) return CLIS_OK;
+    if (!v || !vt8) return CLIS_ERR_INVALID_ARG;
+    if (!aligned16(v) || !aligned16(vt8)) return CLIS_ERR_MISALIGNED;
+    if (shape->B * shape->H > 65535) return CLIS_ERR_UNSUPPORTED;  // grid.y
+    clis::VtArgs a;
+    a.v = static_cast<const uint16_t *>(v);
+    a.v_sb = shape->v_sb;
+    a.v_sh = shape->v_sh;
+    a.v_sn = shape->v_sn;
+    a.B = static_cast<int>(shape->B);
+    a.H = static_cast<int>(shape->H);
+    a.Nk = static_cast<int>(shape->Nk);
+    a.d = static_cast<int>(shape->d);
+    a.vt = static_cast<uint8_t *>(vt8);
+    a.pitch = vt8_pitch(shape->Nk);
+    return clis::launch_v_to_e4m3t(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+clis_status_t clis_attn_fwd_fp8pv(const clis_shape_t *shape, const void *q, const void *k, const void *v,
+                                  const void *vt8, void *o, float *lse2, const float *kbar,
+                                  const clis_head_cert_t *certs, const float *mu, float scale_log2,
+                                  clis_variant_t variant, clis_stream_t stream)
+{
+    clis_status_t st = check_shape(shape, true);
+    if (st != CLIS_OK) return st;
+    if (shape->d != 128 || shape->dtype != CLIS_DT_BF16) return CLIS_ERR_UNSUPPORTED;
+    if (variant != CLIS_AUTO && variant != CLIS_CERTIFIED_FORCED) return CLIS_ERR_INVALID_ARG;
+    if (shape->B * shape->H == 0 || shape->Nq == 0) return CLIS_OK;
+    if (!vt8) return CLIS_ERR_INVALID_ARG;
+    if (!aligned16(vt8)) return CLIS_ERR_MISALIGNED;
+    return attn_fwd_impl(shape, q, k, v, o, lse2, kbar, certs, nullptr, mu, scale_log2, 0, variant, stream, vt8);
 }
 
 clis_status_t clis_certify_noalloc(const clis_shape_t *shape, const void *q, const void *k, const void *v,

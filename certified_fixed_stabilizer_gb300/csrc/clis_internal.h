@@ -84,7 +84,21 @@ struct AttnArgs {
     int chunk_mode = 0;  // 0 off, 1 merge into the accumulators, 2 first chunk
     float *o_acc = nullptr, *l_acc = nullptr, *m_acc = nullptr;
     int k_off = 0;  // causal KV chunk: index of the chunk's first key in the head
+    // FP8 P.V path: V^T in E4M3 [B*H][d][vt8_pitch] (nullptr: BF16 P.V only).
+    const uint8_t *vt8 = nullptr;
+    int64_t vt8_pitch = 0;
 };
+
+// Conversion of V to its E4M3 transpose for the FP8 P.V path.
+struct VtArgs {
+    const uint16_t *v;  // bf16 [B, H, Nk, d]
+    int64_t v_sb, v_sh, v_sn;
+    int B, H, Nk, d;
+    uint8_t *vt;        // E4M3 [B*H][d][pitch]
+    int64_t pitch;      // bytes per row of V^T: Nk rounded up to 16
+};
+
+clis_status_t launch_v_to_e4m3t(const VtArgs &a, cudaStream_t stream);
 
 struct ChunkFinalizeArgs {
     const float *o_acc, *l_acc, *m_acc;

@@ -211,6 +211,38 @@ CLIS_API clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, c
                             const clis_head_cert_t *certs, const float *mu, float scale_log2,
                             int causal, clis_variant_t variant, clis_stream_t stream);
 
+/* FP8 P.V path.  Figure 3 tabulates exp2 limits per format; one step below
+ * FP16 is E4M3 (largest finite value 448, so U_exp = log2 448 and the budget
+ * is floor(U_exp) = 8).  One tcgen05.mma of kind::f8f6f4 takes both operands
+ * in 8 bits, so P in E4M3 needs V in E4M3 too.  A head takes this path when it
+ * certifies (clis_certify, BF16/FP32 formats) and also B_h <= min(8, C) and
+ * G <= 8 (max |V| <= 256 fits E4M3) -- these make E4M3 safe -- and, for
+ * accuracy, Nk >= 4096; every other head runs exactly as in clis_attn_fwd
+ * (certified BF16 path or online softmax).  The row sum stays the fp32 sum of
+ * the unrounded exp2 outputs.  Accuracy: V's E4M3 rounding (up to 2^-4
+ * relative per entry) averages over the keys, so on diffuse heads the mean
+ * output error is about 0.033 / sqrt(Nk) (2e-4 at 32,760 keys, 1.4e-3 at 513)
+ * and the largest about ten times the BF16 path's; sharp heads (B_h above 8)
+ * never qualify.
+ *
+ * clis_v_e4m3_size: bytes of the E4M3 V^T buffer, B*H*d*pitch with pitch =
+ *   Nk rounded up to 16.
+ * clis_v_to_e4m3: writes V^T [b*H + h][c][j] = E4M3(V[b, h, j, c]) (round to
+ *   nearest even, saturating at +-448; bytes from Nk to the pitch are 0).
+ *   BF16 V only (CLIS_ERR_UNSUPPORTED for FP16); vt8 16-byte aligned.
+ * clis_attn_fwd_fp8pv: clis_attn_fwd (no mask) for d = 128 and BF16 data
+ *   (CLIS_ERR_UNSUPPORTED otherwise) that also takes vt8 from clis_v_to_e4m3
+ *   of the same v.  variant: CLIS_AUTO (the rule above) or
+ *   CLIS_CERTIFIED_FORCED (every head on the FP8 P.V path whatever its
+ *   certificate or length: benchmarks and tests only); other variants
+ *   CLIS_ERR_INVALID_ARG. */
+CLIS_API clis_status_t clis_v_e4m3_size(const clis_shape_t *shape, size_t *bytes);
+CLIS_API clis_status_t clis_v_to_e4m3(const clis_shape_t *shape, const void *v, void *vt8, clis_stream_t stream);
+CLIS_API clis_status_t clis_attn_fwd_fp8pv(const clis_shape_t *shape, const void *q, const void *k,
+                                           const void *v, const void *vt8, void *o, float *lse2,
+                                           const float *kbar, const clis_head_cert_t *certs, const float *mu,
+                                           float scale_log2, clis_variant_t variant, clis_stream_t stream);
+
 /* Per-prefix certificates for causal attention: clis_certify plus one flag per
  * block of 256 query rows.  The pages certify causal heads with the head's
  * bound (Table 3) and state no finer rule; this entry point is a finer reading

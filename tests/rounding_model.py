@@ -61,3 +61,23 @@ def backward(q, k, v, o, g, lse2, scale: float, causal: bool):
     dV = bf16(P).T @ g
     dS = bf16(P * (g @ v.T - D))
     return scale * (dS @ k), scale * (dS.T @ q), dV
+
+
+def e4m3(x) -> np.ndarray:
+    """Round to the nearest E4M3 value (ties to even), saturating at +-448."""
+    x = np.clip(np.asarray(x, dtype=np.float32), -448.0, 448.0)
+    return torch.from_numpy(x).to(torch.float8_e4m3fn).float().double().numpy()
+
+
+def certified_forward_fp8pv(q, k, v, scale: float, rows=None):
+    """One head, no mask, on the FP8 P.V path: p = exp2(scale_log2 * s - mu_i)
+    rounded to E4M3 for the P V product with V rounded to E4M3, the row sum of
+    the unrounded p, O rounded to bf16.  Returns (O before its final rounding,
+    lse2) for the given rows (default all)."""
+    sl2 = scale * LOG2E
+    qr = q if rows is None else q[rows]
+    mu = sl2 * (qr @ k.mean(axis=0))
+    p = np.exp2(sl2 * (qr @ k.T) - mu[:, None])
+    l = p.sum(axis=1)
+    o = (e4m3(p) @ e4m3(v)) / l[:, None]
+    return o, mu + np.log2(l)
