@@ -470,7 +470,11 @@ def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
     and one group's kernel can start on SMs the previous one has left idle
     (heads are independent).  The call returns once ``out`` is filled,
     unless ``non_blocking``: then the current stream is ordered after the work
-    and the caller synchronises it before reading ``out``.
+    and the caller synchronises it before reading ``out`` (or changing q, k,
+    v).  The device staging buffers and streams are kept for the next call
+    with the same shapes (one set per device), so consecutive non-blocking
+    calls overlap: a call's copies of a head group start as soon as the
+    previous call's kernels on that group are done.
     """
     if q.device.type == "cpu":
         return _attention_host(q, k, v, softmax_scale, causal, variant, return_certs,
@@ -487,20 +491,50 @@ def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
     return res
 
 
+class _HostPipeline:
+    """Device staging buffers, streams and per-group events of the host-tensor
+    path, kept across calls with the same shapes (allocated once, so no call
+    waits on an allocation; the next call's copies of a head group start as
+    soon as the previous call's kernels on that group have read their inputs).
+
+    Per group g: copy-in (stream s_in) waits until the previous call's kernels
+    on g finished (ev_run[g]); the kernels (one of two compute streams,
+    alternating by group) wait for the copy-in and for the previous call's
+    copy-out of g (ev_out[g]), so the output slice is free; the copy-out
+    (stream s_out) waits for the kernels."""
+
+    def __init__(self, q, k, dev, certified):
+        B, H, Nq, d = q.shape
+        self.key = None
+        self.qd = torch.empty(q.shape, dtype=q.dtype, device=dev)
+        self.kd = torch.empty(k.shape, dtype=k.dtype, device=dev)
+        self.vd = torch.empty(k.shape, dtype=k.dtype, device=dev)
+        self.od = torch.empty(q.shape, dtype=q.dtype, device=dev)
+        self.kbar = torch.empty((B * H, d), dtype=torch.float32, device=dev) if certified else None
+        self.certs = torch.empty((B * H, CERT_WORDS), dtype=torch.int32, device=dev) if certified else None
+        self.mu = torch.empty(B * H * Nq, dtype=torch.float32, device=dev) if certified else None
+        self.s_in, self.s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        self.s_runs = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
+        self.ev_run, self.ev_out = {}, {}
+        self.ev_consumed = None  # the caller's copies of kbar / certs (return_certs)
+
+
+_pipelines: dict = {}
+
+
 def _attention_host(q, k, v, softmax_scale, causal, variant, return_certs, dev, out, groups, non_blocking):
     B, H, Nq, d = q.shape
-    Nk = k.shape[2]
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned())
-    qd = torch.empty(q.shape, dtype=q.dtype, device=dev)
-    kd = torch.empty(k.shape, dtype=k.dtype, device=dev)
-    vd = torch.empty(v.shape, dtype=v.dtype, device=dev)
-    od = torch.empty(q.shape, dtype=q.dtype, device=dev)
     sl2 = scale_log2_for(d, softmax_scale)
     certified = variant in ("auto", "certified")
-    kbar = torch.empty((B * H, d), dtype=torch.float32, device=dev) if certified else None
-    certs = torch.empty((B * H, CERT_WORDS), dtype=torch.int32, device=dev) if certified else None
-    mu = torch.empty(B * H * Nq, dtype=torch.float32, device=dev) if certified else None
+    key = (dev, tuple(q.shape), tuple(k.shape), q.dtype, certified, groups)
+    pl = _pipelines.get(dev)
+    if pl is None or pl.key != key:
+        if pl is not None:
+            torch.cuda.synchronize(dev)  # the old buffers may still be in use
+        pl = _pipelines[dev] = _HostPipeline(q, k, dev, certified)
+        pl.key = key
     # head groups: contiguous (b, h0:h1) slices, about `groups` of them in total
     per = max(1, -(-B * H // max(1, groups)))
     spans = []
@@ -508,44 +542,52 @@ def _attention_host(q, k, v, softmax_scale, causal, variant, return_certs, dev, 
         for h0 in range(0, H, per):
             spans.append((b, h0, min(H, h0 + per)))
     cur = torch.cuda.current_stream(dev)
-    # Two compute streams, alternating by group: the persistent attention kernel of one
-    # group leaves SMs idle in its last wave, and the next group's kernel can start there.
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    s_runs = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
-    for s in (s_in, s_out) + s_runs:
-        s.wait_stream(cur)
+    if pl.ev_consumed is not None:
+        for s_run in pl.s_runs:
+            s_run.wait_event(pl.ev_consumed)
+        pl.ev_consumed = None
     for gi, (b, h0, h1) in enumerate(spans):
-        s_run = s_runs[gi % 2]
+        s_run = pl.s_runs[gi % 2]
         sl = (slice(b, b + 1), slice(h0, h1))
         ev_in = torch.cuda.Event()
-        with torch.cuda.stream(s_in):
-            qd[sl].copy_(q[sl], non_blocking=True)
-            kd[sl].copy_(k[sl], non_blocking=True)
-            vd[sl].copy_(v[sl], non_blocking=True)
-            ev_in.record(s_in)
+        with torch.cuda.stream(pl.s_in):
+            if gi in pl.ev_run:
+                pl.s_in.wait_event(pl.ev_run[gi])
+            pl.qd[sl].copy_(q[sl], non_blocking=True)
+            pl.kd[sl].copy_(k[sl], non_blocking=True)
+            pl.vd[sl].copy_(v[sl], non_blocking=True)
+            ev_in.record(pl.s_in)
         s_run.wait_event(ev_in)
+        if gi in pl.ev_out:
+            s_run.wait_event(pl.ev_out[gi])
         f0, f1 = b * H + h0, b * H + h1
-        ev_run = torch.cuda.Event()
+        ev_run = pl.ev_run[gi] = torch.cuda.Event()
         with torch.cuda.stream(s_run):
             kb = cs = m = None
             if certified:
-                kb, cs, m = kbar[f0:f1], certs[f0:f1], mu[f0 * Nq:f1 * Nq]
-                clis_certify(qd[sl], kd[sl], vd[sl], sl2, kbar=kb, certs=cs, mu=m, exp_fmt=_exp_fmt(q),
+                kb, cs, m = pl.kbar[f0:f1], pl.certs[f0:f1], pl.mu[f0 * Nq:f1 * Nq]
+                clis_certify(pl.qd[sl], pl.kd[sl], pl.vd[sl], sl2, kbar=kb, certs=cs, mu=m, exp_fmt=_exp_fmt(q),
                              stream=s_run)
-            clis_attn_fwd(qd[sl], kd[sl], vd[sl], sl2, kbar=kb, certs=cs, causal=causal, variant=variant,
-                          mu=m, out=od[sl], stream=s_run)
+            clis_attn_fwd(pl.qd[sl], pl.kd[sl], pl.vd[sl], sl2, kbar=kb, certs=cs, causal=causal, variant=variant,
+                          mu=m, out=pl.od[sl], stream=s_run)
             ev_run.record(s_run)
-        s_out.wait_event(ev_run)
-        with torch.cuda.stream(s_out):
-            out[sl].copy_(od[sl], non_blocking=True)
-    cur.wait_stream(s_out)
-    for t in (qd, kd, vd, od, kbar, certs, mu):
-        if t is not None:
-            for s in (s_in, s_out) + s_runs:
-                t.record_stream(s)
+        pl.s_out.wait_event(ev_run)
+        ev_out = pl.ev_out[gi] = torch.cuda.Event()
+        with torch.cuda.stream(pl.s_out):
+            out[sl].copy_(pl.od[sl], non_blocking=True)
+            ev_out.record(pl.s_out)
+    # The caller's stream is ordered after every output copy.
+    cur.wait_stream(pl.s_out)
     if not non_blocking:
-        s_out.synchronize()
+        pl.s_out.synchronize()
     if return_certs:
+        kbar, certs = pl.kbar, pl.certs
+        if certified:
+            # Copies on the caller's stream (ordered after every kernel above);
+            # the next call's kernels wait for them before reusing the buffers.
+            kbar, certs = kbar.clone(), certs.clone()
+            pl.ev_consumed = torch.cuda.Event()
+            pl.ev_consumed.record(cur)
         return out, kbar, certs
     return out
 

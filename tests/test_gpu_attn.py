@@ -239,6 +239,41 @@ def test_host_path_pipelined_over_head_groups(causal):
     assert_close_to_oracle(host.float().numpy().reshape(ref.shape), ref, "host pipelined")
 
 
+def test_host_path_back_to_back_non_blocking_calls():
+    """Consecutive non-blocking host calls with the same shapes reuse one set of
+    staging buffers and overlap (a call's copies of a head group wait only for
+    the previous call's kernels on that group): each call's output must be
+    its own inputs' attention, including a call whose certificates are asked
+    for (copied out on the caller's stream) between two others."""
+    dev = need_gpu()
+    g = torch.Generator(device="cpu")
+    g.manual_seed(23)
+    B, H, N, d = 1, 6, 1500, 128
+    ins, outs = [], []
+    for i in range(4):
+        q = torch.randn(B, H, N, d, generator=g).to(torch.bfloat16).pin_memory()
+        k = (torch.randn(B, H, N, d, generator=g) * 0.5 + 0.2 * i).to(torch.bfloat16).pin_memory()
+        v = torch.randn(B, H, N, d, generator=g).to(torch.bfloat16).pin_memory()
+        ins.append((q, k, v))
+    certs = None
+    for i, (q, k, v) in enumerate(ins):
+        o = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+        if i == 2:
+            _, _, certs = clis.attention(q, k, v, groups=3, out=o, non_blocking=True, return_certs=True)
+        else:
+            clis.attention(q, k, v, groups=3, out=o, non_blocking=True)
+        outs.append(o)
+    torch.cuda.synchronize()
+    for i, ((q, k, v), o) in enumerate(zip(ins, outs)):
+        dev_out, _, dcerts = clis.attention(q.to(dev), k.to(dev), v.to(dev), return_certs=True)
+        torch.cuda.synchronize()
+        assert_paths_agree(flat(o.to(dev)), flat(dev_out), f"back-to-back call {i}")
+        if i == 2:
+            assert torch.equal(certs, dcerts)
+    ref, _ = _oracle(*ins[3], False)
+    assert_close_to_oracle(outs[3].float().numpy().reshape(ref.shape), ref, "back-to-back last call")
+
+
 def test_outputs_are_deterministic():
     dev = need_gpu()
     w = WORKLOADS["mixed"]
