@@ -69,15 +69,25 @@ def e4m3(x) -> np.ndarray:
     return torch.from_numpy(x).to(torch.float8_e4m3fn).float().double().numpy()
 
 
-def certified_forward_fp8pv(q, k, v, scale: float, rows=None):
+def certified_forward_fp8pv(q, k, v, scale: float, rows=None, with_flip_bound=False):
     """One head, no mask, on the FP8 P.V path: p = exp2(scale_log2 * s - mu_i)
     rounded to E4M3 for the P V product with V rounded to E4M3, the row sum of
     the unrounded p, O rounded to bf16.  Returns (O before its final rounding,
-    lse2) for the given rows (default all)."""
+    lse2) for the given rows (default all).
+
+    with_flip_bound: also return how far one E4M3 rounding decision that goes
+    the other way can move an output: one E4M3 step (at most 2^-3 of the
+    weight) times the largest normalised weight p_ij / l_i of the head times
+    max |V|.  A kernel whose fp32 p differs from this model's by a few ulp
+    takes the other rounding now and then; with few keys per row one such
+    decision dominates the difference."""
     sl2 = scale * LOG2E
     qr = q if rows is None else q[rows]
     mu = sl2 * (qr @ k.mean(axis=0))
     p = np.exp2(sl2 * (qr @ k.T) - mu[:, None])
     l = p.sum(axis=1)
     o = (e4m3(p) @ e4m3(v)) / l[:, None]
+    if with_flip_bound:
+        flip = 2.0 ** -3 * float((p / l[:, None]).max()) * float(np.abs(v).max())
+        return o, mu + np.log2(l), flip
     return o, mu + np.log2(l)

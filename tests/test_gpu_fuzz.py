@@ -123,3 +123,79 @@ def test_random_backward_matches_oracle(seed):
         keep = ref_max > 1e-6  # a head whose gradient is zero in exact arithmetic (one key: dQ = dK = 0)
         if keep.any():
             assert_grads_close(flat(g.contiguous()).float().cpu().numpy()[keep], r[keep], name, what)
+
+
+@pytest.mark.parametrize("seed", range(200, 210))
+def test_random_causal_chunks_match_oracle(seed):
+    """Causal KV chunks at random split points (any offset, one-key chunks),
+    a random variant, per-prefix flags on some cases, chunks after the first in
+    random order: the finalized output against the oracle's causal attention."""
+    r = random.Random(seed)
+    d = r.choice([64, 128])
+    B, H = r.choice([1, 2]), r.choice([1, 3])
+    N = r.choice([129, 300, 700, 1000, 1409])
+    dtype = r.choice([torch.bfloat16, torch.bfloat16, torch.float16])
+    variant = r.choice(["auto", "auto", "online", "online_lazy"])
+    n_cuts = r.choice([1, 2, 4])
+    cuts = sorted(set(r.randrange(1, N) for _ in range(n_cuts)))
+    if r.random() < 0.3 and N > 3:
+        cuts = sorted(set(cuts + [cuts[0] + 1] if cuts[0] + 1 < N else cuts))  # a one-key chunk
+    bounds = [0] + cuts + [N]
+    w, q, k, v = _inputs(seed, True, d, B, H, N, N, dtype, False)
+    sl2 = clis.scale_log2_for(d)
+    exp_fmt = "fp16" if dtype == torch.float16 else "bf16"
+    use_tiles = variant == "auto" and r.random() < 0.5
+    if use_tiles:
+        kbar, certs, tiles = clis.clis_certify_tiles(q, k, v, sl2, exp_fmt=exp_fmt)
+    else:
+        kbar, certs = clis.clis_certify(q, k, v, sl2, exp_fmt=exp_fmt)
+        tiles = None
+    BHN = B * H * N
+    o_acc = torch.full((BHN, d), float("nan"), device=q.device)
+    l_acc = torch.full((BHN,), float("nan"), device=q.device)
+    m_acc = torch.full((BHN,), float("nan"), device=q.device)
+    chunks = list(zip(bounds[:-1], bounds[1:]))
+    order = [0] + r.sample(range(1, len(chunks)), len(chunks) - 1)
+    for n, i in enumerate(order):
+        a, b = chunks[i]
+        clis.clis_attn_fwd_chunk_causal(q, k[:, :, a:b], v[:, :, a:b], sl2, o_acc, l_acc, m_acc, a, kbar=kbar,
+                                        certs=certs, tile_certs=tiles, first=(n == 0), variant=variant)
+    lse2 = torch.empty(BHN, device=q.device)
+    out = clis.clis_attn_chunk_finalize(q, o_acc, l_acc, m_acc, lse2=lse2)
+    torch.cuda.synchronize()
+    ref, rlse = oracle.attention(flat(q).cpu(), flat(k).cpu(), flat(v).cpu(), d ** -0.5, causal=True,
+                                 with_lse2=True)
+    what = f"fuzz causal chunks {seed}: d={d} B={B} H={H} N={N} {exp_fmt} {variant} bounds={bounds} tiles={use_tiles}"
+    assert_close_to_oracle(flat(out).float().cpu().numpy(), ref, what)
+    np.testing.assert_allclose(lse2.cpu().numpy().reshape(rlse.shape), rlse, atol=3e-3, rtol=0)
+
+
+@pytest.mark.parametrize("seed", range(300, 308))
+def test_random_fp8pv_matches_rounding_model(seed):
+    """Forced FP8 P.V on random shapes and layouts against the CPU model of the
+    same E4M3 roundings (the bound of tests/test_gpu_fp8pv.py)."""
+    import rounding_model as rm
+    r = random.Random(seed)
+    B, H = r.choice([1, 2]), r.choice([1, 3])
+    Nq = r.choice([1, 100, 128, 300, 777])
+    Nk = r.choice([1, 5, 128, 129, 640, 1500])
+    strided = r.random() < 0.5
+    w, q, k, v = _inputs(seed, False, 128, B, H, max(Nq, Nk), max(Nq, Nk), torch.bfloat16, strided)
+    q, k, v = q[:, :, :Nq], k[:, :, :Nk], v[:, :, :Nk]
+    sl2 = clis.scale_log2_for(128)
+    kbar, certs = clis.clis_certify(q, k, v, sl2)
+    vt8 = clis.clis_v_to_e4m3(v)
+    out = clis.clis_attn_fwd_fp8pv(q, k, v, vt8, sl2, kbar=kbar, certs=certs, variant="certified")
+    torch.cuda.synchronize()
+    got = flat(out).float().cpu().numpy()
+    qf, kf, vf = (flat(t.contiguous()).double().cpu().numpy() for t in (q, k, v))
+    for h in range(qf.shape[0]):
+        # Beyond half a bf16 ulp the two may differ by E4M3 rounding decisions of p
+        # that fp32 order tips the other way: two such per row, plus 1e-4 for the rest
+        # (with thousands of keys a flip moves an output by 1e-4 or less; with 129
+        # keys by up to ~2e-3).
+        e, _, flip = rm.certified_forward_fp8pv(qf[h], kf[h], vf[h], w.softmax_scale(), with_flip_bound=True)
+        sc = max(1.0, np.abs(e).max())
+        excess = np.maximum(np.abs(got[h] - e) - np.abs(e) * 2.0 ** -8, 0.0).max() / sc
+        mean = np.abs(got[h] - rm.bf16(e)).mean() / sc
+        assert excess <= 2 * flip / sc + 1e-4 and mean <= 1e-5, (seed, h, Nq, Nk, strided, excess, flip / sc, mean)
