@@ -1,12 +1,19 @@
 /*
  * c_abi_example.c -- the library used from plain C (no Python, no torch):
- * certify and run the fused forward on inputs read from files, write O, lse2
- * and the certificates back.  Built and run by tests/test_gpu_c_abi.py, which
+ * certify and run the forward on inputs read from files, write O, lse2 and
+ * the certificates back.  Built and run by tests/test_gpu_c_abi.py, which
  * writes the inputs and compares the outputs with the oracle.
  *
- *   c_abi_example <dir> B H N d causal
+ *   c_abi_example <dir> B H N d causal [mode]
  *   reads  <dir>/q.bin k.bin v.bin   (bf16 bits, [B, H, N, d] contiguous)
  *   writes <dir>/o.bin (bf16), lse2.bin (fp32), certs.bin (clis_head_cert_t)
+ *   mode   fused    clis_certify + clis_attn_fwd (default)
+ *          noalloc  clis_certify_noalloc + clis_attn_fwd
+ *          chunks   clis_certify, then K/V in three chunks merged by
+ *                   clis_attn_fwd_chunk (causal: clis_attn_fwd_chunk_causal,
+ *                   chunk offsets as key_offset), then clis_attn_chunk_finalize
+ *          fp8      clis_certify + clis_v_to_e4m3 + clis_attn_fwd_fp8pv with
+ *                   every head forced onto E4M3 P.V (no mask, d = 128)
  * Exit status 0 on success; any CUDA or library error prints a message and
  * exits 1.
  */
@@ -14,6 +21,7 @@
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include <cuda_runtime.h>
 
@@ -61,10 +69,11 @@ static int write_file(const char *dir, const char *name, const void *src, size_t
 
 int main(int argc, char **argv)
 {
-    if (argc != 7) return fail("usage", "c_abi_example <dir> B H N d causal");
+    if (argc != 7 && argc != 8) return fail("usage", "c_abi_example <dir> B H N d causal [mode]");
     const char *dir = argv[1];
     const int64_t B = atol(argv[2]), H = atol(argv[3]), N = atol(argv[4]), d = atol(argv[5]);
     const int causal = atoi(argv[6]);
+    const char *mode = argc == 8 ? argv[7] : "fused";
     const size_t elems = (size_t)(B * H * N * d), bytes = elems * 2, rows = (size_t)(B * H * N);
 
     clis_shape_t s;
@@ -99,10 +108,51 @@ int main(int argc, char **argv)
     cudaStream_t stream;
     CUDA_OK(cudaStreamCreate(&stream));
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)d);  /* log2(e) / sqrt(d) */
-    CLIS_OK_(clis_certify(&s, q, k, v, scale_log2, CLIS_FMT_BF16, CLIS_FMT_FP32, kbar, certs, mu, ws, ws_bytes,
-                          (clis_stream_t)stream));
-    CLIS_OK_(clis_attn_fwd(&s, q, k, v, o, lse2, kbar, certs, mu, scale_log2, causal, CLIS_AUTO,
-                           (clis_stream_t)stream));
+    const clis_stream_t cs = (clis_stream_t)stream;
+    if (strcmp(mode, "noalloc") == 0)
+        CLIS_OK_(clis_certify_noalloc(&s, q, k, v, scale_log2, CLIS_FMT_BF16, CLIS_FMT_FP32, kbar, certs, mu, cs));
+    else
+        CLIS_OK_(clis_certify(&s, q, k, v, scale_log2, CLIS_FMT_BF16, CLIS_FMT_FP32, kbar, certs, mu, ws, ws_bytes,
+                              cs));
+    if (strcmp(mode, "fused") == 0 || strcmp(mode, "noalloc") == 0) {
+        CLIS_OK_(clis_attn_fwd(&s, q, k, v, o, lse2, kbar, certs, mu, scale_log2, causal, CLIS_AUTO, cs));
+    } else if (strcmp(mode, "chunks") == 0) {
+        /* K/V in three chunks (the split points leave ragged tiles); fp32
+         * accumulators O [rows, d], l [rows], m [rows]. */
+        float *o_acc, *l_acc, *m_acc;
+        CUDA_OK(cudaMalloc((void **)&o_acc, rows * (size_t)d * sizeof(float)));
+        CUDA_OK(cudaMalloc((void **)&l_acc, rows * sizeof(float)));
+        CUDA_OK(cudaMalloc((void **)&m_acc, rows * sizeof(float)));
+        const int64_t cut[4] = {0, N / 3 + 1, 2 * N / 3 + 5, N};
+        for (int c = 0; c < 3; c++) {
+            clis_shape_t sc = s;
+            sc.Nk = cut[c + 1] - cut[c];
+            const uint16_t *kc = (const uint16_t *)k + cut[c] * d, *vc = (const uint16_t *)v + cut[c] * d;
+            if (causal)
+                CLIS_OK_(clis_attn_fwd_chunk_causal(&sc, q, kc, vc, o_acc, l_acc, m_acc, kbar, certs, NULL, mu,
+                                                    scale_log2, cut[c], c == 0, CLIS_AUTO, cs));
+            else
+                CLIS_OK_(clis_attn_fwd_chunk(&sc, q, kc, vc, o_acc, l_acc, m_acc, kbar, certs, mu, scale_log2,
+                                             c == 0, CLIS_AUTO, cs));
+        }
+        CLIS_OK_(clis_attn_chunk_finalize(&s, o_acc, l_acc, m_acc, o, lse2, cs));
+        CUDA_OK(cudaStreamSynchronize(stream));
+        cudaFree(o_acc);
+        cudaFree(l_acc);
+        cudaFree(m_acc);
+    } else if (strcmp(mode, "fp8") == 0) {
+        size_t vt_bytes = 0;
+        void *vt8;
+        CLIS_OK_(clis_v_e4m3_size(&s, &vt_bytes));
+        CUDA_OK(cudaMalloc(&vt8, vt_bytes));
+        CLIS_OK_(clis_v_to_e4m3(&s, v, vt8, cs));
+        CLIS_OK_(clis_attn_fwd_fp8pv(&s, q, k, v, vt8, o, lse2, kbar, certs, mu, scale_log2, CLIS_CERTIFIED_FORCED,
+                                     cs));
+        CUDA_OK(cudaStreamSynchronize(stream));
+        cudaFree(vt8);
+    } else {
+        return fail("mode", mode);
+    }
     CUDA_OK(cudaStreamSynchronize(stream));
     uint32_t code = 0;
     if (clis_get_device_error(&code) != CLIS_OK || code != 0) return fail("device error word", "set");
