@@ -375,8 +375,10 @@ def main():
         n_e2e = max(1, min(args.steps, 10))
         with ClockSampler(local) as cs_e2e:
             e0.record(stream)
+            e0.synchronize()  # the first step's copies are queued after the start mark
             for _ in range(n_e2e):
                 e2e_step()
+            stream.wait_event(clis.host_done_event(dev))  # after the last step's output copy
             e1.record(stream)
             torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, ws)

@@ -468,13 +468,14 @@ def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
     copies in and out on two streams and the kernels on two more (alternating
     groups), so that the copies of one group overlap the compute of another
     and one group's kernel can start on SMs the previous one has left idle
-    (heads are independent).  The call returns once ``out`` is filled,
-    unless ``non_blocking``: then the current stream is ordered after the work
-    and the caller synchronises it before reading ``out`` (or changing q, k,
-    v).  The device staging buffers and streams are kept for the next call
-    with the same shapes (one set per device), so consecutive non-blocking
-    calls overlap: a call's copies of a head group start as soon as the
-    previous call's kernels on that group are done.
+    (heads are independent).  The input copies follow the work already queued
+    on the current stream.  The call returns once ``out`` is filled, unless
+    ``non_blocking``: then it returns after queueing, and the caller waits for
+    :func:`host_done_event` (or synchronises the device) before reading
+    ``out`` or changing q, k, v.  The device staging buffers and streams are
+    kept for the next call with the same shapes (one set per device), so
+    consecutive non-blocking calls overlap: a call's copies of a head group
+    start as soon as the previous call's kernels on that group are done.
     """
     if q.device.type == "cpu":
         return _attention_host(q, k, v, softmax_scale, causal, variant, return_certs,
@@ -517,6 +518,7 @@ class _HostPipeline:
         self.s_runs = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
         self.ev_run, self.ev_out = {}, {}
         self.ev_consumed = None  # the caller's copies of kbar / certs (return_certs)
+        self.ev_done = None      # after the last output copy of the latest call
 
 
 _pipelines: dict = {}
@@ -542,6 +544,11 @@ def _attention_host(q, k, v, softmax_scale, causal, variant, return_certs, dev, 
         for h0 in range(0, H, per):
             spans.append((b, h0, min(H, h0 + per)))
     cur = torch.cuda.current_stream(dev)
+    # The copies of the inputs follow whatever the caller queued on its stream
+    # before this call (for instance the copies that fill the host inputs).
+    ev_entry = torch.cuda.Event()
+    ev_entry.record(cur)
+    pl.s_in.wait_event(ev_entry)
     if pl.ev_consumed is not None:
         for s_run in pl.s_runs:
             s_run.wait_event(pl.ev_consumed)
@@ -576,20 +583,34 @@ def _attention_host(q, k, v, softmax_scale, causal, variant, return_certs, dev, 
         with torch.cuda.stream(pl.s_out):
             out[sl].copy_(pl.od[sl], non_blocking=True)
             ev_out.record(pl.s_out)
-    # The caller's stream is ordered after every output copy.
-    cur.wait_stream(pl.s_out)
+    # Done once the last output copy is: host_done_event() returns this event.
+    # (The caller's stream is not made to wait for it, so that its next call's
+    # copies can start while this call's last groups still run.)
+    pl.ev_done = torch.cuda.Event()
+    pl.ev_done.record(pl.s_out)
     if not non_blocking:
         pl.s_out.synchronize()
     if return_certs:
         kbar, certs = pl.kbar, pl.certs
         if certified:
-            # Copies on the caller's stream (ordered after every kernel above);
-            # the next call's kernels wait for them before reusing the buffers.
+            # Copies on the caller's stream, after every kernel above; the next
+            # call's kernels wait for them before reusing the buffers.
+            for s_run in pl.s_runs:
+                cur.wait_stream(s_run)
             kbar, certs = kbar.clone(), certs.clone()
             pl.ev_consumed = torch.cuda.Event()
             pl.ev_consumed.record(cur)
         return out, kbar, certs
     return out
+
+
+def host_done_event(device=None):
+    """The event after the last output copy of the most recent host-tensor
+    attention() call on ``device`` (default cuda:0), or None: a stream that
+    waits for it (``stream.wait_event(...)``) is ordered after that call's
+    output, and ``.synchronize()`` waits for it on the host."""
+    pl = _pipelines.get(torch.device(device or "cuda:0"))
+    return None if pl is None else pl.ev_done
 
 
 load_library()

@@ -274,6 +274,29 @@ def test_host_path_back_to_back_non_blocking_calls():
     assert_close_to_oracle(outs[3].float().numpy().reshape(ref.shape), ref, "back-to-back last call")
 
 
+def test_host_path_follows_work_queued_on_the_current_stream():
+    """Host inputs filled by asynchronous copies queued on the current stream
+    (behind a long kernel) are read only after those copies: the call's input
+    copies follow the caller's stream."""
+    dev = need_gpu()
+    w = WORKLOADS["480p"]
+    q, k, v = make_inputs(w, device=dev, N=1200, H=4, seed=31)
+    hosts = [torch.zeros(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3)]
+    a = torch.randn(8192, 8192, device=dev)
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    for _ in range(3):
+        a = a @ a / 8192.0  # a few milliseconds of work ahead of the copies
+    for h, t in zip(hosts, (q, k, v)):
+        h.copy_(t, non_blocking=True)
+    out = clis.attention(*hosts, groups=2)
+    torch.cuda.synchronize()
+    ref = clis.attention(q, k, v)
+    torch.cuda.synchronize()
+    assert_paths_agree(flat(out.to(dev)), flat(ref), "host inputs from queued copies")
+    del a, cur
+
+
 def test_outputs_are_deterministic():
     dev = need_gpu()
     w = WORKLOADS["mixed"]
