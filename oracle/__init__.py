@@ -39,7 +39,7 @@ _SRC = os.path.join(_HERE, "clis_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libclis_oracle.so")
 
-FMT = {"fp16": 0, "bf16": 1, "fp32": 2}
+FMT = {"fp16": 0, "bf16": 1, "fp32": 2, "e4m3": 3}
 
 _lib = None
 _lock = threading.Lock()

@@ -60,7 +60,7 @@
 #endif
 
 /* Format codes of this file (the Python wrapper maps names onto them). */
-enum { ORC_FMT_FP16 = 0, ORC_FMT_BF16 = 1, ORC_FMT_FP32 = 2 };
+enum { ORC_FMT_FP16 = 0, ORC_FMT_BF16 = 1, ORC_FMT_FP32 = 2, ORC_FMT_E4M3 = 3 };
 
 typedef struct {
     int32_t certified; /* 1 = fixed-stabiliser path is safe for this head     */
@@ -107,7 +107,11 @@ static double bits_to_double(uint16_t b, int in_fmt)
 double oracle_decode(uint16_t bits, int in_fmt) { return bits_to_double(bits, in_fmt); }
 
 /* Largest finite value of a binary floating-point format with p significand
- * bits (implicit bit included) and maximum exponent emax: (2 - 2^(1-p)) 2^emax. */
+ * bits (implicit bit included) and maximum exponent emax: (2 - 2^(1-p)) 2^emax.
+ * E4M3 (the 8-bit format one step below Figure 3's FP16, as the OCP 8-bit
+ * floating-point definition fixes it: 4 exponent bits with bias 7, 3 fraction
+ * bits, no infinities) keeps its all-ones pattern for NaN, so its largest
+ * finite significand is 1.110b = 1.75 and its maximum 1.75 * 2^8 = 448. */
 static double format_max_finite(int fmt)
 {
     int p, emax;
@@ -115,6 +119,7 @@ static double format_max_finite(int fmt)
     case ORC_FMT_FP16: p = 11; emax = 15; break;
     case ORC_FMT_BF16: p = 8; emax = 127; break;
     case ORC_FMT_FP32: p = 24; emax = 127; break;
+    case ORC_FMT_E4M3: return (2.0 - ldexp(1.0, -2)) * ldexp(1.0, 8);
     default: return NAN;
     }
     return (2.0 - ldexp(1.0, 1 - p)) * ldexp(1.0, emax);

@@ -126,6 +126,12 @@ def test_auto_routes_heads_by_eligibility():
     cs = clis.decode_certs(certs)
     elig = [_fp8_eligible(c, N) for c in cs]
     assert 0 < sum(elig) < len(elig)
+    # The same rule from the oracle's certificate under the E4M3 budget (Algorithm 1
+    # with exp_fmt = E4M3: C = min(8, 127 - A)), independent of the GPU's numbers.
+    _, oc = oracle.certify(q.cpu(), k.cpu(), v.cpu(), sl2, exp_fmt="e4m3")
+    for h, (e, c) in enumerate(zip(elig, oc)):
+        if not c["band"]:
+            assert e == (bool(c["certified"]) and c["G"] <= 8 and N >= 4096), (h, c)
     fo, ff, fb = flat(out), flat(forced), flat(bf)
     for h, e in enumerate(elig):
         assert torch.equal(fo[h], ff[h] if e else fb[h]), (h, e)
@@ -144,6 +150,23 @@ def test_auto_keeps_short_heads_on_bf16():
     bf = clis.clis_attn_fwd(q, k, v, clis.scale_log2_for(w.d), kbar=kbar, certs=certs, mu=mu)
     torch.cuda.synchronize()
     assert torch.equal(out, bf)
+
+
+@pytest.mark.parametrize("Nk", [4095, 4096])
+def test_auto_key_count_threshold(Nk):
+    """AUTO takes E4M3 from 4096 keys on: 4095 keys give the BF16 kernel's
+    output, 4096 the forced FP8 output, bit for bit."""
+    dev = need_gpu()
+    w = WORKLOADS["480p"]
+    q, _, _ = make_inputs(w, device=dev, N=600, H=2, seed=51)
+    _, k, v = make_inputs(w, device=dev, N=Nk, H=2, seed=52)
+    out, _, kbar, certs, mu = _run(q, k, v, "auto")
+    forced, _, _, _, _ = _run(q, k, v, "certified")
+    bf = clis.clis_attn_fwd(q, k, v, clis.scale_log2_for(w.d), kbar=kbar, certs=certs, mu=mu)
+    torch.cuda.synchronize()
+    assert all(c["certified"] and c["B_h"] <= 8 for c in clis.decode_certs(certs))
+    assert torch.equal(out, forced if Nk >= 4096 else bf)
+    assert not torch.equal(forced, bf)
 
 
 @pytest.mark.parametrize("Nq,Nk", [(1, 1), (127, 129), (1000, 300), (257, 1025)])

@@ -44,6 +44,7 @@ def test_format_limits_match_golden_and_libraries(oracle_mod):
     assert abs(2.0 ** oracle_mod.format_log2_max("fp16") - float(np.finfo(np.float16).max)) < 1e-9
     assert abs(2.0 ** oracle_mod.format_log2_max("fp32") / float(np.finfo(np.float32).max) - 1) < 1e-14
     assert abs(2.0 ** oracle_mod.format_log2_max("bf16") / torch.finfo(torch.bfloat16).max - 1) < 1e-14
+    assert abs(2.0 ** oracle_mod.format_log2_max("e4m3") - torch.finfo(torch.float8_e4m3fn).max) < 1e-9
 
 
 def test_exp2_limits_in_each_format(oracle_mod):
@@ -58,6 +59,11 @@ def test_exp2_limits_in_each_format(oracle_mod):
     Ub = math.floor(oracle_mod.format_log2_max("bf16"))
     t = torch.exp2(torch.tensor([float(Ub), float(Ub + 1)], dtype=torch.bfloat16))
     assert torch.isfinite(t[0]) and torch.isinf(t[1])
+    # E4M3 has no infinity: 2^8 = 256 is exact, 2^9 = 512 lies beyond its largest
+    # value 448 (torch's conversion gives NaN there, a saturating one 448).
+    U8 = math.floor(oracle_mod.format_log2_max("e4m3"))
+    t8 = torch.tensor([2.0 ** U8, 2.0 ** (U8 + 1)]).to(torch.float8_e4m3fn).float()
+    assert t8[0].item() == 256.0 and not (abs(t8[1].item()) <= 448.0)
 
 
 # ------------------------------------------------------- Algorithm 1, 5-7 ----
@@ -85,6 +91,8 @@ def test_exponent_budget_closed_forms(oracle_mod):
         assert oracle_mod.exponent_budget("fp16", "fp32", A) == min(15, 127 - A)
         assert oracle_mod.exponent_budget("bf16", "fp16", A) == 15 - A
         assert oracle_mod.exponent_budget("fp16", "fp16", A) == 15 - A
+        # E4M3 exp outputs (the FP8 P.V path), FP32 accumulator: min(8, 127 - A)
+        assert oracle_mod.exponent_budget("e4m3", "fp32", A) == min(8, 127 - A)
 
 
 # ------------------------------------------------- hand-built boundary heads ----
@@ -133,6 +141,21 @@ def test_boundary_head_just_above_fails(oracle_mod):
     _, certs = oracle_mod.certify(q, k, v, scale_log2=1.0 / 16)
     c = certs[0]
     assert c["B_h"] == 125.5 and c["certified"] == 0 and c["reason"] == 1
+
+
+def test_boundary_heads_under_the_e4m3_budget(oracle_mod):
+    """With E4M3 exp outputs the budget is min(8, 127 - A) = 8: B_h = 8 exactly
+    certifies (the tie), B_h = 8.0625 fails, and the same heads certify easily
+    under the BF16 budget (C = 125)."""
+    d = 64
+    for qv, B, ok in ((128.0, 8.0, 1), (129.0, 8.0625, 0)):
+        q0 = np.zeros(d, dtype=np.float32)
+        q0[0] = qv
+        q, k, v = _head(_pm_keys(d, 1.0), [q0])
+        _, c8 = oracle_mod.certify(q, k, v, scale_log2=1.0 / 16, exp_fmt="e4m3")
+        _, cb = oracle_mod.certify(q, k, v, scale_log2=1.0 / 16)
+        assert c8[0]["C"] == 8 and c8[0]["B_h"] == B and c8[0]["certified"] == ok, c8[0]
+        assert cb[0]["C"] == 125 and cb[0]["certified"] == 1
 
 
 def test_centering_is_applied(oracle_mod):
