@@ -725,6 +725,7 @@ __device__ __forceinline__ void write_row(const Params &p, const Tile &T, uint32
     } else {
         const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
         uint16_t *orow = p.o + T.b * p.o_sb + T.h * p.o_sh + static_cast<int64_t>(row) * p.o_sn;
+        const uint64_t pol_o = policy_evict_first();
 #pragma unroll
         for (int c32 = 0; c32 < D / 32; c32++) {
             uint32_t r[32];
@@ -739,9 +740,14 @@ __device__ __forceinline__ void write_row(const Params &p, const Tile &T, uint32
                         fmul2(make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), inv2);
                     pk[e] = pack2<DT>(o2.x, o2.y);
                 }
+                // O is written once and never read here: evict-first, so that the
+                // stream of output lines does not push the K/V tiles that every
+                // query block of the head rereads out of L2.
                 uint4 *dst = reinterpret_cast<uint4 *>(orow + c32 * 32);
 #pragma unroll
-                for (int e = 0; e < 4; e++) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                for (int e = 0; e < 4; e++)
+                    st_global_v4_hint(dst + e, make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]),
+                                      pol_o);
             }
         }
         if (p.lse2 && row_ok) {

@@ -302,6 +302,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r)
         : "memory");
 }
 
+// 16-byte global store with an L2 cache-policy hint (createpolicy value).
+__device__ __forceinline__ void st_global_v4_hint(void *addr, uint4 v, uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(policy)
+                 : "memory");
+}
+
 // ------------------------------------------------------------ reductions
 
 // Fire-and-forget fp32 adds into global memory (no value returned, so the
