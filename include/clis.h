@@ -167,13 +167,14 @@ CLIS_API clis_status_t clis_certify(const clis_shape_t *shape, const void *q, co
  * until the process exits.  The caller still provides q, k, v, kbar and
  * certs.  Nothing is allocated or freed, by this call or by any routine it
  * uses.
- *   - Each call made outside stream capture looks up the array's device
- *     address in the current context with cudaGetSymbolAddress (the first
- *     such call on a device does this set-up; it allocates nothing).  A call
- *     made while `stream` is being captured uses the address found by the last
- *     call outside capture in the same context, so make one call on each
- *     device (and again after a device reset) before capturing; without one
- *     the call returns CLIS_ERR_CUDA.
+ *   - The first call on a device (with that device current) does the set-up:
+ *     it looks up the array's device address with cudaGetSymbolAddress (which
+ *     allocates nothing).  Make that first call before any stream capture on
+ *     that device.  Later calls made outside capture repeat the lookup in the
+ *     current context, so a device reset or another context gets its own
+ *     address; a call made while `stream` is being captured does no lookup and
+ *     uses the address of the last lookup in the same context (CLIS_ERR_CUDA
+ *     if there was none).
  *   - All calls share the one array and it keeps what the last call left in
  *     it.  The kernels overwrite every scratch word they read, so nothing
  *     needs clearing between calls, but calls that overlap on the GPU (two
