@@ -86,3 +86,38 @@ def test_fp8pv_leg_mixed_full_size():
     ref, _ = oracle.attention(flat(q).cpu(), flat(k).cpu(), flat(v).cpu(), w.softmax_scale(), rows=rows,
                               with_lse2=True)
     assert_close_to_oracle(flat(out)[:, rows].float().cpu().numpy(), ref, "mixed fp8 P.V")
+
+
+def test_backward_leg_720p_full_size():
+    """The backward as the bench times it at 720p (from a forward that wrote
+    lse2): dQ on seed-chosen rows of three heads against the oracle's row-wise
+    dQ, and two identities over every head: sum_j dV_j = sum_i dO_i (each row's
+    softmax weights sum to 1) and sum_j dK_j = 0 (each row's dS sums to 0)."""
+    from certified_fixed_stabilizer_gb300.workloads import make_dout
+    from gpu_util import assert_grads_close
+    dev = need_gpu()
+    w = WORKLOADS["720p"]
+    q, k, v = make_inputs(w, device=dev)
+    do = make_dout(q.shape, device=dev)
+    o, lse2 = clis.attention_fwd_lse(q, k, v)
+    dq, dk, dv = clis.attention_bwd(q, k, v, o, do, lse2)
+    torch.cuda.synchronize()
+    heads, rows = [0, 21, 39], sample_rows(w.N, 8, seed=7)
+    ref = oracle.attention_bwd_dq_rows(flat(q)[heads].cpu(), flat(k)[heads].cpu(), flat(v)[heads].cpu(),
+                                       flat(do)[heads].cpu(), w.softmax_scale(), rows)
+    assert_grads_close(flat(dq)[heads][:, rows].float().cpu().numpy(), ref, "dq", "720p backward")
+    # sum_j dV_j = sum_i dO_i up to two roundings, each unbiased and at most 2^-9
+    # of its term: P to bf16 inside the product and each dV_j to bf16.  Summed
+    # over tens of thousands of independent terms they grow like the square
+    # root of the count, so the difference is compared with the column's own
+    # random-walk scale sqrt(sum_i dO_i^2) (a 0.1% slip in dV's scale moves it
+    # by about that scale times 1e-3).
+    dvf, dof = flat(dv).double(), flat(do).double()
+    err = (dvf.sum(dim=1) - dof.sum(dim=1)).abs()                      # [BH, d]
+    scale = dof.pow(2).sum(dim=1).sqrt()                               # [BH, d]
+    from gpu_util import report
+    report("720p backward sum dV", worst_ratio=float((err / scale).max()), worst_err=float(err.max()))
+    assert (err <= 1e-3 * scale).all(), float((err / scale).max())
+    dkf = flat(dk).double()
+    assert torch.isfinite(dkf).all()
+    assert (dkf.sum(dim=1).abs().amax(dim=1) <= 1e-2 * dkf.abs().sum(dim=1).amax(dim=1)).all()
