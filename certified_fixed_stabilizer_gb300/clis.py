@@ -458,7 +458,7 @@ def _exp_fmt(q) -> str:
 
 def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
               variant: str = "auto", return_certs: bool = False, device=None, out=None,
-              groups: int = 8, non_blocking: bool = False):
+              groups: int = 8, non_blocking: bool = False, pv: str = "bf16"):
     """CLiS attention forward: certification pre-pass, then the fused kernel.
 
     q, k, v: bf16 or fp16 [B, H, N, d].  Device tensors are processed in place
@@ -476,7 +476,23 @@ def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
     kept for the next call with the same shapes (one set per device), so
     consecutive non-blocking calls overlap: a call's copies of a head group
     start as soon as the previous call's kernels on that group are done.
+
+    ``pv="fp8"`` (device tensors, bf16, d = 128, no mask, variant "auto" or
+    "certified") runs the FP8 P.V path: V's E4M3 transpose, then
+    clis_attn_fwd_fp8pv, where heads within the E4M3 budget multiply P and V
+    in E4M3 and every other head runs as with ``pv="bf16"``.
     """
+    if pv not in ("bf16", "fp8"):
+        raise ValueError(f"pv must be 'bf16' or 'fp8', not {pv!r}")
+    if pv == "fp8":
+        if q.device.type == "cpu" or causal or variant not in ("auto", "certified"):
+            raise ValueError("pv='fp8' takes device tensors, no mask and variant 'auto' or 'certified'")
+        sl2 = scale_log2_for(q.shape[-1], softmax_scale)
+        mu = torch.empty(q.shape[0] * q.shape[1] * q.shape[2], dtype=torch.float32, device=q.device)
+        kbar, certs = clis_certify(q, k, v, sl2, mu=mu)
+        res = clis_attn_fwd_fp8pv(q, k, v, clis_v_to_e4m3(v), sl2, kbar=kbar, certs=certs, variant=variant,
+                                  out=out, mu=mu)
+        return (res, kbar, certs) if return_certs else res
     if q.device.type == "cpu":
         return _attention_host(q, k, v, softmax_scale, causal, variant, return_certs,
                                torch.device(device or "cuda:0"), out, groups, non_blocking)

@@ -197,3 +197,17 @@ def test_full_720p_sampled_rows():
     ref, _ = oracle.attention(flat(q)[heads].cpu(), flat(k)[heads].cpu(), flat(v)[heads].cpu(), w.softmax_scale(),
                               rows=rows, with_lse2=True)
     assert_close_to_oracle(got, ref, "fp8pv 720p sampled")
+
+
+def test_attention_call_with_fp8_pv():
+    """The public attention() call with pv="fp8" is certify + conversion +
+    clis_attn_fwd_fp8pv, bit for bit."""
+    dev = need_gpu()
+    w = WORKLOADS["480p"]
+    q, k, v = make_inputs(w, device=dev, N=5000, H=2, seed=61)
+    out = clis.attention(q, k, v, pv="fp8")
+    ref, _, _, _, _ = _run(q, k, v, "auto")
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    with pytest.raises(ValueError):
+        clis.attention(q, k, v, causal=True, pv="fp8")
