@@ -469,9 +469,19 @@ def main():
         l_acc = torch.empty((heads * w.N,), dtype=torch.float32, device=dev)
         m_acc = torch.empty((heads * w.N,), dtype=torch.float32, device=dev)
 
+        fp8_chunks = not w.causal and args.dtype == "bf16" and w.d == 128
+        vt8s = ([torch.empty((heads, w.d, -(-(b - a) // 16) * 16), dtype=torch.uint8, device=dev)
+                 for a, b in zip(bounds[:-1], bounds[1:])] if fp8_chunks else [])
+
         def chunk_pass(variant):
             for i, (a, b) in enumerate(zip(bounds[:-1], bounds[1:])):
-                if w.causal:
+                if variant == "fp8":
+                    # FP8 P.V: each chunk's V converted to E4M3 as it arrives, then merged.
+                    kc, vc = k[:, :, a:b], v[:, :, a:b]
+                    clis.clis_v_to_e4m3(vc, vt8s[i])
+                    clis.clis_attn_fwd_chunk_fp8pv(q, kc, vc, vt8s[i], sl2, o_acc, l_acc, m_acc, kbar=kbar,
+                                                   certs=certs, first=(i == 0), mu=mu)
+                elif w.causal:
                     clis.clis_attn_fwd_chunk_causal(q, k[:, :, a:b], v[:, :, a:b], sl2, o_acc, l_acc, m_acc, a,
                                                     kbar=kbar, certs=certs, first=(i == 0), variant=variant,
                                                     mu=mu)
@@ -481,7 +491,7 @@ def main():
             clis.clis_attn_chunk_finalize(q, o_acc, l_acc, m_acc, out=out)
 
         chunked = {"chunks": n_chunks, "causal": w.causal}
-        for variant in ("auto", "online"):
+        for variant in ("auto", "online") + (("fp8",) if fp8_chunks else ()):
             for _ in range(args.warmup):
                 chunk_pass(variant)
             torch.cuda.synchronize()
@@ -492,11 +502,11 @@ def main():
             e1.record(stream)
             torch.cuda.synchronize()
             ms = e0.elapsed_time(e1) / args.steps
-            chunked["certified" if variant == "auto" else "online"] = {
+            chunked[{"auto": "certified", "online": "online", "fp8": "certified_fp8_pv"}[variant]] = {
                 "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms": ms}
         chunked["certified_speedup_vs_online"] = chunked["online"]["ms"] / chunked["certified"]["ms"]
         line["chunked"] = chunked
-        del o_acc, l_acc, m_acc
+        del o_acc, l_acc, m_acc, vt8s
     if extras in ("all", "backward"):
         # Backward (clis_attn_bwd: row dots, dK/dV kernel, dQ kernel) on the same
         # inputs, from a forward that also wrote lse2, for a seeded dO.  FLOPs

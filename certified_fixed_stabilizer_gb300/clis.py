@@ -92,6 +92,8 @@ def load_library():
     lib.clis_v_to_e4m3.restype = i32
     lib.clis_attn_fwd_fp8pv.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, vp]
     lib.clis_attn_fwd_fp8pv.restype = i32
+    lib.clis_attn_fwd_chunk_fp8pv.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp]
+    lib.clis_attn_fwd_chunk_fp8pv.restype = i32
     lib.clis_attn_chunk_finalize.argtypes = [sp, vp, vp, vp, vp, vp, vp]
     lib.clis_attn_chunk_finalize.restype = i32
     lib.clis_debug_wait_selftest.argtypes = [ctypes.c_uint32, vp]
@@ -283,6 +285,18 @@ def clis_attn_fwd_fp8pv(q, k, v, vt8, scale_log2: float, kbar=None, certs=None, 
     if st != 0:
         raise ClisError("clis_attn_fwd_fp8pv", st)
     return out
+
+
+def clis_attn_fwd_chunk_fp8pv(q, k, v, vt8, scale_log2: float, o_acc, l_acc, m_acc, kbar=None, certs=None,
+                              first: bool = False, variant: str = "auto", stream=None, mu=None):
+    """clis_attn_fwd_chunk with the FP8 P.V path; vt8 = clis_v_to_e4m3 of this chunk's v."""
+    lib = load_library()
+    shape = make_shape(q, k, v)
+    st = lib.clis_attn_fwd_chunk_fp8pv(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(vt8), _ptr(o_acc),
+                                       _ptr(l_acc), _ptr(m_acc), _ptr(kbar), _ptr(certs), _ptr(mu),
+                                       float(scale_log2), int(bool(first)), VARIANT[variant], _stream(stream))
+    if st != 0:
+        raise ClisError("clis_attn_fwd_chunk_fp8pv", st)
 
 
 def clis_attn_fwd_chunk(q, k, v, scale_log2: float, o_acc, l_acc, m_acc, kbar=None, certs=None,

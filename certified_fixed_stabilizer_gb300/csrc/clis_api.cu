@@ -317,7 +317,8 @@ namespace {
 clis_status_t attn_chunk_impl(const clis_shape_t *shape, const void *q, const void *k, const void *v, float *o_acc,
                               float *l_acc, float *m_acc, const float *kbar, const clis_head_cert_t *certs,
                               const uint8_t *tile_certs, const float *mu, float scale_log2, int causal,
-                              int64_t key_offset, int first, clis_variant_t variant, clis_stream_t stream)
+                              int64_t key_offset, int first, clis_variant_t variant, clis_stream_t stream,
+                              const void *vt8 = nullptr)
 {
     clis_status_t st = check_shape(shape, false);
     if (st != CLIS_OK) return st;
@@ -380,6 +381,8 @@ clis_status_t attn_chunk_impl(const clis_shape_t *shape, const void *q, const vo
     a.o_acc = o_acc;
     a.l_acc = l_acc;
     a.m_acc = m_acc;
+    a.vt8 = static_cast<const uint8_t *>(vt8);
+    a.vt8_pitch = vt8_pitch(shape->Nk);
     return clis::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -394,6 +397,22 @@ clis_status_t clis_attn_fwd_chunk(const clis_shape_t *shape, const void *q, cons
 {
     return attn_chunk_impl(shape, q, k, v, o_acc, l_acc, m_acc, kbar, certs, nullptr, mu, scale_log2, 0, 0, first,
                            variant, stream);
+}
+
+clis_status_t clis_attn_fwd_chunk_fp8pv(const clis_shape_t *shape, const void *q, const void *k, const void *v,
+                                        const void *vt8, float *o_acc, float *l_acc, float *m_acc,
+                                        const float *kbar, const clis_head_cert_t *certs, const float *mu,
+                                        float scale_log2, int first, clis_variant_t variant, clis_stream_t stream)
+{
+    if (!shape) return CLIS_ERR_INVALID_ARG;
+    if (shape->d != 128 || shape->dtype != CLIS_DT_BF16) return CLIS_ERR_UNSUPPORTED;
+    if (variant != CLIS_AUTO && variant != CLIS_CERTIFIED_FORCED) return CLIS_ERR_INVALID_ARG;
+    if (shape->B * shape->H != 0 && shape->Nq != 0) {
+        if (!vt8) return CLIS_ERR_INVALID_ARG;
+        if (!aligned16(vt8)) return CLIS_ERR_MISALIGNED;
+    }
+    return attn_chunk_impl(shape, q, k, v, o_acc, l_acc, m_acc, kbar, certs, nullptr, mu, scale_log2, 0, 0, first,
+                           variant, stream, vt8);
 }
 
 clis_status_t clis_attn_fwd_chunk_causal(const clis_shape_t *shape, const void *q, const void *k, const void *v,

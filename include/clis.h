@@ -244,6 +244,17 @@ CLIS_API clis_status_t clis_attn_fwd_fp8pv(const clis_shape_t *shape, const void
                                            const float *kbar, const clis_head_cert_t *certs, const float *mu,
                                            float scale_log2, clis_variant_t variant, clis_stream_t stream);
 
+/* The ring-step form (clis_attn_fwd_chunk, no mask) with the FP8 P.V path:
+ * vt8 is clis_v_to_e4m3 of the chunk's v (k and v point at the chunk, shape->Nk
+ * its length); a head takes E4M3 by the rule above, with Nk the chunk's
+ * length.  Certified heads still merge by plain addition.  Other arguments
+ * and errors as clis_attn_fwd_chunk and clis_attn_fwd_fp8pv. */
+CLIS_API clis_status_t clis_attn_fwd_chunk_fp8pv(const clis_shape_t *shape, const void *q, const void *k,
+                                                 const void *v, const void *vt8, float *o_acc, float *l_acc,
+                                                 float *m_acc, const float *kbar, const clis_head_cert_t *certs,
+                                                 const float *mu, float scale_log2, int first,
+                                                 clis_variant_t variant, clis_stream_t stream);
+
 /* Per-prefix certificates for causal attention: clis_certify plus one flag per
  * block of 256 query rows.  The pages certify causal heads with the head's
  * bound (Table 3) and state no finer rule; this entry point is a finer reading

@@ -29,7 +29,8 @@ def test_header_declares_the_boundary():
               "clis_get_device_error", "clis_clear_device_error", "clis_debug_wait_selftest",
               "clis_attn_fwd_chunk", "clis_attn_chunk_finalize", "clis_certify_noalloc",
               "clis_attn_bwd_workspace_size", "clis_attn_bwd", "clis_certify_tiles", "clis_attn_fwd_tiles",
-              "clis_attn_fwd_chunk_causal", "clis_v_e4m3_size", "clis_v_to_e4m3", "clis_attn_fwd_fp8pv"):
+              "clis_attn_fwd_chunk_causal", "clis_v_e4m3_size", "clis_v_to_e4m3", "clis_attn_fwd_fp8pv",
+              "clis_attn_fwd_chunk_fp8pv"):
         assert n in names
 
 
@@ -209,6 +210,15 @@ def test_fp8pv_entry_points_reject_bad_arguments(clis):
     assert call(_shape(clis), vt8=0) == 1
     assert call(_shape(clis), vt8=FAKE + 8) == 3
     assert lib.clis_v_to_e4m3(ctypes.byref(s16), vp(FAKE), vp(FAKE), None) == 2
+
+    def chunk(s, vt8=FAKE, variant=0):
+        return lib.clis_attn_fwd_chunk_fp8pv(ctypes.byref(s), vp(FAKE), vp(FAKE), vp(FAKE), vp(vt8), vp(FAKE),
+                                             vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, 0.1, 1, variant, None)
+    assert chunk(_shape(clis, d=64)) == 2
+    assert chunk(s16) == 2
+    assert chunk(_shape(clis), variant=1) == 1
+    assert chunk(_shape(clis), vt8=0) == 1
+    assert chunk(_shape(clis), vt8=FAKE + 8) == 3
     assert lib.clis_v_to_e4m3(ctypes.byref(_shape(clis)), vp(FAKE), vp(0), None) == 1
     n = ctypes.c_size_t(0)
     assert lib.clis_v_e4m3_size(ctypes.byref(_shape(clis, Nk=1000)), ctypes.byref(n)) == 0

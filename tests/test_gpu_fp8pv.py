@@ -211,3 +211,40 @@ def test_attention_call_with_fp8_pv():
     assert torch.equal(out, ref)
     with pytest.raises(ValueError):
         clis.attention(q, k, v, causal=True, pv="fp8")
+
+
+def test_ring_step_chunks_with_fp8_pv():
+    """The ring-step form with E4M3 P.V: K/V of 480p-distributed heads in three
+    chunks of 4096 keys and more (each converted on its own), merged into the
+    fp32 accumulators; AUTO sends every head to E4M3 (chunks of at least 4096
+    keys) and the result meets the bar against the oracle; forced FP8 on one
+    chunk holding every key equals clis_attn_fwd_fp8pv, bit for bit."""
+    dev = need_gpu()
+    w = WORKLOADS["480p"]
+    N = 13000
+    q, k, v = make_inputs(w, device=dev, N=N, H=3, seed=71)
+    sl2 = clis.scale_log2_for(w.d)
+    mu = torch.empty(3 * N, device=dev)
+    kbar, certs = clis.clis_certify(q, k, v, sl2, mu=mu)
+    BHN = 3 * N
+
+    def run(bounds, variant):
+        o_acc = torch.full((BHN, w.d), float("nan"), device=dev)
+        l_acc = torch.full((BHN,), float("nan"), device=dev)
+        m_acc = torch.full((BHN,), float("nan"), device=dev)
+        for i, (a, b) in enumerate(zip(bounds[:-1], bounds[1:])):
+            kc, vc = k[:, :, a:b], v[:, :, a:b]
+            clis.clis_attn_fwd_chunk_fp8pv(q, kc, vc, clis.clis_v_to_e4m3(vc), sl2, o_acc, l_acc, m_acc, kbar=kbar,
+                                           certs=certs, first=(i == 0), variant=variant, mu=mu)
+        lse2 = torch.empty(BHN, device=dev)
+        out = clis.clis_attn_chunk_finalize(q, o_acc, l_acc, m_acc, lse2=lse2)
+        torch.cuda.synchronize()
+        return out, lse2
+
+    out, lse2 = run([0, 4096, 8400, N], "auto")
+    ref, rlse = oracle.attention(flat(q).cpu(), flat(k).cpu(), flat(v).cpu(), w.softmax_scale(), with_lse2=True)
+    assert_close_to_oracle(flat(out).float().cpu().numpy(), ref, "fp8pv ring step")
+    np.testing.assert_allclose(lse2.cpu().numpy().reshape(rlse.shape), rlse, atol=2e-3, rtol=0)
+    one, _ = run([0, N], "certified")
+    fused, _, _, _, _ = _run(q, k, v, "certified")
+    assert torch.equal(one, fused)
