@@ -21,11 +21,12 @@
 //   warps 4-7   softmax for query tile 1 (rows 128-255)
 //   warps 8-11  correction: rescales O in TMEM (online tiles) and writes the
 //               output of every finished tile (so softmax moves on at once)
-//   warp 12     TMA producer: Q tiles once per work tile, K and V tiles
-//               through an NSTAGE-deep shared-memory ring
+//   warp 12     TMA producer of K and V tiles, through an NSTAGE-deep
+//               shared-memory ring
 //   warp 13     MMA issuer: S = Q K^T (SMEM x SMEM -> TMEM) and
 //               O += P V (P from TMEM, V from SMEM -> TMEM); owns TMEM
-//   (warps 12 and 13 run warp-uniform code; one elected lane issues)
+//   warp 14     TMA producer of Q tiles, once per work tile
+//   (warps 12-14 run warp-uniform code; one elected lane issues)
 //
 // TMEM (512 columns x 128 lanes x 32 bit): S0 @0, S1 @128 (fp32 scores,
 // overwritten in place by P as packed bf16 in their first 64 columns),
@@ -235,20 +236,19 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
 // Runs on all 32 lanes of its warp (warp-uniform control flow); one elected
 // lane issues the copies.
 
+// Q tiles have a producer warp of their own, so that the first K/V loads of
+// the next work tile are not queued behind its Q loads, which can only start
+// once the current tile's last Q K^T has read Q.
 template <int D, int CAUSAL, int DT, bool PV8>
-__device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
-                              const CUtensorMap *tm_v, const CUtensorMap *tm_vt8, uint32_t sQ0, uint32_t sKV)
+__device__ void q_producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, uint32_t sQ0)
 {
     using C = Cfg<D>;
     volatile int *ab = &c.abort_flag;
     unsigned *err = &g_attn_error_word;
     const bool leader = elect_one();
-    const uint64_t pol_kv = policy_evict_last();
     const uint64_t pol_q = policy_evict_first();
-    uint32_t it = 0;  // K/V tiles issued (ring slot = it % NSTAGE)
-    uint32_t gq = 0;  // load groups issued (full barrier = gq % NSTAGE)
     int w = 0;
-    int q_issued = -1;
+    int q_issued[2] = {-1, -1};  // last work tile whose query tile t was issued
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
         const Tile T = decode_tile<CAUSAL, DT, PV8>(p, tile);
         for (int t = 0; t < 2; t++) {
@@ -263,8 +263,29 @@ __device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_q, 
                                      T.b, pol_q);
             }
             __syncwarp();
+            q_issued[t] = w;
         }
-        q_issued = w;
+    }
+    return;
+abort:
+    // Let the Q copies already issued land before the CTA leaves.
+    for (int t = 0; t < 2; t++)
+        if (q_issued[t] >= 0) drain_wait(smem_u32(&c.q_full[t]), q_issued[t] & 1);
+}
+
+template <int D, int CAUSAL, int DT, bool PV8>
+__device__ void producer_role(const Params &p, Ctl &c, const CUtensorMap *tm_k, const CUtensorMap *tm_v,
+                              const CUtensorMap *tm_vt8, uint32_t sKV)
+{
+    using C = Cfg<D>;
+    volatile int *ab = &c.abort_flag;
+    unsigned *err = &g_attn_error_word;
+    const bool leader = elect_one();
+    const uint64_t pol_kv = policy_evict_last();
+    uint32_t it = 0;  // K/V tiles issued (ring slot = it % NSTAGE)
+    uint32_t gq = 0;  // load groups issued (full barrier = gq % NSTAGE)
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+        const Tile T = decode_tile<CAUSAL, DT, PV8>(p, tile);
         // K and V tiles go through the NSTAGE-slot ring in the order the MMAs use them
         // (K_0, V_0, K_1, V_1, ...), and are signalled in groups by the step that first
         // needs them: {K_0}, {V_0, K_1}, ..., {V_{n-2}, K_{n-1}}, {V_{n-1}}, one full
@@ -309,8 +330,6 @@ abort:
     // Let every copy already issued land before the CTA leaves.
     for (uint32_t k = (gq > C::NSTAGE ? gq - C::NSTAGE : 0); k < gq; k++)
         drain_wait(smem_u32(&c.kv_full[k % C::NSTAGE]), (k / C::NSTAGE) & 1);
-    if (q_issued >= 0)
-        for (int t = 0; t < 2; t++) drain_wait(smem_u32(&c.q_full[t]), q_issued & 1);
 }
 
 // ----------------------------------------------------------------------- MMA
@@ -883,8 +902,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         correction_role<D, CAUSAL, DT, PV8>(p, ctl, tmem, warp, lane);
     } else {
         setmaxnreg_dec<80>();
-        if (warp == 12) producer_role<D, CAUSAL, DT, PV8>(p, ctl, &tm_q, &tm_k, &tm_v, &tm_vt8, sQ0, sKV);
+        if (warp == 12) producer_role<D, CAUSAL, DT, PV8>(p, ctl, &tm_k, &tm_v, &tm_vt8, sKV);
         if (warp == 13) mma_role<D, CAUSAL, DT, PV8>(p, ctl, tmem, sQ0, sKV);
+        if (warp == 14) q_producer_role<D, CAUSAL, DT, PV8>(p, ctl, &tm_q, sQ0);
     }
 
     tc_fence_before();
