@@ -505,6 +505,12 @@ def main():
             chunked[{"auto": "certified", "online": "online", "fp8": "certified_fp8_pv"}[variant]] = {
                 "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms": ms}
         chunked["certified_speedup_vs_online"] = chunked["online"]["ms"] / chunked["certified"]["ms"]
+        if fp8_chunks:
+            # (head, chunk) pairs on E4M3: eligible certified heads, chunks of 4096 keys or more.
+            n_elig = sum(1 for c in clis.decode_certs(certs)
+                         if c["certified"] and c["B_h"] <= min(8, c["C"]) and c["G"] <= 8)
+            n_big = sum(1 for a, b in zip(bounds[:-1], bounds[1:]) if b - a >= 4096)
+            chunked["certified_fp8_pv"]["fp8_head_chunks"] = f"{n_elig * n_big}/{heads * n_chunks}"
         line["chunked"] = chunked
         del o_acc, l_acc, m_acc, vt8s
     if extras in ("all", "backward"):
