@@ -194,8 +194,13 @@ def test_random_fp8pv_matches_rounding_model(seed):
         # that fp32 order tips the other way: two such per row, plus 1e-4 for the rest
         # (with thousands of keys a flip moves an output by 1e-4 or less; with 129
         # keys by up to ~2e-3).
+        # With a handful of keys a weight is of order one, so one flipped decision moves
+        # every output of its row by up to `flip` and the head's mean cannot average it
+        # away: there the mean may also carry up to four flipped rows.
         e, _, flip = rm.certified_forward_fp8pv(qf[h], kf[h], vf[h], w.softmax_scale(), with_flip_bound=True)
         sc = max(1.0, np.abs(e).max())
         excess = np.maximum(np.abs(got[h] - e) - np.abs(e) * 2.0 ** -8, 0.0).max() / sc
         mean = np.abs(got[h] - rm.bf16(e)).mean() / sc
-        assert excess <= 2 * flip / sc + 1e-4 and mean <= 1e-5, (seed, h, Nq, Nk, strided, excess, flip / sc, mean)
+        mean_bound = 1e-5 + (4 * flip / (sc * Nq) if Nk < 16 else 0.0)
+        assert excess <= 2 * flip / sc + 1e-4 and mean <= mean_bound, (seed, h, Nq, Nk, strided, excess,
+                                                                         flip / sc, mean)
