@@ -470,6 +470,35 @@ def _exp_fmt(q) -> str:
     return "fp16" if q.dtype == torch.float16 else "bf16"
 
 
+def grouped_query_views(q, k, v, out=None):
+    """Views for grouped-query / multi-query attention: q [B, H, Nq, d] and k, v
+    [B, H_kv, Nk, d] with H a multiple of H_kv (query head h uses key/value head
+    h // (H / H_kv)).  Returns (q', k', v', out') of shape [B * H_kv, H / H_kv, N, d]
+    over the same memory: the key/value heads are folded into the batch and K, V
+    get head stride 0, so every query head of a group reads its group's keys and
+    values (no copy).  The certificate of folded head (b', j) sits at index
+    b' * (H / H_kv) + j = b * H + h, as without folding."""
+    B, H, Nq, d = q.shape
+    Hkv = k.shape[1]
+    if v.shape[1] != Hkv or H % Hkv:
+        raise ValueError("k and v need the same number of heads, dividing q's")
+    g = H // Hkv
+    views = []
+    for t, heads, bcast in ((q, H, False), (k, Hkv, True), (v, Hkv, True), (out, H, False)):
+        if t is None:
+            views.append(None)
+            continue
+        sb, sh, sn, sd = t.stride()
+        if sb != heads * sh and t.shape[0] > 1:
+            raise ValueError("the batch stride must span the heads (sb == H * sh) to fold them")
+        n = t.shape[2]
+        if bcast:
+            views.append(t.as_strided((B * Hkv, g, n, d), (sh, 0, sn, sd)))
+        else:
+            views.append(t.as_strided((B * Hkv, g, n, d), (g * sh, sh, sn, sd)))
+    return tuple(views)
+
+
 def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
               variant: str = "auto", return_certs: bool = False, device=None, out=None,
               groups: int = 8, non_blocking: bool = False, pv: str = "bf16"):
@@ -495,9 +524,21 @@ def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
     "certified") runs the FP8 P.V path: V's E4M3 transpose, then
     clis_attn_fwd_fp8pv, where heads within the E4M3 budget multiply P and V
     in E4M3 and every other head runs as with ``pv="bf16"``.
+
+    k and v may have fewer heads than q (grouped-query or multi-query
+    attention, device tensors): see :func:`grouped_query_views`; the output
+    has q's shape.
     """
     if pv not in ("bf16", "fp8"):
         raise ValueError(f"pv must be 'bf16' or 'fp8', not {pv!r}")
+    if k.shape[1] != q.shape[1]:
+        if q.device.type == "cpu":
+            raise ValueError("grouped key/value heads take device tensors")
+        if out is None:
+            out = torch.empty_like(q, memory_format=torch.contiguous_format)
+        qf, kf, vf, of = grouped_query_views(q, k, v, out)
+        res = attention(qf, kf, vf, softmax_scale, causal, variant, return_certs, out=of, pv=pv)
+        return (out,) + tuple(res[1:]) if return_certs else out
     if pv == "fp8":
         if q.device.type == "cpu" or causal or variant not in ("auto", "certified"):
             raise ValueError("pv='fp8' takes device tensors, no mask and variant 'auto' or 'certified'")

@@ -22,6 +22,14 @@ clis_status_t check_strides(int64_t sb, int64_t sh, int64_t sn, int64_t d)
     return CLIS_OK;
 }
 
+// Strides of a written tensor must give every (b, h) its own elements: a zero
+// head (batch) stride with more than one head (batch) would make them share
+// (a tensor of N = 0 rows has no elements to share).
+bool aliasing(int64_t B, int64_t H, int64_t N, int64_t sb, int64_t sh)
+{
+    return N > 0 && ((H > 1 && sh == 0) || (B > 1 && sb == 0));
+}
+
 clis_status_t check_shape(const clis_shape_t *s, bool with_o)
 {
     if (!s) return CLIS_ERR_INVALID_ARG;
@@ -35,6 +43,7 @@ clis_status_t check_shape(const clis_shape_t *s, bool with_o)
     if ((st = check_strides(s->k_sb, s->k_sh, s->k_sn, s->d)) != CLIS_OK) return st;
     if ((st = check_strides(s->v_sb, s->v_sh, s->v_sn, s->d)) != CLIS_OK) return st;
     if (with_o && (st = check_strides(s->o_sb, s->o_sh, s->o_sn, s->d)) != CLIS_OK) return st;
+    if (with_o && aliasing(s->B, s->H, s->Nq, s->o_sb, s->o_sh)) return CLIS_ERR_INVALID_ARG;
     return CLIS_OK;
 }
 
@@ -437,6 +446,7 @@ clis_status_t clis_attn_chunk_finalize(const clis_shape_t *shape, const float *o
     if (!o_acc || !l_acc || !m_acc || !o) return CLIS_ERR_INVALID_ARG;
     clis_status_t st = check_strides(shape->o_sb, shape->o_sh, shape->o_sn, shape->d);
     if (st != CLIS_OK) return st;
+    if (aliasing(shape->B, shape->H, shape->Nq, shape->o_sb, shape->o_sh)) return CLIS_ERR_INVALID_ARG;
     if (!aligned16(o_acc) || !aligned16(o) || (reinterpret_cast<uintptr_t>(l_acc) & 3u) ||
         (reinterpret_cast<uintptr_t>(m_acc) & 3u) || (lse2 && (reinterpret_cast<uintptr_t>(lse2) & 3u)))
         return CLIS_ERR_MISALIGNED;
@@ -487,6 +497,11 @@ clis_status_t clis_attn_bwd(const clis_shape_t *shape, const void *q, const void
 {
     clis_status_t st = check_shape(shape, true);
     if (st != CLIS_OK) return st;
+    // dQ, dK and dV are written with the Q, K and V strides.
+    if (aliasing(shape->B, shape->H, shape->Nq, shape->q_sb, shape->q_sh) ||
+        aliasing(shape->B, shape->H, shape->Nk, shape->k_sb, shape->k_sh) ||
+        aliasing(shape->B, shape->H, shape->Nk, shape->v_sb, shape->v_sh))
+        return CLIS_ERR_INVALID_ARG;
     if (shape->B * shape->H == 0) return CLIS_OK;
     if (!std::isfinite(scale_log2) || !(scale_log2 > 0.f)) return CLIS_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return CLIS_ERR_INVALID_ARG;

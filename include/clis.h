@@ -93,7 +93,19 @@ typedef enum { CLIS_DT_BF16 = 0, CLIS_DT_FP16 = 1 } clis_dtype_t;
 
 /* Problem shape and element strides (elements, not bytes).  K and V share
  * Nk; Q and O share Nq.  O strides are ignored by clis_certify.  dtype is a
- * clis_dtype_t (0 = BF16, the zero-initialised default). */
+ * clis_dtype_t (0 = BF16, the zero-initialised default).
+ *
+ * Strides are non-negative, n-strides at least d.  A head or batch stride of
+ * 0 on K and V makes the heads (or batches) read one K/V head: grouped-query
+ * and multi-query attention map onto it by folding the key/value heads into
+ * the batch (B' = B * H_kv, H' = query heads per key/value head, K and V
+ * head stride 0, batch stride one K/V head).  Each query head is then
+ * certified against the shared keys and values like any other head.  Strides
+ * of anything written must not make two elements share an address: an O (or,
+ * in the backward, dQ, dK, dV) head stride of 0 with H > 1 or batch stride of
+ * 0 with B > 1 is CLIS_ERR_INVALID_ARG -- so the backward, which writes dK and
+ * dV with the K and V strides, takes no broadcast K/V (sum the gradients of a
+ * group from a repeated layout instead). */
 typedef struct {
     int64_t B, H, Nq, Nk, d;
     int64_t q_sb, q_sh, q_sn;

@@ -152,6 +152,40 @@ def test_attn_rejects_bad_arguments(clis):
     assert _attn(clis, s) == MIS
 
 
+def test_written_tensors_must_not_alias(clis):
+    """A zero head or batch stride may broadcast K and V (grouped-query
+    attention) but never an output: O in the forward and the chunk finalize,
+    dQ/dK/dV (written with the Q/K/V strides) in the backward."""
+    INV = 1
+    s = _shape(clis)
+    s.o_sh = 0
+    assert _attn(clis, s) == INV
+    s = _shape(clis, B=2, H=1)
+    s.o_sb = 0
+    assert _attn(clis, s) == INV
+    lib = clis.load_library()
+    vp = ctypes.c_void_p
+    s = _shape(clis)
+    s.o_sh = 0
+    assert lib.clis_attn_chunk_finalize(ctypes.byref(s), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, None) == INV
+    for t in "qkv":
+        s = _shape(clis)
+        setattr(s, f"{t}_sh", 0)
+        assert _bwd(clis, s) == INV, t
+
+
+def test_broadcast_kv_passes_the_forward_checks(clis):
+    """K and V with head stride 0 (the grouped-query fold) pass the shape and
+    stride checks, which come first: the calls below get as far as the
+    deliberately misaligned pointer."""
+    MIS = 3
+    s = _shape(clis)
+    s.k_sh = s.v_sh = 0
+    assert _attn(clis, s, o=FAKE + 2) == MIS
+    assert _certify(clis, s, k=FAKE + 8) == MIS
+    assert clis.clis_certify_workspace_size(s) > 0
+
+
 def test_chunk_entry_points_reject_bad_arguments(clis):
     lib = clis.load_library()
     vp = ctypes.c_void_p

@@ -1,0 +1,106 @@
+"""Grouped-query and multi-query attention through broadcast K/V strides.
+
+The query heads of a group share one key/value head: the key/value heads are
+folded into the batch and K, V get head stride 0 (clis.grouped_query_views, no
+copy).  Checks, against the oracle on the same keys and values repeated per
+query head: the certificates (flags and the integers G, A, C bit-exact), the
+forward output and lse2; and bit-identity with the same call on a materialised
+repeated K/V (the kernels read the same values through the broadcast map).
+The backward rejects broadcast K/V (dK and dV would alias).
+"""
+import dataclasses
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from certified_fixed_stabilizer_gb300 import clis
+from certified_fixed_stabilizer_gb300.workloads import WORKLOADS, make_inputs
+from gpu_util import assert_close_to_oracle, flat, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    need_gpu()
+    oracle.set_num_threads(os.cpu_count() or 1)
+    clis.clis_clear_device_error()
+    yield
+
+
+@pytest.fixture(autouse=True)
+def _device_error_word_stays_clear():
+    yield
+    code = clis.clis_get_device_error()
+    clis.clis_clear_device_error()
+    assert code == 0, f"device error word {code:#x}"
+
+
+CASES = [  # B, H (query heads), H_kv, N, d, causal
+    (2, 8, 2, 1000, 128, False),
+    (2, 8, 2, 1000, 128, True),
+    (1, 8, 1, 777, 64, False),      # multi-query
+    (3, 6, 3, 513, 128, True),
+]
+
+
+def _inputs(B, H, Hkv, N, d, causal, seed):
+    dev = need_gpu()
+    w = dataclasses.replace(WORKLOADS["causal" if causal else "480p"], B=B, d=d)
+    q, _, _ = make_inputs(w, device=dev, N=N, H=H, seed=seed)
+    _, k, v = make_inputs(w, device=dev, N=N, H=Hkv, seed=seed + 1)
+    return q, k, v
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,causal", CASES)
+def test_grouped_query_forward_matches_oracle(B, H, Hkv, N, d, causal):
+    q, k, v = _inputs(B, H, Hkv, N, d, causal, seed=40 + H + N)
+    g = H // Hkv
+    o, kbar, certs = clis.attention(q, k, v, causal=causal, return_certs=True)
+    torch.cuda.synchronize()
+    assert o.shape == q.shape
+    krep, vrep = (t.repeat_interleave(g, dim=1) for t in (k, v))  # [B, H, N, d]: head h uses h // g
+    ref, _ = oracle.attention(flat(q).cpu(), flat(krep).cpu(), flat(vrep).cpu(), d ** -0.5, causal=causal,
+                              with_lse2=True)
+    what = f"GQA B={B} H={H} H_kv={Hkv} N={N} d={d} causal={causal}"
+    assert_close_to_oracle(flat(o).float().cpu().numpy(), ref, what)
+    sl2 = clis.scale_log2_for(d)
+    _, ocerts = oracle.certify(q.cpu(), krep.cpu(), vrep.cpu(), sl2)
+    for hd, (gc, oc) in enumerate(zip(clis.decode_certs(certs), ocerts)):
+        if not oc["band"]:
+            for key in ("certified", "G", "A", "C", "reason"):
+                assert gc[key] == oc[key], (what, hd, key, gc, oc)
+    # The same call on materialised repeated K/V gives the same bits.
+    o2, _, certs2 = clis.attention(q, krep.contiguous(), vrep.contiguous(), causal=causal, return_certs=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2), what
+    assert torch.equal(certs, certs2), what
+
+
+def test_grouped_query_lse2_and_views():
+    B, H, Hkv, N, d = 2, 8, 2, 640, 128
+    q, k, v = _inputs(B, H, Hkv, N, d, False, seed=77)
+    qf, kf, vf, _ = clis.grouped_query_views(q, k, v)
+    assert qf.shape == (B * Hkv, H // Hkv, N, d) and kf.stride(1) == 0 and vf.stride(1) == 0
+    assert qf.data_ptr() == q.data_ptr() and kf.data_ptr() == k.data_ptr()
+    sl2 = clis.scale_log2_for(d)
+    lse2 = torch.empty(B * H * N, device=q.device)
+    kbar, certs = clis.clis_certify(qf, kf, vf, sl2)
+    o = clis.clis_attn_fwd(qf, kf, vf, sl2, kbar=kbar, certs=certs, lse2=lse2)
+    torch.cuda.synchronize()
+    krep, vrep = (t.repeat_interleave(H // Hkv, dim=1) for t in (k, v))
+    ref, rlse = oracle.attention(flat(q).cpu(), flat(krep).cpu(), flat(vrep).cpu(), d ** -0.5, with_lse2=True)
+    assert_close_to_oracle(o.reshape(B * H, N, d).float().cpu().numpy(), ref, "GQA views")
+    np.testing.assert_allclose(lse2.reshape(B * H, N).cpu().numpy(), rlse, atol=2e-3, rtol=0)
+
+
+def test_backward_rejects_broadcast_kv():
+    B, H, Hkv, N, d = 1, 4, 1, 256, 128
+    q, k, v = _inputs(B, H, Hkv, N, d, False, seed=3)
+    qf, kf, vf, _ = clis.grouped_query_views(q, k, v)
+    o, lse2 = clis.attention_fwd_lse(qf, kf, vf)
+    with pytest.raises(clis.ClisError, match="INVALID_ARG"):
+        clis.attention_bwd(qf, kf, vf, o, torch.randn_like(o), lse2)
