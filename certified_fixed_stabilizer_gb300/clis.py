@@ -382,22 +382,45 @@ def clis_attn_bwd(q, k, v, o, dout, lse2, scale_log2: float, causal: bool = Fals
     return dq, dk, dv
 
 
-def attention_fwd_lse(q, k, v, softmax_scale: float | None = None, causal: bool = False, variant: str = "auto"):
+def attention_fwd_lse(q, k, v, softmax_scale: float | None = None, causal: bool = False, variant: str = "auto",
+                      out=None):
     """Forward that also returns the row statistic the backward needs:
-    (o, lse2), lse2 fp32 [B*H*Nq]."""
+    (o, lse2), lse2 fp32 [B*H*Nq].  k, v may have fewer heads than q
+    (grouped-query attention, see :func:`grouped_query_views`)."""
+    if k.shape[1] != q.shape[1]:
+        o = torch.empty_like(q, memory_format=torch.contiguous_format) if out is None else out
+        qf, kf, vf, of = grouped_query_views(q, k, v, o)
+        _, lse2 = attention_fwd_lse(qf, kf, vf, softmax_scale, causal, variant, out=of)
+        return o, lse2
     sl2 = scale_log2_for(q.shape[-1], softmax_scale)
     lse2 = torch.empty(q.shape[0] * q.shape[1] * q.shape[2], dtype=torch.float32, device=q.device)
     kbar = certs = mu = None
     if variant in ("auto", "certified"):
         mu = torch.empty_like(lse2)
         kbar, certs = clis_certify(q, k, v, sl2, mu=mu, exp_fmt=_exp_fmt(q))
-    o = clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=causal, variant=variant, mu=mu, lse2=lse2)
+    o = clis_attn_fwd(q, k, v, sl2, kbar=kbar, certs=certs, causal=causal, variant=variant, mu=mu, lse2=lse2,
+                      out=out)
     return o, lse2
 
 
 def attention_bwd(q, k, v, o, dout, lse2, softmax_scale: float | None = None, causal: bool = False):
-    """(dq, dk, dv) for the attention whose forward gave (o, lse2)."""
-    return clis_attn_bwd(q, k, v, o, dout, lse2, scale_log2_for(q.shape[-1], softmax_scale), causal=causal)
+    """(dq, dk, dv) for the attention whose forward gave (o, lse2).  With k, v
+    of fewer heads than q (grouped-query attention) dk and dv have k's and v's
+    shape: each holds the sum over its group's query heads, accumulated in the
+    kernel (K and V pass as broadcast views, dK and dV as broadcast views of
+    tensors shaped like k and v)."""
+    sl2 = scale_log2_for(q.shape[-1], softmax_scale)
+    if k.shape[1] == q.shape[1]:
+        return clis_attn_bwd(q, k, v, o, dout, lse2, sl2, causal=causal)
+    if dout.stride() != o.stride():
+        dout = torch.empty_strided(o.shape, o.stride(), dtype=o.dtype, device=o.device).copy_(dout)
+    dq = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+    dk = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)
+    dv = torch.empty_strided(v.shape, v.stride(), dtype=v.dtype, device=v.device)
+    qf, kf, vf, of = grouped_query_views(q, k, v, o)
+    dqf, dkf, dvf, dof = grouped_query_views(dq, dk, dv, dout)
+    clis_attn_bwd(qf, kf, vf, of, dof, lse2, sl2, causal=causal, dq=dqf, dk=dkf, dv=dvf)
+    return dq, dk, dv
 
 
 class AttentionFunction(torch.autograd.Function):

@@ -91,6 +91,11 @@ struct BParams {
     int64_t q_sb, q_sh, q_sn, k_sb, k_sh, k_sn, v_sb, v_sh, v_sn;
     int B, H, Nq, Nk;
     int nqb, nkb;    // 128-row query / key blocks per head
+    // dK/dV kernel: query heads per key/value head.  1, or H when K and V are
+    // broadcast over the heads (head stride 0: grouped-query attention folded
+    // into the batch), in which case a work tile sums the gradients of every
+    // query head of its batch entry.
+    int kvg;
     int grp;         // causal: heads per scheduling group
     int num_tiles;
     float scale_log2;
@@ -116,20 +121,25 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
 // one group of heads stays in L2.  Non-causal: head-major.
 struct KTile {
     int bh, b, h, kb, q0, nq;  // key block kb meets query blocks q0 .. q0 + nq - 1
+    int hq0, nh;               // ... of query heads hq0 .. hq0 + nh - 1: steps nh * nq
 };
 
+// A dK/dV work tile is one key block of one key/value head (bh over the
+// B * H / kvg key/value heads); its steps run over the query blocks of each of
+// the head's kvg query heads in turn.
 template <bool CAUSAL>
 __device__ __forceinline__ KTile decode_ktile(const BParams &p, int tile)
 {
     KTile t;
+    const int kv_heads = p.B * p.H / p.kvg;
     if (CAUSAL) {
         const int per_grp = p.grp * p.nkb;
         const int gi = tile / per_grp;
         const int r = tile % per_grp;
-        const int heads = min(p.grp, p.B * p.H - gi * p.grp);
+        const int heads = min(p.grp, kv_heads - gi * p.grp);
         const int ki = r / heads;
         t.bh = gi * p.grp + r % heads;
-        t.kb = (gi & 1) ? (p.nkb - 1 - ki) : ki;  // key block kb costs nqb - kb steps
+        t.kb = (gi & 1) ? (p.nkb - 1 - ki) : ki;  // key block kb costs nqb - kb steps per query head
         t.q0 = t.kb;                               // queries before the block see none of its keys
         t.nq = p.nqb - t.kb;
     } else {
@@ -138,8 +148,11 @@ __device__ __forceinline__ KTile decode_ktile(const BParams &p, int tile)
         t.q0 = 0;
         t.nq = p.nqb;
     }
-    t.b = t.bh / p.H;
-    t.h = t.bh % p.H;
+    const int hkv = p.H / p.kvg;  // key/value heads per batch entry
+    t.b = t.bh / hkv;
+    t.h = t.bh % hkv;             // key/value head coordinate (0 when broadcast)
+    t.hq0 = t.h * p.kvg;
+    t.nh = p.kvg;
     return t;
 }
 
@@ -272,9 +285,10 @@ __device__ void kv_producer(const BParams &p, KCtl<D> &c, const CUtensorMap *tm_
         }
         __syncwarp();
         kv_issued = w;
-        for (int i = 0; i < T.nq; i++) {
+        for (int i = 0; i < T.nh * T.nq; i++) {
             const uint32_t n = nq;  // global step index
-            const int qb = T.q0 + i;
+            const int hq = T.hq0 + i / T.nq;  // query head and block of this step
+            const int qb = T.q0 + i % T.nq;
             // Q_n and dO_n are signalled together on Q_n's full barrier: the MMA warp
             // waits once per step (before S^T_n), and dO_n has landed for dP^T_n.
             const uint32_t qs = n % C::QRING;
@@ -288,9 +302,9 @@ __device__ void kv_producer(const BParams &p, KCtl<D> &c, const CUtensorMap *tm_
                 mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES);
 #pragma unroll
                 for (int bx = 0; bx < C::NBOX; bx++) {
-                    tma_load_4d_hint(sQ + qs * C::TILE_BYTES + bx * C::BOX_BYTES, tm_q, bar, bx * 64, qb * BN, T.h,
+                    tma_load_4d_hint(sQ + qs * C::TILE_BYTES + bx * C::BOX_BYTES, tm_q, bar, bx * 64, qb * BN, hq,
                                      T.b, pol_keep);
-                    tma_load_4d_hint(sO + os * C::TILE_BYTES + bx * C::BOX_BYTES, tm_do, bar, bx * 64, qb * BN, T.h,
+                    tma_load_4d_hint(sO + os * C::TILE_BYTES + bx * C::BOX_BYTES, tm_do, bar, bx * 64, qb * BN, hq,
                                      T.b, pol_keep);
                 }
             }
@@ -302,7 +316,7 @@ __device__ void kv_producer(const BParams &p, KCtl<D> &c, const CUtensorMap *tm_
             const uint32_t ls = n % C::LSLOT;
             if (!mbar_wait_warp(smem_u32(&c.ls_empty[ls]), ((n / C::LSLOT) & 1) ^ 1, ab, err, kErrProducer))
                 goto abort;
-            const int64_t rbase = static_cast<int64_t>(T.bh) * p.Nq;
+            const int64_t rbase = (static_cast<int64_t>(T.b) * p.H + hq) * p.Nq;
 #pragma unroll
             for (int r = lane; r < BN; r += 32) {
                 const int row = qb * BN + r;
@@ -358,11 +372,12 @@ __device__ void kv_mma(const BParams &p, KCtl<D> &c, uint32_t tmem, uint32_t sK,
         __syncwarp();
         if (leader) {
             issue_dp(n);  // dO_n landed with Q_n
-            if (T.nq == 1) umma_commit(smem_u32(&c.kv_empty));
+            if (T.nh * T.nq == 1) umma_commit(smem_u32(&c.kv_empty));
         }
         __syncwarp();
-        for (int i = 0; i < T.nq; i++, n++) {
-            const bool has_next = i + 1 < T.nq;
+        const int ns = T.nh * T.nq;  // steps of the tile
+        for (int i = 0; i < ns; i++, n++) {
+            const bool has_next = i + 1 < ns;
             const uint32_t nx = n + 1;
             // The previous tile's epilogue must have read dV and dK before they restart.
             if (i == 0 && w > 0)
@@ -406,7 +421,7 @@ __device__ void kv_mma(const BParams &p, KCtl<D> &c, uint32_t tmem, uint32_t sK,
                 // (dO_{n+1} landed with Q_{n+1}).
                 if (leader) {
                     issue_dp(nx);
-                    if (i + 2 == T.nq) umma_commit(smem_u32(&c.kv_empty));
+                    if (i + 2 == ns) umma_commit(smem_u32(&c.kv_empty));
                 }
                 __syncwarp();
             }
@@ -438,10 +453,10 @@ __device__ void kv_softmax(const BParams &p, KCtl<D> &c, uint32_t tmem, int warp
     int w = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
         const KTile T = decode_ktile<CAUSAL>(p, tile);
-        for (int i = 0; i < T.nq; i++, n++) {
+        for (int i = 0; i < T.nh * T.nq; i++, n++) {
             const uint32_t s = n % C::LSLOT;
             // The diagonal block: query column c sees this key only if c >= rl.
-            const bool diag = CAUSAL && (T.q0 + i == T.kb);
+            const bool diag = CAUSAL && (T.q0 + i % T.nq == T.kb);
             if (!mbar_wait(smem_u32(&c.s_full), n & 1, ab, err, kErrSoftmax)) return;
             // -lse2 and -D of this step's query block, staged by the producer warp.
             if (!mbar_wait(smem_u32(&c.ls_full[s]), (n / C::LSLOT) & 1, ab, err, kErrSoftmax)) return;
@@ -1024,11 +1039,15 @@ clis_status_t launch_impl(const AttnBwdArgs &a, cudaStream_t stream)
     p.scale_log2 = a.scale_log2;
     p.scale = a.scale_log2 * 0.693147180559945309f;
     const int BH = a.B * a.H;
+    // K and V broadcast over the heads (head stride 0): one key/value head per
+    // batch entry, shared by all H query heads.
+    p.kvg = (a.H > 1 && a.k_sh == 0 && a.v_sh == 0) ? a.H : 1;
+    const int KVH = BH / p.kvg;
 
-    // dK, dV: one work tile per (head, key block).
-    p.num_tiles = BH * p.nkb;
+    // dK, dV: one work tile per (key/value head, key block).
+    p.num_tiles = KVH * p.nkb;
     p.grp = (2 * nsm + p.nkb - 1) / p.nkb;
-    p.grp = p.grp > BH ? BH : (p.grp < 1 ? 1 : p.grp);
+    p.grp = p.grp > KVH ? KVH : (p.grp < 1 ? 1 : p.grp);
     int grid = p.num_tiles < nsm ? p.num_tiles : nsm;
     p.smem_bytes = kv_smem;
     bwd_dkdv_kernel<D, CAUSAL, DT><<<grid, kThreads, kv_smem, stream>>>(mq, mk, mv, mdo, p);

@@ -497,10 +497,14 @@ clis_status_t clis_attn_bwd(const clis_shape_t *shape, const void *q, const void
 {
     clis_status_t st = check_shape(shape, true);
     if (st != CLIS_OK) return st;
-    // dQ, dK and dV are written with the Q, K and V strides.
+    // dQ, dK and dV are written with the Q, K and V strides.  K and V broadcast
+    // over the heads together (both head strides 0: grouped-query attention
+    // folded into the batch) are the one sharing allowed: the kernel then sums
+    // the group's gradients and writes each dK, dV row once.
+    const bool kv_bcast = shape->H > 1 && shape->k_sh == 0 && shape->v_sh == 0;
     if (aliasing(shape->B, shape->H, shape->Nq, shape->q_sb, shape->q_sh) ||
-        aliasing(shape->B, shape->H, shape->Nk, shape->k_sb, shape->k_sh) ||
-        aliasing(shape->B, shape->H, shape->Nk, shape->v_sb, shape->v_sh))
+        aliasing(shape->B, kv_bcast ? 1 : shape->H, shape->Nk, shape->k_sb, shape->k_sh) ||
+        aliasing(shape->B, kv_bcast ? 1 : shape->H, shape->Nk, shape->v_sb, shape->v_sh))
         return CLIS_ERR_INVALID_ARG;
     if (shape->B * shape->H == 0) return CLIS_OK;
     if (!std::isfinite(scale_log2) || !(scale_log2 > 0.f)) return CLIS_ERR_INVALID_ARG;

@@ -103,9 +103,10 @@ typedef enum { CLIS_DT_BF16 = 0, CLIS_DT_FP16 = 1 } clis_dtype_t;
  * certified against the shared keys and values like any other head.  Strides
  * of anything written must not make two elements share an address: an O (or,
  * in the backward, dQ, dK, dV) head stride of 0 with H > 1 or batch stride of
- * 0 with B > 1 is CLIS_ERR_INVALID_ARG -- so the backward, which writes dK and
- * dV with the K and V strides, takes no broadcast K/V (sum the gradients of a
- * group from a repeated layout instead). */
+ * 0 with B > 1 is CLIS_ERR_INVALID_ARG, with one exception: the backward
+ * writes dK and dV with the K and V strides, and when K and V are broadcast
+ * over the heads together (both head strides 0) it sums the gradients of all
+ * H query heads into each dK and dV row and writes it once. */
 typedef struct {
     int64_t B, H, Nq, Nk, d;
     int64_t q_sb, q_sh, q_sn;

@@ -155,7 +155,9 @@ def test_attn_rejects_bad_arguments(clis):
 def test_written_tensors_must_not_alias(clis):
     """A zero head or batch stride may broadcast K and V (grouped-query
     attention) but never an output: O in the forward and the chunk finalize,
-    dQ/dK/dV (written with the Q/K/V strides) in the backward."""
+    dQ/dK/dV (written with the Q/K/V strides) in the backward -- except dK and
+    dV when K and V are broadcast over the heads together, where the kernel
+    sums each group and writes every row once."""
     INV = 1
     s = _shape(clis)
     s.o_sh = 0
@@ -168,10 +170,16 @@ def test_written_tensors_must_not_alias(clis):
     s = _shape(clis)
     s.o_sh = 0
     assert lib.clis_attn_chunk_finalize(ctypes.byref(s), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, None) == INV
-    for t in "qkv":
+    for t in "qkv":  # one of Q, K, V alone with head stride 0: its gradient rows would alias
         s = _shape(clis)
         setattr(s, f"{t}_sh", 0)
         assert _bwd(clis, s) == INV, t
+    s = _shape(clis, B=2)  # K and V broadcast over the batch
+    s.k_sb = s.v_sb = 0
+    assert _bwd(clis, s) == INV
+    s = _shape(clis)       # K and V broadcast over the heads together: grouped-query, allowed
+    s.k_sh = s.v_sh = 0
+    assert _bwd(clis, s, dq=FAKE + 8) == 3
 
 
 def test_broadcast_kv_passes_the_forward_checks(clis):
