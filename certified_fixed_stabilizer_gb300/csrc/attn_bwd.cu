@@ -126,12 +126,14 @@ struct KTile {
 
 // A dK/dV work tile is one key block of one key/value head (bh over the
 // B * H / kvg key/value heads); its steps run over the query blocks of each of
-// the head's kvg query heads in turn.
-template <bool CAUSAL>
+// the head's kvg query heads in turn.  G: kernels built for grouped heads
+// (kvg > 1); otherwise kvg is 1 at compile time.
+template <bool CAUSAL, bool G>
 __device__ __forceinline__ KTile decode_ktile(const BParams &p, int tile)
 {
     KTile t;
-    const int kv_heads = p.B * p.H / p.kvg;
+    const int kvg = G ? p.kvg : 1;
+    const int kv_heads = p.B * p.H / kvg;
     if (CAUSAL) {
         const int per_grp = p.grp * p.nkb;
         const int gi = tile / per_grp;
@@ -148,11 +150,11 @@ __device__ __forceinline__ KTile decode_ktile(const BParams &p, int tile)
         t.q0 = 0;
         t.nq = p.nqb;
     }
-    const int hkv = p.H / p.kvg;  // key/value heads per batch entry
+    const int hkv = p.H / kvg;  // key/value heads per batch entry
     t.b = t.bh / hkv;
-    t.h = t.bh % hkv;             // key/value head coordinate (0 when broadcast)
-    t.hq0 = t.h * p.kvg;
-    t.nh = p.kvg;
+    t.h = t.bh % hkv;           // key/value head coordinate (0 when broadcast)
+    t.hq0 = t.h * kvg;
+    t.nh = kvg;
     return t;
 }
 
@@ -258,7 +260,7 @@ struct __align__(16) KCtl {
 };
 
 
-template <int D, bool CAUSAL, int DT>
+template <int D, bool CAUSAL, int DT, bool G>
 __device__ void kv_producer(const BParams &p, KCtl<D> &c, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                             const CUtensorMap *tm_v, const CUtensorMap *tm_do, uint32_t sK, uint32_t sV,
                             uint32_t sQ, uint32_t sO, int lane)
@@ -272,7 +274,7 @@ __device__ void kv_producer(const BParams &p, KCtl<D> &c, const CUtensorMap *tm_
     uint32_t nq = 0, no = 0;  // Q and dO tiles issued (one of each per step)
     int w = 0, kv_issued = -1;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
-        const KTile T = decode_ktile<CAUSAL>(p, tile);
+        const KTile T = decode_ktile<CAUSAL, G>(p, tile);
         if (!mbar_wait_warp(smem_u32(&c.kv_empty), (w & 1) ^ 1, ab, err, kErrProducer)) goto abort;
         if (leader) {
             const uint32_t bar = smem_u32(&c.kv_full);
@@ -285,10 +287,11 @@ __device__ void kv_producer(const BParams &p, KCtl<D> &c, const CUtensorMap *tm_
         }
         __syncwarp();
         kv_issued = w;
-        for (int i = 0; i < T.nh * T.nq; i++) {
+        // Steps: the query blocks of each query head of the tile in turn.
+        for (int hg = T.hq0, qi = 0, i = 0; i < T.nh * T.nq; i++) {
             const uint32_t n = nq;  // global step index
-            const int hq = T.hq0 + i / T.nq;  // query head and block of this step
-            const int qb = T.q0 + i % T.nq;
+            const int hq = G ? hg : T.h;
+            const int qb = T.q0 + (G ? qi : i);
             // Q_n and dO_n are signalled together on Q_n's full barrier: the MMA warp
             // waits once per step (before S^T_n), and dO_n has landed for dP^T_n.
             const uint32_t qs = n % C::QRING;
@@ -327,6 +330,10 @@ __device__ void kv_producer(const BParams &p, KCtl<D> &c, const CUtensorMap *tm_
             __syncwarp();
             if (leader) mbar_arrive(smem_u32(&c.ls_full[ls]));
             __syncwarp();
+            if (++qi == T.nq) {
+                qi = 0;
+                ++hg;
+            }
         }
     }
     return;
@@ -336,7 +343,7 @@ abort:
     if (kv_issued >= 0) drain_wait(smem_u32(&c.kv_full), kv_issued & 1);
 }
 
-template <int D, bool CAUSAL, int DT>
+template <int D, bool CAUSAL, int DT, bool G>
 __device__ void kv_mma(const BParams &p, KCtl<D> &c, uint32_t tmem, uint32_t sK, uint32_t sV, uint32_t sQ,
                        uint32_t sO)
 {
@@ -363,7 +370,7 @@ __device__ void kv_mma(const BParams &p, KCtl<D> &c, uint32_t tmem, uint32_t sK,
     uint32_t n = 0;
     int w = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
-        const KTile T = decode_ktile<CAUSAL>(p, tile);
+        const KTile T = decode_ktile<CAUSAL, G>(p, tile);
         if (!mbar_wait_warp(smem_u32(&c.kv_full), w & 1, ab, err, kErrMma)) goto abort;
         // First step of the tile: S^T and dP^T.
         if (!mbar_wait_warp(smem_u32(&c.q_full[n % C::QRING]), (n / C::QRING) & 1, ab, err, kErrMma)) goto abort;
@@ -434,7 +441,7 @@ abort:
     drain_wait(smem_u32(&c.drain), 0);
 }
 
-template <int D, bool CAUSAL, int DT>
+template <int D, bool CAUSAL, int DT, bool G>
 __device__ void kv_softmax(const BParams &p, KCtl<D> &c, uint32_t tmem, int warp, int lane)
 {
     using C = BCfg<D>;
@@ -452,11 +459,11 @@ __device__ void kv_softmax(const BParams &p, KCtl<D> &c, uint32_t tmem, int warp
     uint32_t n = 0;
     int w = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++w) {
-        const KTile T = decode_ktile<CAUSAL>(p, tile);
-        for (int i = 0; i < T.nh * T.nq; i++, n++) {
+        const KTile T = decode_ktile<CAUSAL, G>(p, tile);
+        for (int i = 0, qi = 0; i < T.nh * T.nq; i++, n++, qi = (qi + 1 == T.nq) ? 0 : qi + 1) {
             const uint32_t s = n % C::LSLOT;
             // The diagonal block: query column c sees this key only if c >= rl.
-            const bool diag = CAUSAL && (T.q0 + i % T.nq == T.kb);
+            const bool diag = CAUSAL && (T.q0 + (G ? qi : i) == T.kb);
             if (!mbar_wait(smem_u32(&c.s_full), n & 1, ab, err, kErrSoftmax)) return;
             // -lse2 and -D of this step's query block, staged by the producer warp.
             if (!mbar_wait(smem_u32(&c.ls_full[s]), (n / C::LSLOT) & 1, ab, err, kErrSoftmax)) return;
@@ -535,7 +542,7 @@ __device__ void kv_softmax(const BParams &p, KCtl<D> &c, uint32_t tmem, int warp
     }
 }
 
-template <int D, bool CAUSAL, int DT>
+template <int D, bool CAUSAL, int DT, bool G>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -595,11 +602,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = ctl.tmem_base;
     if (warp < 8)
-        kv_softmax<D, CAUSAL, DT>(p, ctl, tmem, warp, lane);
+        kv_softmax<D, CAUSAL, DT, G>(p, ctl, tmem, warp, lane);
     else if (warp == 8)
-        kv_producer<D, CAUSAL, DT>(p, ctl, &tm_q, &tm_k, &tm_v, &tm_do, sK, sV, sQ, sO, lane);
+        kv_producer<D, CAUSAL, DT, G>(p, ctl, &tm_q, &tm_k, &tm_v, &tm_do, sK, sV, sQ, sO, lane);
     else
-        kv_mma<D, CAUSAL, DT>(p, ctl, tmem, sK, sV, sQ, sO);
+        kv_mma<D, CAUSAL, DT, G>(p, ctl, tmem, sK, sV, sQ, sO);
     tc_fence_before();
     __syncthreads();
     if (warp == 9) {
@@ -993,8 +1000,12 @@ clis_status_t launch_impl(const AttnBwdArgs &a, cudaStream_t stream)
     const int kv_need = C::KV_TILES + static_cast<int>(sizeof(KCtl<D>));
     if (kv_need > optin) return CLIS_ERR_UNSUPPORTED;
     const int kv_smem = kv_need + 1023 < optin ? kv_need + 1023 : optin;
-    if (cudaFuncSetAttribute(bwd_dkdv_kernel<D, CAUSAL, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kv_smem) != cudaSuccess ||
+    // K and V broadcast over the heads (head stride 0): one key/value head per
+    // batch entry, shared by all H query heads (grouped-query attention folded
+    // into the batch); the dK/dV kernel built for it sums each group.
+    const bool grouped = a.H > 1 && a.k_sh == 0 && a.v_sh == 0;
+    if (cudaFuncSetAttribute(grouped ? bwd_dkdv_kernel<D, CAUSAL, DT, true> : bwd_dkdv_kernel<D, CAUSAL, DT, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kv_smem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_dq_kernel<D, CAUSAL, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::Q_SMEM) != cudaSuccess)
         return CLIS_ERR_CUDA;
@@ -1039,9 +1050,7 @@ clis_status_t launch_impl(const AttnBwdArgs &a, cudaStream_t stream)
     p.scale_log2 = a.scale_log2;
     p.scale = a.scale_log2 * 0.693147180559945309f;
     const int BH = a.B * a.H;
-    // K and V broadcast over the heads (head stride 0): one key/value head per
-    // batch entry, shared by all H query heads.
-    p.kvg = (a.H > 1 && a.k_sh == 0 && a.v_sh == 0) ? a.H : 1;
+    p.kvg = grouped ? a.H : 1;
     const int KVH = BH / p.kvg;
 
     // dK, dV: one work tile per (key/value head, key block).
@@ -1050,7 +1059,10 @@ clis_status_t launch_impl(const AttnBwdArgs &a, cudaStream_t stream)
     p.grp = p.grp > KVH ? KVH : (p.grp < 1 ? 1 : p.grp);
     int grid = p.num_tiles < nsm ? p.num_tiles : nsm;
     p.smem_bytes = kv_smem;
-    bwd_dkdv_kernel<D, CAUSAL, DT><<<grid, kThreads, kv_smem, stream>>>(mq, mk, mv, mdo, p);
+    if (grouped)
+        bwd_dkdv_kernel<D, CAUSAL, DT, true><<<grid, kThreads, kv_smem, stream>>>(mq, mk, mv, mdo, p);
+    else
+        bwd_dkdv_kernel<D, CAUSAL, DT, false><<<grid, kThreads, kv_smem, stream>>>(mq, mk, mv, mdo, p);
     if (cudaGetLastError() != cudaSuccess) return CLIS_ERR_CUDA;
 
     // dQ: one work tile per (head, query block).
