@@ -58,11 +58,12 @@ def parse():
     ap.add_argument("--variant", default="auto", choices=["auto", "online", "certified", "online_lazy"])
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"],
                     help="element type of Q, K, V, P and O (fp16 certifies with the FP16 exp2 budget)")
-    ap.add_argument("--extras", default="all", choices=["all", "none", "backward", "chunks", "e2e", "tiles", "fp8"],
+    ap.add_argument("--extras", default="all", choices=["all", "none", "backward", "chunks", "e2e", "tiles", "fp8", "gqa"],
                     help="legs after the headline step: all (online variants, ring-step chunks, backward, e2e, "
                          "CPU baseline, per-prefix certificates for causal configs, FP8 P.V for non-causal BF16 "
+                         "configs, grouped-query attention with a quarter of the key/value heads for causal "
                          "configs), none, or only the backward, the ring-step chunks, the e2e leg, the per-prefix "
-                         "leg or the FP8 P.V leg (profiling runs)")
+                         "leg, the FP8 P.V leg or the grouped-query leg (profiling runs)")
     ap.add_argument("--no-extras", action="store_true", help="same as --extras none")
     return ap.parse_args()
 
@@ -547,6 +548,52 @@ def main():
                             "launches_per_step": 3, "flops": "five matmuls (2.5x the forward's count)",
                             "fwd_plus_bwd_ms": attn_avg_ms + cert_avg_ms + bwd_ms}
         del dout, dq, dk, dv, bws, lse2
+    if extras in ("all", "gqa") and w.causal and heads % (4 * w.B) == 0:
+        # Grouped-query attention (the LLM training shape with one key/value head
+        # per four query heads): Q as the headline's, K and V the first quarter of
+        # the heads of each batch entry, shared through zero head strides.
+        # Certification + forward, and the backward (whose dK/dV kernel sums each
+        # group), on the same FLOP counts as the headline.
+        hkv = heads // w.B // 4
+        kg, vg = k[:, :hkv].contiguous(), v[:, :hkv].contiguous()
+        qf, kf, vf, of = clis.grouped_query_views(q, kg, vg, out)
+        lse2 = torch.empty(heads * w.N, dtype=torch.float32, device=dev)
+        dout = make_dout(q.shape, device=dev, dtype=dt)
+        dq, dkg, dvg = torch.empty_like(q), torch.empty_like(kg), torch.empty_like(vg)
+        dqf, dkf, dvf, dof = clis.grouped_query_views(dq, dkg, dvg, dout)
+        gws = torch.empty(max(256, clis.clis_certify_workspace_size(clis.make_shape(qf, kf, vf))), dtype=torch.uint8,
+                          device=dev)
+        bws = torch.empty(max(256, clis.clis_attn_bwd_workspace_size(clis.make_shape(qf, kf, vf, of))),
+                          dtype=torch.uint8, device=dev)
+
+        def gqa_fwd():
+            clis.clis_certify(qf, kf, vf, sl2, kbar=kbar, certs=certs, workspace=gws, mu=mu, exp_fmt=exp_fmt)
+            clis.clis_attn_fwd(qf, kf, vf, sl2, kbar=kbar, certs=certs, causal=True, variant=args.variant, out=of,
+                               mu=mu, lse2=lse2)
+
+        def gqa_bwd():
+            clis.clis_attn_bwd(qf, kf, vf, of, dof, lse2, sl2, causal=True, dq=dqf, dk=dkf, dv=dvf, workspace=bws)
+
+        res = {}
+        for name, fn in (("forward", gqa_fwd), ("backward", gqa_bwd)):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for e0, e1 in gev:
+                if flush_buf is not None:
+                    flush_buf.zero_()
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in gev)
+            mult = 2.5 if name == "backward" else 1.0
+            res[name] = {"value": mult * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms": ms}
+        line["grouped_query"] = {"kv_heads_per_batch": hkv, "query_heads_per_kv_head": 4,
+                                 "forward_step": res["forward"], "backward": res["backward"]}
+        del kg, vg, lse2, dout, dq, dkg, dvg, gws, bws
     if rank == 0 and ws == 1 and extras == "all":
         # CPU baseline: the oracle on a bounded sample of this workload.
         import oracle
