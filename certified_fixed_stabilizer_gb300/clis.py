@@ -524,13 +524,15 @@ def grouped_query_views(q, k, v, out=None):
 
 def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
               variant: str = "auto", return_certs: bool = False, device=None, out=None,
-              groups: int = 8, non_blocking: bool = False, pv: str = "bf16"):
+              groups: int | None = None, non_blocking: bool = False, pv: str = "bf16"):
     """CLiS attention forward: certification pre-pass, then the fused kernel.
 
     q, k, v: bf16 or fp16 [B, H, N, d].  Device tensors are processed in place
     on the current stream.  Host tensors (pinned for overlap) are copied to
     ``device`` (default cuda:0) and the result is written to ``out`` (a host
-    tensor, allocated if None): heads are processed in ``groups`` groups, with
+    tensor, allocated if None): heads are processed in ``groups`` groups (by
+    default about one group per 2 TFLOP of attention work, at least 8, at most
+    one per head), with
     copies in and out on two streams and the kernels on two more (alternating
     groups), so that the copies of one group overlap the compute of another
     and one group's kernel can start on SMs the previous one has left idle
@@ -631,7 +633,13 @@ def _attention_host(q, k, v, softmax_scale, causal, variant, return_certs, dev, 
             torch.cuda.synchronize(dev)  # the old buffers may still be in use
         pl = _pipelines[dev] = _HostPipeline(q, k, dev, certified)
         pl.key = key
-    # head groups: contiguous (b, h0:h1) slices, about `groups` of them in total
+    # head groups: contiguous (b, h0:h1) slices, about `groups` of them in total.
+    # By default a group holds about 2 TFLOP of work (~1.2 ms): many small groups
+    # leave only a small first copy-in and last copy-out exposed, and two
+    # compute streams hide each launch's tail behind the next one.
+    if groups is None:
+        work = 4.0 * B * H * Nq * k.shape[2] * d / (2.0 if causal else 1.0)
+        groups = min(B * H, max(8, int(work / 2e12)))
     per = max(1, -(-B * H // max(1, groups)))
     spans = []
     for b in range(B):
