@@ -133,3 +133,30 @@ def test_grouped_query_autograd():
     o.float().sum().backward()
     assert q.grad.shape == q.shape and k.grad.shape == k.shape and v.grad.shape == v.shape
     assert all(torch.isfinite(t.grad.float()).all() for t in (q, k, v))
+
+
+def test_grouped_query_fp8pv_and_chunks_match_repeated_layout():
+    """The FP8 P.V path and the ring-step chunk form read broadcast K/V like
+    the forward: bit-identical to the same calls on materialised repeats."""
+    B, H, Hkv, N, d = 1, 4, 1, 4608, 128
+    q, k, v = _inputs(B, H, Hkv, N, d, False, seed=23)
+    krep, vrep = (t.repeat_interleave(H // Hkv, dim=1).contiguous() for t in (k, v))
+    o8 = clis.attention(q, k, v, pv="fp8")
+    o8r = clis.attention(q, krep, vrep, pv="fp8")
+    torch.cuda.synchronize()
+    assert torch.equal(o8, o8r)
+    qf, kf, vf, _ = clis.grouped_query_views(q, k, v)
+    sl2 = clis.scale_log2_for(d)
+    outs = []
+    for kk, vv, qq in ((kf, vf, qf), (krep.view(B * Hkv, H // Hkv, N, d), vrep.view(B * Hkv, H // Hkv, N, d), qf)):
+        mu = torch.empty(B * H * N, device=q.device)
+        kbar, certs = clis.clis_certify(qq, kk, vv, sl2, mu=mu)
+        o_acc = torch.empty((B * H * N, d), device=q.device)
+        l_acc = torch.empty(B * H * N, device=q.device)
+        m_acc = torch.empty(B * H * N, device=q.device)
+        for i, (a, b) in enumerate(((0, 2048), (2048, N))):
+            clis.clis_attn_fwd_chunk(qq, kk[:, :, a:b], vv[:, :, a:b], sl2, o_acc, l_acc, m_acc, kbar=kbar,
+                                     certs=certs, first=(i == 0), mu=mu)
+        outs.append(clis.clis_attn_chunk_finalize(qq, o_acc, l_acc, m_acc))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
