@@ -476,8 +476,10 @@ def main():
 
         def chunk_pass(variant):
             for i, (a, b) in enumerate(zip(bounds[:-1], bounds[1:])):
-                if variant == "fp8":
+                if variant == "fp8" and b - a >= 4096:
                     # FP8 P.V: each chunk's V converted to E4M3 as it arrives, then merged.
+                    # (A chunk under 4096 keys runs BF16 on every head, so it is merged
+                    # as in the certified pass, without a conversion.)
                     kc, vc = k[:, :, a:b], v[:, :, a:b]
                     clis.clis_v_to_e4m3(vc, vt8s[i])
                     clis.clis_attn_fwd_chunk_fp8pv(q, kc, vc, vt8s[i], sl2, o_acc, l_acc, m_acc, kbar=kbar,
@@ -488,7 +490,8 @@ def main():
                                                     mu=mu)
                 else:
                     clis.clis_attn_fwd_chunk(q, k[:, :, a:b], v[:, :, a:b], sl2, o_acc, l_acc, m_acc,
-                                             kbar=kbar, certs=certs, first=(i == 0), variant=variant, mu=mu)
+                                             kbar=kbar, certs=certs, first=(i == 0),
+                                             variant="auto" if variant == "fp8" else variant, mu=mu)
             clis.clis_attn_chunk_finalize(q, o_acc, l_acc, m_acc, out=out)
 
         chunked = {"chunks": n_chunks, "causal": w.causal}
