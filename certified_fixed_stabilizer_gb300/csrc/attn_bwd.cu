@@ -24,6 +24,9 @@
 //                      shared memory while the query blocks stream past:
 //                        S^T = K Q^T, dP^T = V dO^T          (SMEM x SMEM)
 //                        dV += P^T dO, dK += dS^T Q          (P^T, dS^T from TMEM)
+//                      (when K and V are shared by all the heads of a batch entry,
+//                      zero head stride, the query blocks of every one of those
+//                      heads stream past in turn, so dK and dV sum the group)
 //   bwd_dq_kernel      persistent; a work tile is 128 queries of one head:
 //                        S = Q K^T, dP = dO V^T, dQ += dS K
 // Splitting dQ from dK/dV recomputes S and dP once more (7 matmuls per
