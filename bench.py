@@ -360,8 +360,9 @@ def main():
         # (Timed right after the headline step, in the same thermal and power
         # state, before the other legs heat the chip.)
         # End to end through the public call (clis.attention) with pinned host
-        # buffers: every step copies Q, K, V in, computes and copies O out; the
-        # call pipelines head groups over a copy-in, two compute and a copy-out stream.
+        # buffers, which marshals them to the C ABI's clis_attention_host: every
+        # step copies Q, K, V in, computes and copies O out, the library
+        # pipelining head groups over a copy-in, two compute and a copy-out stream.
         qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
         oh = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
 
@@ -385,7 +386,7 @@ def main():
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, ws)
         line["e2e"] = {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                        "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out.numel() * out.element_size(),
-                       "ms_per_step": e2e_ms, "api": "certified_fixed_stabilizer_gb300.clis.attention",
+                       "ms_per_step": e2e_ms, "api": "certified_fixed_stabilizer_gb300.clis.attention -> clis_attention_host (C ABI, host buffers)",
                        "clocks": cs_e2e.summary()}
         del qh, kh, vh, oh
     if extras == "all":

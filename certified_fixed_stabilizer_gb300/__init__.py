@@ -20,7 +20,8 @@ _BINDING_NAMES = {
     "Shape", "CERT_WORDS", "LOG2E", "clis_debug_wait_selftest", "clis_attn_fwd_chunk", "clis_attn_fwd_chunk_causal",
     "clis_attn_chunk_finalize", "clis_v_e4m3_size", "clis_v_to_e4m3", "clis_attn_fwd_fp8pv", "clis_attn_fwd_chunk_fp8pv",
     "clis_attn_bwd", "clis_attn_bwd_workspace_size", "attention_bwd", "attention_fwd_lse", "attention_autograd",
-    "AttentionFunction", "host_done_event", "grouped_query_views",
+    "AttentionFunction", "host_done_event", "grouped_query_views", "clis_attention_host",
+    "HostPlan",
 }
 
 

@@ -19,7 +19,7 @@ OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libclis.so")
 OBJ_DIR = os.path.join(HERE, "_build")
 
-SOURCES = ["clis_api.cu", "certify.cu", "attn_fwd.cu", "attn_bwd.cu"]
+SOURCES = ["clis_api.cu", "certify.cu", "attn_fwd.cu", "attn_bwd.cu", "host_attention.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xcompiler", "-fvisibility=hidden"]

@@ -102,6 +102,16 @@ def load_library():
     lib.clis_attn_bwd_workspace_size.restype = i32
     lib.clis_attn_bwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, vp, sz, vp]
     lib.clis_attn_bwd.restype = i32
+    lib.clis_host_plan_create.argtypes = [sp, i32, i32, ctypes.POINTER(vp)]
+    lib.clis_host_plan_create.restype = i32
+    lib.clis_host_plan_workspace_size.argtypes = [vp, ctypes.POINTER(sz)]
+    lib.clis_host_plan_workspace_size.restype = i32
+    lib.clis_attention_host.argtypes = [vp, vp, vp, vp, vp, f32, i32, vp, sz, vp]
+    lib.clis_attention_host.restype = i32
+    lib.clis_host_plan_wait.argtypes = [vp, vp]
+    lib.clis_host_plan_wait.restype = i32
+    lib.clis_host_plan_destroy.argtypes = [vp]
+    lib.clis_host_plan_destroy.restype = i32
     _lib = lib
     return lib
 
@@ -528,22 +538,23 @@ def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
     """CLiS attention forward: certification pre-pass, then the fused kernel.
 
     q, k, v: bf16 or fp16 [B, H, N, d].  Device tensors are processed in place
-    on the current stream.  Host tensors (pinned for overlap) are copied to
-    ``device`` (default cuda:0) and the result is written to ``out`` (a host
-    tensor, allocated if None): heads are processed in ``groups`` groups (by
-    default about one group per 2 TFLOP of attention work, at least 8, at most
-    one per head), with
-    copies in and out on two streams and the kernels on two more (alternating
-    groups), so that the copies of one group overlap the compute of another
-    and one group's kernel can start on SMs the previous one has left idle
-    (heads are independent).  The input copies follow the work already queued
-    on the current stream.  The call returns once ``out`` is filled, unless
-    ``non_blocking``: then it returns after queueing, and the caller waits for
-    :func:`host_done_event` (or synchronises the device) before reading
-    ``out`` or changing q, k, v.  The device staging buffers and streams are
-    kept for the next call with the same shapes (one set per device), so
-    consecutive non-blocking calls overlap: a call's copies of a head group
-    start as soon as the previous call's kernels on that group are done.
+    on the current stream.  Host tensors (pinned for overlap) go through the
+    library's clis_attention_host on ``device`` (default cuda:0), which writes
+    the result to ``out`` (a contiguous host tensor, allocated if None): heads
+    are processed in ``groups`` groups (by default about one group per 2 TFLOP
+    of attention work, at least 8, at most one per head), with copies in and
+    out on two streams of the library's and the kernels on two more
+    (alternating groups), so that the copies of one group overlap the compute
+    of another and one group's kernel can start on SMs the previous one has
+    left idle (heads are independent).  The input copies follow the work
+    already queued on the current stream.  The call returns once ``out`` is
+    filled, unless ``non_blocking``: then it returns after queueing, and the
+    caller waits for :func:`host_done_event` (or synchronises the device)
+    before reading ``out`` or changing q, k, v.  The plan (streams, events)
+    and its device workspace (staging for every head) are kept for the next
+    call with the same shapes, so consecutive non-blocking calls overlap: a
+    call's copies of a head group start as soon as the previous call's
+    kernels on that group are done.
 
     ``pv="fp8"`` (device tensors, bf16, d = 128, no mask, variant "auto" or
     "certified") runs the FP8 P.V path: V's E4M3 transpose, then
@@ -592,120 +603,99 @@ def attention(q, k, v, softmax_scale: float | None = None, causal: bool = False,
     return res
 
 
-class _HostPipeline:
-    """Device staging buffers, streams and per-group events of the host-tensor
-    path, kept across calls with the same shapes (allocated once, so no call
-    waits on an allocation; the next call's copies of a head group start as
-    soon as the previous call's kernels on that group have read their inputs).
+class HostPlan:
+    """A clis_host_plan_t (streams and per-group events of the host-memory
+    forward for one shape on one device) with its device workspace."""
 
-    Per group g: copy-in (stream s_in) waits until the previous call's kernels
-    on g finished (ev_run[g]); the kernels (one of two compute streams,
-    alternating by group) wait for the copy-in and for the previous call's
-    copy-out of g (ev_out[g]), so the output slice is free; the copy-out
-    (stream s_out) waits for the kernels."""
+    def __init__(self, q, k, v, out, causal: bool = False, groups: int = 0, device=None):
+        lib = load_library()
+        self.device = torch.device(device or "cuda:0")
+        self.shape = make_shape(q, k, v, out)
+        self.handle = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            st = lib.clis_host_plan_create(ctypes.byref(self.shape), int(bool(causal)), int(groups),
+                                           ctypes.byref(self.handle))
+            if st != 0:
+                raise ClisError("clis_host_plan_create", st)
+            n = ctypes.c_size_t(0)
+            st = lib.clis_host_plan_workspace_size(self.handle, ctypes.byref(n))
+            if st != 0:
+                raise ClisError("clis_host_plan_workspace_size", st)
+            self.workspace = torch.empty(max(n.value, 256), dtype=torch.uint8, device=self.device)
+            self.side = torch.cuda.Stream(device=self.device)  # records the completion events
 
-    def __init__(self, q, k, dev, certified):
-        B, H, Nq, d = q.shape
-        self.key = None
-        self.qd = torch.empty(q.shape, dtype=q.dtype, device=dev)
-        self.kd = torch.empty(k.shape, dtype=k.dtype, device=dev)
-        self.vd = torch.empty(k.shape, dtype=k.dtype, device=dev)
-        self.od = torch.empty(q.shape, dtype=q.dtype, device=dev)
-        self.kbar = torch.empty((B * H, d), dtype=torch.float32, device=dev) if certified else None
-        self.certs = torch.empty((B * H, CERT_WORDS), dtype=torch.int32, device=dev) if certified else None
-        self.mu = torch.empty(B * H * Nq, dtype=torch.float32, device=dev) if certified else None
-        self.s_in, self.s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-        self.s_runs = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
-        self.ev_run, self.ev_out = {}, {}
-        self.ev_consumed = None  # the caller's copies of kbar / certs (return_certs)
-        self.ev_done = None      # after the last output copy of the latest call
+    def wait(self, stream=None) -> None:
+        """clis_host_plan_wait: ``stream`` waits for the latest call's last copy out."""
+        st = load_library().clis_host_plan_wait(self.handle, _stream(stream))
+        if st != 0:
+            raise ClisError("clis_host_plan_wait", st)
+
+    def destroy(self) -> None:
+        if self.handle:
+            load_library().clis_host_plan_destroy(self.handle)
+            self.handle = ctypes.c_void_p()
 
 
-_pipelines: dict = {}
+def clis_attention_host(plan: HostPlan, q, k, v, out, scale_log2: float, variant: str = "auto", stream=None):
+    """One forward of host tensors q, k, v into out (dense [B, H, N, d], the
+    plan's shape; pinned for asynchronous copies) with ``plan``: copies in,
+    certification, attention and copies out pipelined over head groups inside
+    the library.  Queued, not waited for: ``plan.wait(stream)`` orders a
+    stream after it."""
+    st = load_library().clis_attention_host(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), float(scale_log2),
+                                            VARIANT[variant], _ptr(plan.workspace), plan.workspace.numel(),
+                                            _stream(stream))
+    if st != 0:
+        raise ClisError("clis_attention_host", st)
+    return out
+
+
+# Per device: the plan of the host-tensor path (kept for the next call with
+# the same shapes, so that consecutive calls overlap) and the event after the
+# latest call's last output copy.
+_host_plans: dict = {}
+_host_done: dict = {}
 
 
 def _attention_host(q, k, v, softmax_scale, causal, variant, return_certs, dev, out, groups, non_blocking):
+    q, k, v = (t.contiguous() for t in (q, k, v))
     B, H, Nq, d = q.shape
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned())
+    elif not out.is_contiguous():
+        raise ValueError("out must be a contiguous host tensor")
     sl2 = scale_log2_for(d, softmax_scale)
-    certified = variant in ("auto", "certified")
-    key = (dev, tuple(q.shape), tuple(k.shape), q.dtype, certified, groups)
-    pl = _pipelines.get(dev)
-    if pl is None or pl.key != key:
-        if pl is not None:
-            torch.cuda.synchronize(dev)  # the old buffers may still be in use
-        pl = _pipelines[dev] = _HostPipeline(q, k, dev, certified)
-        pl.key = key
-    # head groups: contiguous (b, h0:h1) slices, about `groups` of them in total.
-    # By default a group holds about 2 TFLOP of work (~1.2 ms): many small groups
-    # leave only a small first copy-in and last copy-out exposed, and two
-    # compute streams hide each launch's tail behind the next one.
-    if groups is None:
-        work = 4.0 * B * H * Nq * k.shape[2] * d / (2.0 if causal else 1.0)
-        groups = min(B * H, max(8, int(work / 2e12)))
-    per = max(1, -(-B * H // max(1, groups)))
-    spans = []
-    for b in range(B):
-        for h0 in range(0, H, per):
-            spans.append((b, h0, min(H, h0 + per)))
-    cur = torch.cuda.current_stream(dev)
-    # The copies of the inputs follow whatever the caller queued on its stream
-    # before this call (for instance the copies that fill the host inputs).
-    ev_entry = torch.cuda.Event()
-    ev_entry.record(cur)
-    pl.s_in.wait_event(ev_entry)
-    if pl.ev_consumed is not None:
-        for s_run in pl.s_runs:
-            s_run.wait_event(pl.ev_consumed)
-        pl.ev_consumed = None
-    for gi, (b, h0, h1) in enumerate(spans):
-        s_run = pl.s_runs[gi % 2]
-        sl = (slice(b, b + 1), slice(h0, h1))
-        ev_in = torch.cuda.Event()
-        with torch.cuda.stream(pl.s_in):
-            if gi in pl.ev_run:
-                pl.s_in.wait_event(pl.ev_run[gi])
-            pl.qd[sl].copy_(q[sl], non_blocking=True)
-            pl.kd[sl].copy_(k[sl], non_blocking=True)
-            pl.vd[sl].copy_(v[sl], non_blocking=True)
-            ev_in.record(pl.s_in)
-        s_run.wait_event(ev_in)
-        if gi in pl.ev_out:
-            s_run.wait_event(pl.ev_out[gi])
-        f0, f1 = b * H + h0, b * H + h1
-        ev_run = pl.ev_run[gi] = torch.cuda.Event()
-        with torch.cuda.stream(s_run):
-            kb = cs = m = None
-            if certified:
-                kb, cs, m = pl.kbar[f0:f1], pl.certs[f0:f1], pl.mu[f0 * Nq:f1 * Nq]
-                clis_certify(pl.qd[sl], pl.kd[sl], pl.vd[sl], sl2, kbar=kb, certs=cs, mu=m, exp_fmt=_exp_fmt(q),
-                             stream=s_run)
-            clis_attn_fwd(pl.qd[sl], pl.kd[sl], pl.vd[sl], sl2, kbar=kb, certs=cs, causal=causal, variant=variant,
-                          mu=m, out=pl.od[sl], stream=s_run)
-            ev_run.record(s_run)
-        pl.s_out.wait_event(ev_run)
-        ev_out = pl.ev_out[gi] = torch.cuda.Event()
-        with torch.cuda.stream(pl.s_out):
-            out[sl].copy_(pl.od[sl], non_blocking=True)
-            ev_out.record(pl.s_out)
-    # Done once the last output copy is: host_done_event() returns this event.
-    # (The caller's stream is not made to wait for it, so that its next call's
-    # copies can start while this call's last groups still run.)
-    pl.ev_done = torch.cuda.Event()
-    pl.ev_done.record(pl.s_out)
+    g = 0 if groups is None else int(groups)
+    key = (tuple(q.shape), tuple(k.shape), q.dtype, bool(causal), g)
+    with torch.cuda.device(dev):
+        plan = _host_plans.get(dev)
+        if plan is None or plan.key != key:
+            if plan is not None:
+                torch.cuda.synchronize(dev)  # the old workspace may still be in use
+                plan.destroy()
+            plan = _host_plans[dev] = HostPlan(q, k, v, out, causal, g, dev)
+            plan.key = key
+        cur = torch.cuda.current_stream(dev)
+        clis_attention_host(plan, q, k, v, out, sl2, variant, stream=cur)
+        # The caller's stream is not made to wait, so that its next call's copies
+        # can start while this call's last groups still run.
+        plan.wait(plan.side)
+        done = _host_done[dev] = torch.cuda.Event()
+        done.record(plan.side)
+        kbar = certs = None
+        if return_certs and variant in ("auto", "certified") and B * H > 0 and Nq > 0:
+            # k-bar at the start of the workspace, the certificates at the next
+            # multiple of 256 bytes (include/clis.h), copied on the caller's
+            # stream once every kernel of the call has run.
+            plan.wait(cur)
+            BH, ws = B * H, plan.workspace
+            nk = BH * d * 4
+            off = (nk + 255) // 256 * 256
+            kbar = ws[:nk].view(torch.float32).view(BH, d).clone()
+            certs = ws[off:off + BH * CERT_WORDS * 4].view(torch.int32).view(BH, CERT_WORDS).clone()
     if not non_blocking:
-        pl.s_out.synchronize()
+        done.synchronize()
     if return_certs:
-        kbar, certs = pl.kbar, pl.certs
-        if certified:
-            # Copies on the caller's stream, after every kernel above; the next
-            # call's kernels wait for them before reusing the buffers.
-            for s_run in pl.s_runs:
-                cur.wait_stream(s_run)
-            kbar, certs = kbar.clone(), certs.clone()
-            pl.ev_consumed = torch.cuda.Event()
-            pl.ev_consumed.record(cur)
         return out, kbar, certs
     return out
 
@@ -715,8 +705,7 @@ def host_done_event(device=None):
     attention() call on ``device`` (default cuda:0), or None: a stream that
     waits for it (``stream.wait_event(...)``) is ordered after that call's
     output, and ``.synchronize()`` waits for it on the host."""
-    pl = _pipelines.get(torch.device(device or "cuda:0"))
-    return None if pl is None else pl.ev_done
+    return _host_done.get(torch.device(device or "cuda:0"))
 
 
 load_library()

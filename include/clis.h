@@ -225,6 +225,68 @@ CLIS_API clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, c
                             const clis_head_cert_t *certs, const float *mu, float scale_log2,
                             int causal, clis_variant_t variant, clis_stream_t stream);
 
+/* The forward for Q, K, V and O held in host memory (the abstract's
+ * plug-and-play use: the attention call of a model whose tensors live on the
+ * host).  Per group of consecutive heads: copy Q, K, V to the device, run
+ * clis_certify (variants CLIS_AUTO and CLIS_CERTIFIED_FORCED; exp2 format of
+ * the data type, FP32 accumulation) and clis_attn_fwd with its stabilisers,
+ * copy O back.  The copies of one group overlap the kernels of others: copies
+ * in on one stream of the plan, the kernels of even and odd groups on two
+ * more, copies out on a fourth.  Each head is computed alone by the kernels
+ * of clis_certify and clis_attn_fwd, so k-bar and the certificates equal
+ * theirs on the whole tensors bit for bit; O may differ from their O by
+ * rounding, because the attention kernel sweeps the keys of some work tiles
+ * in reverse order depending on where the tile falls in its launch.
+ *
+ * clis_host_plan_create: a plan for one shape on the current device: its
+ *   four streams and per-group events.  shape is as for clis_attn_fwd, but
+ *   Q, K, V and O must be dense (n-stride d, head stride N*d, batch stride
+ *   H*N*d, free when B = 1; CLIS_ERR_UNSUPPORTED otherwise); causal as for
+ *   clis_attn_fwd; groups = number of head groups, 0 = about one group per
+ *   2 TFLOP of attention work, at least 8 and at most B*H.  Argument errors
+ *   as for clis_attn_fwd; CLIS_ERR_CUDA if a stream or event cannot be made.
+ * clis_host_plan_workspace_size: bytes of device workspace every call with
+ *   the plan needs: staging for Q, K, V and O of every head, k-bar,
+ *   certificates and stabilisers, and two certification scratch areas (0 when
+ *   B*H = 0 or Nq = 0).
+ * clis_attention_host: one forward with the plan.
+ *   q, k, v, o  host memory, any alignment; o is written.  Page-locked memory
+ *               (cudaHostAlloc, cudaHostRegister) lets the copies run
+ *               asynchronously; with pageable memory the CUDA runtime stages
+ *               each copy and the call returns only after its copies ran.
+ *   scale_log2, variant  as for clis_attn_fwd
+ *   workspace   device memory of clis_host_plan_workspace_size() bytes,
+ *               256-byte aligned, the same for every call with the plan.  Once
+ *               the call is complete, its first B*H*d floats hold k-bar and the
+ *               B*H certificates start at the next multiple of 256 bytes
+ *               (certified variants).
+ *   stream      the copies in follow the work queued on it before the call
+ *   The call is queued, not waited for.  Consecutive calls with one plan
+ *   overlap: a call's copies of a group start once the previous call's
+ *   kernels on that group have run, and its kernels once the previous call's
+ *   copy out of that group has.  Must be called on the plan's device
+ *   (CLIS_ERR_INVALID_ARG otherwise).  Errors: the argument checks of
+ *   clis_attn_fwd, CLIS_ERR_WORKSPACE, CLIS_ERR_MISALIGNED for the
+ *   workspace, all before anything is queued; CLIS_ERR_CUDA when a copy or
+ *   launch fails, after which clis_host_plan_wait still covers everything the
+ *   call queued.  B*H = 0 or Nq = 0 returns CLIS_OK and queues nothing.
+ * clis_host_plan_wait: makes `stream` wait for the last copy out of the most
+ *   recent call with the plan (nothing if there was none): o of that call and
+ *   of every earlier one is complete once `stream` passes this point.
+ * clis_host_plan_destroy: releases the plan (NULL is a no-op); work already
+ *   queued still runs, and the CUDA runtime frees the streams and events
+ *   after it.  The workspace may be reused or freed once that work is done. */
+typedef struct clis_host_plan_s clis_host_plan_t;
+CLIS_API clis_status_t clis_host_plan_create(const clis_shape_t *shape, int causal, int groups,
+                                             clis_host_plan_t **plan);
+CLIS_API clis_status_t clis_host_plan_workspace_size(const clis_host_plan_t *plan, size_t *bytes);
+CLIS_API clis_status_t clis_attention_host(clis_host_plan_t *plan, const void *q, const void *k,
+                                           const void *v, void *o, float scale_log2,
+                                           clis_variant_t variant, void *workspace, size_t ws_bytes,
+                                           clis_stream_t stream);
+CLIS_API clis_status_t clis_host_plan_wait(clis_host_plan_t *plan, clis_stream_t stream);
+CLIS_API clis_status_t clis_host_plan_destroy(clis_host_plan_t *plan);
+
 /* FP8 P.V path.  Figure 3 tabulates exp2 limits per format; one step below
  * FP16 is E4M3 (largest finite value 448, so U_exp = log2 448 and the budget
  * is floor(U_exp) = 8).  One tcgen05.mma of kind::f8f6f4 takes both operands

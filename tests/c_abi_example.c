@@ -14,6 +14,10 @@
  *                   chunk offsets as key_offset), then clis_attn_chunk_finalize
  *          fp8      clis_certify + clis_v_to_e4m3 + clis_attn_fwd_fp8pv with
  *                   every head forced onto E4M3 P.V (no mask, d = 128)
+ *          host     clis_attention_host on page-locked host buffers with a
+ *                   plan of three head groups; the certificates come from the workspace
+ *                   (k-bar first, certificates at the next multiple of 256
+ *                   bytes) and lse2.bin holds NaN (this path has no lse2)
  * Exit status 0 on success; any CUDA or library error prints a message and
  * exits 1.
  */
@@ -111,10 +115,33 @@ int main(int argc, char **argv)
     const clis_stream_t cs = (clis_stream_t)stream;
     if (strcmp(mode, "noalloc") == 0)
         CLIS_OK_(clis_certify_noalloc(&s, q, k, v, scale_log2, CLIS_FMT_BF16, CLIS_FMT_FP32, kbar, certs, mu, cs));
-    else
+    else if (strcmp(mode, "host") != 0)
         CLIS_OK_(clis_certify(&s, q, k, v, scale_log2, CLIS_FMT_BF16, CLIS_FMT_FP32, kbar, certs, mu, ws, ws_bytes,
                               cs));
-    if (strcmp(mode, "fused") == 0 || strcmp(mode, "noalloc") == 0) {
+    if (strcmp(mode, "host") == 0) {
+        void *hbuf[4], *hws;
+        size_t hws_bytes = 0;
+        clis_host_plan_t *plan = NULL;
+        CLIS_OK_(clis_host_plan_create(&s, causal, 3, &plan));
+        CLIS_OK_(clis_host_plan_workspace_size(plan, &hws_bytes));
+        CUDA_OK(cudaMalloc(&hws, hws_bytes));
+        for (int t = 0; t < 4; t++) CUDA_OK(cudaMallocHost(&hbuf[t], bytes));
+        for (int t = 0; t < 3; t++)
+            if (!read_file(dir, names[t], hbuf[t], bytes)) return fail("read", names[t]);
+        CLIS_OK_(clis_attention_host(plan, hbuf[0], hbuf[1], hbuf[2], hbuf[3], scale_log2, CLIS_AUTO, hws, hws_bytes,
+                                     cs));
+        CLIS_OK_(clis_host_plan_wait(plan, cs));
+        CUDA_OK(cudaStreamSynchronize(stream));
+        CLIS_OK_(clis_host_plan_destroy(plan));
+        /* Through the device buffers, so the common code below writes the files. */
+        const size_t cert_off = ((size_t)(B * H * d) * sizeof(float) + 255) / 256 * 256;
+        CUDA_OK(cudaMemcpy(o, hbuf[3], bytes, cudaMemcpyHostToDevice));
+        CUDA_OK(cudaMemcpy(certs, (const char *)hws + cert_off, (size_t)(B * H) * sizeof(clis_head_cert_t),
+                           cudaMemcpyDeviceToDevice));
+        CUDA_OK(cudaMemset(lse2, 0xff, rows * sizeof(float)));
+        for (int t = 0; t < 4; t++) cudaFreeHost(hbuf[t]);
+        cudaFree(hws);
+    } else if (strcmp(mode, "fused") == 0 || strcmp(mode, "noalloc") == 0) {
         CLIS_OK_(clis_attn_fwd(&s, q, k, v, o, lse2, kbar, certs, mu, scale_log2, causal, CLIS_AUTO, cs));
     } else if (strcmp(mode, "chunks") == 0) {
         /* K/V in three chunks (the split points leave ragged tiles); fp32

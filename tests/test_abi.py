@@ -30,7 +30,8 @@ def test_header_declares_the_boundary():
               "clis_attn_fwd_chunk", "clis_attn_chunk_finalize", "clis_certify_noalloc",
               "clis_attn_bwd_workspace_size", "clis_attn_bwd", "clis_certify_tiles", "clis_attn_fwd_tiles",
               "clis_attn_fwd_chunk_causal", "clis_v_e4m3_size", "clis_v_to_e4m3", "clis_attn_fwd_fp8pv",
-              "clis_attn_fwd_chunk_fp8pv"):
+              "clis_attn_fwd_chunk_fp8pv", "clis_host_plan_create", "clis_host_plan_workspace_size",
+              "clis_attention_host", "clis_host_plan_wait", "clis_host_plan_destroy"):
         assert n in names
 
 
@@ -330,3 +331,56 @@ def test_binding_has_no_cpu_fallback(clis):
     src = open(os.path.join(ROOT, "certified_fixed_stabilizer_gb300", "clis.py")).read()
     assert "oracle" not in src
     assert "softmax" not in src.replace("softmax_scale", "")
+
+
+
+def _plan(clis, shape, causal=0, groups=0):
+    h = ctypes.c_void_p()
+    st = clis.load_library().clis_host_plan_create(ctypes.byref(shape) if shape is not None else None, causal,
+                                                   groups, ctypes.byref(h))
+    return st, h
+
+
+def test_host_plan_rejects_bad_arguments(clis):
+    """clis_host_plan_create checks everything before any CUDA call."""
+    lib = clis.load_library()
+    INVALID, UNSUP = 1, 2
+    assert lib.clis_host_plan_create(ctypes.byref(_shape(clis)), 0, 0, None) == INVALID
+    assert _plan(clis, None)[0] == INVALID
+    assert _plan(clis, _shape(clis), causal=2)[0] == INVALID
+    assert _plan(clis, _shape(clis), groups=-1)[0] == INVALID
+    assert _plan(clis, _shape(clis, Nk=0))[0] == INVALID
+    s = _shape(clis)
+    s.dtype = 5
+    assert _plan(clis, s)[0] == INVALID
+    assert _plan(clis, _shape(clis, d=96))[0] == UNSUP
+    assert _plan(clis, _shape(clis, Nq=300, Nk=400), causal=1)[0] == UNSUP
+    for field, val in (("k_sn", 136), ("q_sh", 300 * 128 + 8), ("o_sb", 0), ("v_sh", 0)):
+        s = _shape(clis, B=2)
+        setattr(s, field, val)
+        st, h = _plan(clis, s)
+        assert st == UNSUP and not h.value, field  # not dense
+    vp = ctypes.c_void_p
+    assert lib.clis_attention_host(None, vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 0.1, 0, vp(FAKE), 1 << 30,
+                                   None) == INVALID
+    assert lib.clis_host_plan_wait(None, None) == INVALID
+    assert lib.clis_host_plan_workspace_size(None, None) == INVALID
+    assert lib.clis_host_plan_destroy(None) == 0
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk", [(0, 3, 300, 300), (1, 2, 0, 5)])
+def test_host_plan_with_nothing_to_compute(clis, B, H, Nq, Nk):
+    """B*H = 0 or Nq = 0: a plan without streams (no CUDA call), a workspace of
+    0 bytes, calls that queue nothing; the scale and variant are still checked."""
+    lib = clis.load_library()
+    st, h = _plan(clis, _shape(clis, B=B, H=H, Nq=Nq, Nk=Nk))
+    assert st == 0 and h.value
+    n = ctypes.c_size_t(123)
+    assert lib.clis_host_plan_workspace_size(h, ctypes.byref(n)) == 0 and n.value == 0
+    vp = ctypes.c_void_p
+    assert lib.clis_attention_host(h, None, None, None, None, 0.1, 0, None, 0, None) == 0
+    assert lib.clis_attention_host(h, None, None, None, None, 0.0, 0, None, 0, None) == 1
+    assert lib.clis_attention_host(h, None, None, None, None, 0.1, 9, None, 0, None) == 1
+    assert lib.clis_host_plan_wait(h, None) == 0
+    assert lib.clis_host_plan_destroy(h) == 0
+    del vp

@@ -274,6 +274,50 @@ def test_host_path_back_to_back_non_blocking_calls():
     assert_close_to_oracle(outs[3].float().numpy().reshape(ref.shape), ref, "back-to-back last call")
 
 
+def test_host_plan_workspace_and_argument_checks():
+    """clis_host_plan_workspace_size covers staging for every head, k-bar,
+    certificates, stabilisers and two certification scratch areas; the
+    forward's pointer and workspace checks return their statuses (nothing is
+    queued); the certificates sit where include/clis.h says."""
+    import ctypes
+    dev = need_gpu()
+    B, H, N, d = 2, 3, 1000, 128
+    g = torch.Generator(device="cpu")
+    g.manual_seed(41)
+    q, k, v = (torch.randn(B, H, N, d, generator=g).to(torch.bfloat16).pin_memory() for _ in range(3))
+    o = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    plan = clis.HostPlan(q, k, v, o, groups=2, device=dev)
+    n = ctypes.c_size_t(0)
+    lib = clis.load_library()
+    assert lib.clis_host_plan_workspace_size(plan.handle, ctypes.byref(n)) == 0
+    n = n.value
+    per_group = clis.clis_certify_workspace_size(clis.make_shape(q[:1], k[:1], v[:1]))
+    assert n % 256 == 0 and n >= 4 * B * H * N * d * 2 + B * H * (d * 4 + 32 + N * 4) + 2 * per_group
+    vp, ws = ctypes.c_void_p, plan.workspace
+    args = [vp(t.data_ptr()) for t in (q, k, v, o)]
+    for i in range(4):
+        bad = list(args)
+        bad[i] = None
+        assert lib.clis_attention_host(plan.handle, *bad, 0.1, 0, vp(ws.data_ptr()), n, None) == 1
+    assert lib.clis_attention_host(plan.handle, *args, 0.1, 0, None, n, None) == 4
+    assert lib.clis_attention_host(plan.handle, *args, 0.1, 0, vp(ws.data_ptr()), n - 1, None) == 4
+    assert lib.clis_attention_host(plan.handle, *args, 0.1, 0, vp(ws.data_ptr() + 16), n, None) == 3
+    # A real call, then the certificates from the workspace against clis_certify.
+    clis.clis_attention_host(plan, q, k, v, o, clis.scale_log2_for(d))
+    plan.wait()
+    torch.cuda.synchronize()
+    off = (B * H * d * 4 + 255) // 256 * 256
+    certs = ws[off:off + B * H * clis.CERT_WORDS * 4].view(torch.int32).view(B * H, clis.CERT_WORDS)
+    kbar = ws[:B * H * d * 4].view(torch.float32).view(B * H, d)
+    dkbar, dcerts = clis.clis_certify(q.to(dev), k.to(dev), v.to(dev), clis.scale_log2_for(d))
+    torch.cuda.synchronize()
+    assert torch.equal(certs, dcerts) and torch.equal(kbar, dkbar)
+    ref = clis.attention(q.to(dev), k.to(dev), v.to(dev))
+    torch.cuda.synchronize()
+    assert_paths_agree(flat(o.to(dev)), flat(ref), "plan call")
+    plan.destroy()
+
+
 def test_host_path_follows_work_queued_on_the_current_stream():
     """Host inputs filled by asynchronous copies queued on the current stream
     (behind a long kernel) are read only after those copies: the call's input
