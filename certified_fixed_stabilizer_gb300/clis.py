@@ -635,6 +635,12 @@ class HostPlan:
             load_library().clis_host_plan_destroy(self.handle)
             self.handle = ctypes.c_void_p()
 
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:  # interpreter shutdown: the library may be gone already
+            pass
+
 
 def clis_attention_host(plan: HostPlan, q, k, v, out, scale_log2: float, variant: str = "auto", stream=None):
     """One forward of host tensors q, k, v into out (dense [B, H, N, d], the

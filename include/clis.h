@@ -261,7 +261,8 @@ CLIS_API clis_status_t clis_attn_fwd(const clis_shape_t *shape, const void *q, c
  *               B*H certificates start at the next multiple of 256 bytes
  *               (certified variants).
  *   stream      the copies in follow the work queued on it before the call
- *   The call is queued, not waited for.  Consecutive calls with one plan
+ *   The call is queued, not waited for.  Calls with one plan must come from
+ *   one host thread at a time (the plan records its events in each call).  Consecutive calls with one plan
  *   overlap: a call's copies of a group start once the previous call's
  *   kernels on that group have run, and its kernels once the previous call's
  *   copy out of that group has.  Must be called on the plan's device
