@@ -631,7 +631,11 @@ class HostPlan:
             raise ClisError("clis_host_plan_wait", st)
 
     def destroy(self) -> None:
+        """Waits for the plan's queued work (the workspace tensor is freed through
+        torch, which does not see the plan's streams), then releases the plan."""
         if self.handle:
+            self.wait(self.side)
+            self.side.synchronize()
             load_library().clis_host_plan_destroy(self.handle)
             self.handle = ctypes.c_void_p()
 
